@@ -1,0 +1,189 @@
+"""ctypes binding of libcpsa.so: argument marshalling only.
+
+Every function here has the name of the C entry point it calls (include/cpsa.h)
+and passes torch tensors as raw pointers plus sizes; all computation happens in
+the library's CUDA kernels. There is no fallback: when the library is missing
+or a call fails, an exception is raised.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libcpsa.so")
+
+_lib = None
+
+_c_i64 = ctypes.c_int64
+_c_int = ctypes.c_int
+_c_p = ctypes.c_void_p
+_c_f = ctypes.c_float
+_c_d = ctypes.c_double
+_c_size = ctypes.c_size_t
+
+# device error bits (mirrors include/cpsa.h)
+DEV_SLOT_OUT_OF_RANGE = 0x01
+DEV_PAGE_OUT_OF_RANGE = 0x02
+DEV_SEQ_LT_QUERY = 0x04
+DEV_TOKENS_MISMATCH = 0x08
+DEV_SEQ_GT_TABLE = 0x10
+DEV_SPLITS_CLAMPED = 0x20
+DEV_WAIT_TIMEOUT = 0x40
+
+
+class CpsaError(RuntimeError):
+    pass
+
+
+def load():
+    """Load libcpsa.so (built in-tree by __graft_entry__.build()); raises if absent."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    if not os.path.exists(LIB_PATH):
+        raise CpsaError(f"{LIB_PATH} is missing: build it first (python -c 'import __graft_entry__ as g; g.build()')")
+    lib = ctypes.CDLL(LIB_PATH)
+    lib.cpp_kv_cache_write.restype = _c_int
+    lib.cpp_kv_cache_write.argtypes = [_c_p, _c_p, _c_p, _c_i64, _c_int, _c_int, _c_int, _c_i64, _c_p, _c_p, _c_p, _c_p]
+    lib.cpp_attn_workspace_bytes.restype = _c_size
+    lib.cpp_attn_workspace_bytes.argtypes = [_c_int, _c_i64, _c_int, _c_int, _c_int, _c_int]
+    lib.cpp_attn_workspace_min_bytes.restype = _c_size
+    lib.cpp_attn_workspace_min_bytes.argtypes = [_c_int, _c_i64, _c_int, _c_int, _c_int, _c_int]
+    lib.cpp_chunked_prefill_attn.restype = _c_int
+    lib.cpp_chunked_prefill_attn.argtypes = [_c_p, _c_p, _c_p, _c_p, _c_p, _c_p, _c_int, _c_i64, _c_int, _c_int,
+                                             _c_int, _c_int, _c_int, _c_i64, _c_f, _c_int, _c_p, _c_p, _c_size,
+                                             _c_p, _c_p]
+    lib.cpp_split_microbatch.restype = _c_int
+    lib.cpp_split_microbatch.argtypes = [_c_p, _c_int, _c_f, ctypes.c_int32, _c_p, _c_p]
+    lib.cpp_read_device_error.restype = _c_int
+    lib.cpp_read_device_error.argtypes = [_c_p, _c_p, _c_int, _c_p]
+    lib.cpp_plan_chunk_sizes.restype = _c_int
+    lib.cpp_plan_chunk_sizes.argtypes = [_c_d, _c_d, _c_d, _c_i64, _c_i64, _c_int, _c_i64, _c_i64, _c_i64, _c_d,
+                                         _c_p, _c_i64, _c_p]
+    lib.cpp_fit_latency_quadratic.restype = _c_int
+    lib.cpp_fit_latency_quadratic.argtypes = [_c_p, _c_p, _c_int, _c_p]
+    lib.cpp_fit_latency_two_var.restype = _c_int
+    lib.cpp_fit_latency_two_var.argtypes = [_c_p, _c_p, _c_p, _c_p, _c_int, _c_p]
+    lib.cpp_status_string.restype = ctypes.c_char_p
+    lib.cpp_status_string.argtypes = [_c_int]
+    _lib = lib
+    return lib
+
+
+def _check(status: int, what: str):
+    if status != 0:
+        msg = load().cpp_status_string(status).decode()
+        raise CpsaError(f"{what} failed: {msg} ({status})")
+
+
+def _stream_ptr(stream):
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return _c_p(stream.cuda_stream)
+
+
+def _dev(t: torch.Tensor, dtype, name):
+    if not isinstance(t, torch.Tensor) or not t.is_cuda:
+        raise CpsaError(f"{name} must be a CUDA tensor")
+    if t.dtype != dtype:
+        raise CpsaError(f"{name} must be {dtype}, got {t.dtype}")
+    if not t.is_contiguous():
+        raise CpsaError(f"{name} must be contiguous")
+    return _c_p(t.data_ptr())
+
+
+def cpp_kv_cache_write(k, v, slot_mapping, k_cache, v_cache, dev_err, stream=None):
+    """k, v [T, Hkv, d] bf16; slot_mapping [T] int64; caches [pages, Hkv, P, d] bf16."""
+    T, Hkv, d = k.shape
+    pages, Hkv2, P, d2 = k_cache.shape
+    if v.shape != k.shape or v_cache.shape != k_cache.shape or Hkv2 != Hkv or d2 != d or slot_mapping.shape != (T,):
+        raise CpsaError("cpp_kv_cache_write: inconsistent shapes")
+    st = load().cpp_kv_cache_write(_dev(k, torch.bfloat16, "k"), _dev(v, torch.bfloat16, "v"),
+                                   _dev(slot_mapping, torch.int64, "slot_mapping"), T, Hkv, d, P, pages,
+                                   _dev(k_cache, torch.bfloat16, "k_cache"), _dev(v_cache, torch.bfloat16, "v_cache"),
+                                   _dev(dev_err, torch.int32, "dev_err"), _stream_ptr(stream))
+    _check(st, "cpp_kv_cache_write")
+
+
+def cpp_attn_workspace_bytes(num_reqs, num_tokens, num_q_heads, num_kv_heads, head_dim, max_kv_splits=8):
+    n = load().cpp_attn_workspace_bytes(num_reqs, num_tokens, num_q_heads, num_kv_heads, head_dim, max_kv_splits)
+    if n == 0:
+        raise CpsaError("cpp_attn_workspace_bytes: invalid arguments")
+    return int(n)
+
+
+def cpp_attn_workspace_min_bytes(num_reqs, num_tokens, num_q_heads, num_kv_heads, head_dim, max_kv_splits=8):
+    n = load().cpp_attn_workspace_min_bytes(num_reqs, num_tokens, num_q_heads, num_kv_heads, head_dim, max_kv_splits)
+    if n == 0:
+        raise CpsaError("cpp_attn_workspace_min_bytes: invalid arguments")
+    return int(n)
+
+
+def cpp_chunked_prefill_attn(q, k_cache, v_cache, query_lens, seq_lens, block_table, out, workspace, dev_err,
+                             scale=0.0, max_kv_splits=8, stream=None):
+    """q/out [T, Hq, d] bf16; caches [pages, Hkv, P, d] bf16; lens [B] int32; block_table [B, M] int32;
+    workspace uint8 of cpp_attn_workspace_*_bytes; dev_err int32 [1] (bit flags)."""
+    T, Hq, d = q.shape
+    pages, Hkv, P, d2 = k_cache.shape
+    B = query_lens.shape[0]
+    if out.shape != q.shape or v_cache.shape != k_cache.shape or d2 != d or seq_lens.shape != (B,) \
+            or block_table.dim() != 2 or block_table.shape[0] != B:
+        raise CpsaError("cpp_chunked_prefill_attn: inconsistent shapes")
+    st = load().cpp_chunked_prefill_attn(
+        _dev(q, torch.bfloat16, "q"), _dev(k_cache, torch.bfloat16, "k_cache"),
+        _dev(v_cache, torch.bfloat16, "v_cache"), _dev(query_lens, torch.int32, "query_lens"),
+        _dev(seq_lens, torch.int32, "seq_lens"), _dev(block_table, torch.int32, "block_table"),
+        B, T, block_table.shape[1], Hq, Hkv, d, P, pages, float(scale), int(max_kv_splits),
+        _dev(out, torch.bfloat16, "out"), _dev(workspace, torch.uint8, "workspace"), workspace.numel(),
+        _dev(dev_err, torch.int32, "dev_err"), _stream_ptr(stream))
+    _check(st, "cpp_chunked_prefill_attn")
+
+
+def cpp_split_microbatch(query_lens, out3, balance_threshold=0.1, length_threshold=256, stream=None):
+    """Writes (batch_split, token_split, use_two) into the int32 [3] device tensor out3."""
+    st = load().cpp_split_microbatch(_dev(query_lens, torch.int32, "query_lens"), query_lens.shape[0],
+                                     float(balance_threshold), int(length_threshold),
+                                     _dev(out3, torch.int32, "out3"), _stream_ptr(stream))
+    _check(st, "cpp_split_microbatch")
+
+
+def cpp_read_device_error(dev_err, clear=True, stream=None) -> int:
+    host = ctypes.c_uint32(0)
+    st = load().cpp_read_device_error(_dev(dev_err, torch.int32, "dev_err"), ctypes.byref(host), int(clear),
+                                      _stream_ptr(stream))
+    _check(st, "cpp_read_device_error")
+    return int(host.value)
+
+
+def cpp_plan_chunk_sizes(a, b, c, prompt_len, base_chunk_size, page_size, min_chunk=64, max_model_len=0,
+                         max_num_scheduled_tokens=0, smooth_factor=1.0):
+    lib = load()
+    n = ctypes.c_int64(0)
+    cap = max(16, int(prompt_len) // max(1, int(min_chunk)) + 2)
+    buf = (ctypes.c_int64 * cap)()
+    st = lib.cpp_plan_chunk_sizes(a, b, c, prompt_len, base_chunk_size, page_size, min_chunk, max_model_len,
+                                  max_num_scheduled_tokens, smooth_factor, buf, cap, ctypes.byref(n))
+    _check(st, "cpp_plan_chunk_sizes")
+    return [int(buf[i]) for i in range(n.value)]
+
+
+def _dbl(xs):
+    arr = (ctypes.c_double * len(xs))(*[float(x) for x in xs])
+    return arr
+
+
+def cpp_fit_latency_quadratic(lengths, times):
+    coef = (ctypes.c_double * 3)()
+    _check(load().cpp_fit_latency_quadratic(_dbl(lengths), _dbl(times), len(lengths), coef),
+           "cpp_fit_latency_quadratic")
+    return [coef[0], coef[1], coef[2]]
+
+
+def cpp_fit_latency_two_var(x0, x1, x2, times):
+    coef = (ctypes.c_double * 3)()
+    _check(load().cpp_fit_latency_two_var(_dbl(x0), _dbl(x1), _dbl(x2), _dbl(times), len(times), coef),
+           "cpp_fit_latency_two_var")
+    return [coef[0], coef[1], coef[2]]

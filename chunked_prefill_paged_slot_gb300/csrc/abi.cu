@@ -1,0 +1,299 @@
+// abi.cu -- the extern "C" entry points of libcpsa.so (declared in
+// include/cpsa.h): argument checks, TMA tensor maps, workspace carving and the
+// stream-ordered launch sequence. No device memory is allocated here.
+#include <math.h>
+#include <mutex>
+
+#include <cudaTypedefs.h>
+
+#include "common.cuh"
+#include "kernels.cuh"
+#include "plan.cuh"
+
+using namespace cpsa;
+
+namespace {
+
+PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+std::once_flag g_encode_once;
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn()
+{
+    std::call_once(g_encode_once, [] {
+        void *fn = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+    });
+    return g_encode;
+}
+
+// SM count of the current device (cached per device ordinal).
+int sm_count()
+{
+    static int cache[64] = {0};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0)
+        return 0;
+    if (dev < 64 && cache[dev])
+        return cache[dev];
+    int n = 0;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+        return 0;
+    if (dev < 64)
+        cache[dev] = n;
+    return n;
+}
+
+bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+bool pow2_in(int x, int lo, int hi) { return x >= lo && x <= hi && (x & (x - 1)) == 0; }
+
+// 3-D bf16 tensor map, innermost dimension first, 128-byte swizzle.
+bool make_map(CUtensorMap *m, const void *base, uint64_t d0, uint64_t d1, uint64_t d2, uint64_t stride1_bytes,
+              uint64_t stride2_bytes, uint32_t b0, uint32_t b1, uint32_t b2)
+{
+    auto enc = encode_fn();
+    if (!enc)
+        return false;
+    cuuint64_t dims[3] = {d0, d1, d2};
+    cuuint64_t strides[2] = {stride1_bytes, stride2_bytes};
+    cuuint32_t box[3] = {b0, b1, b2};
+    cuuint32_t estr[3] = {1, 1, 1};
+    CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(base), dims, strides, box, estr,
+                     CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                     CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
+int nq_for_group(int group) { return (group % 2 == 0) ? 2 : 1; }
+
+int check_attn_shape(int num_reqs, int64_t num_tokens, int num_q_heads, int num_kv_heads, int head_dim,
+                     int max_kv_splits)
+{
+    if (num_reqs < 0 || num_tokens < 0 || num_q_heads <= 0 || num_kv_heads <= 0 || max_kv_splits < 1 ||
+        max_kv_splits > 32 || num_tokens > (int64_t)INT32_MAX / 2 || num_reqs >= (1 << 24))
+        return CPSA_ERR_BAD_SHAPE;
+    if (head_dim != 64 && head_dim != 128)
+        return CPSA_ERR_UNSUPPORTED;
+    if (num_q_heads % num_kv_heads != 0 || num_q_heads / num_kv_heads > kMaxGroup || num_q_heads > 65535)
+        return CPSA_ERR_UNSUPPORTED;
+    return CPSA_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char *cpp_status_string(int status)
+{
+    switch (status) {
+    case CPSA_OK: return "ok";
+    case CPSA_ERR_NULL_ARG: return "null argument";
+    case CPSA_ERR_BAD_SHAPE: return "bad shape or count";
+    case CPSA_ERR_MISALIGNED: return "pointer not 16-byte aligned";
+    case CPSA_ERR_UNSUPPORTED: return "unsupported head_dim, head grouping or page_size";
+    case CPSA_ERR_WORKSPACE_TOO_SMALL: return "workspace too small";
+    case CPSA_ERR_CUDA: return "CUDA error";
+    case CPSA_ERR_NO_DEVICE: return "no usable device";
+    default: return "unknown status";
+    }
+}
+
+int cpp_kv_cache_write(const void *k, const void *v, const int64_t *slot_mapping, int64_t num_tokens,
+                       int num_kv_heads, int head_dim, int page_size, int64_t num_pages, void *k_cache,
+                       void *v_cache, uint32_t *dev_err, void *stream)
+{
+    if (num_tokens < 0 || num_kv_heads <= 0 || num_pages < 0)
+        return CPSA_ERR_BAD_SHAPE;
+    if (head_dim != 64 && head_dim != 128)
+        return CPSA_ERR_UNSUPPORTED;
+    if (!pow2_in(page_size, 1, 1 << 20))
+        return CPSA_ERR_UNSUPPORTED;
+    if (num_tokens == 0)
+        return CPSA_OK;
+    if (!k || !v || !slot_mapping || !k_cache || !v_cache || !dev_err)
+        return CPSA_ERR_NULL_ARG;
+    if (!aligned16(k) || !aligned16(v) || !aligned16(k_cache) || !aligned16(v_cache))
+        return CPSA_ERR_MISALIGNED;
+    int sms = sm_count();
+    if (sms <= 0)
+        return CPSA_ERR_NO_DEVICE;
+    cudaError_t e = launch_kv_cache_write(k, v, slot_mapping, num_tokens, num_kv_heads, head_dim, page_size,
+                                          num_pages, k_cache, v_cache, dev_err, sms, (cudaStream_t)stream);
+    return e == cudaSuccess ? CPSA_OK : CPSA_ERR_CUDA;
+}
+
+size_t cpp_attn_workspace_bytes(int num_reqs, int64_t num_tokens, int num_q_heads, int num_kv_heads, int head_dim,
+                                int max_kv_splits)
+{
+    if (check_attn_shape(num_reqs, num_tokens, num_q_heads, num_kv_heads, head_dim, max_kv_splits) != CPSA_OK)
+        return 0;
+    WsLayout L = ws_layout(num_reqs, num_tokens, num_q_heads, num_kv_heads, head_dim, max_kv_splits,
+                           nq_for_group(num_q_heads / num_kv_heads));
+    return L.end_full + 512;
+}
+
+size_t cpp_attn_workspace_min_bytes(int num_reqs, int64_t num_tokens, int num_q_heads, int num_kv_heads,
+                                    int head_dim, int max_kv_splits)
+{
+    if (check_attn_shape(num_reqs, num_tokens, num_q_heads, num_kv_heads, head_dim, max_kv_splits) != CPSA_OK)
+        return 0;
+    WsLayout L = ws_layout(num_reqs, num_tokens, num_q_heads, num_kv_heads, head_dim, max_kv_splits,
+                           nq_for_group(num_q_heads / num_kv_heads));
+    return L.end_meta;
+}
+
+int cpp_chunked_prefill_attn(const void *q, const void *k_cache, const void *v_cache, const int32_t *query_lens,
+                             const int32_t *seq_lens, const int32_t *block_table, int num_reqs, int64_t num_tokens,
+                             int max_blocks_per_req, int num_q_heads, int num_kv_heads, int head_dim, int page_size,
+                             int64_t num_pages, float scale, int max_kv_splits, void *out, void *workspace,
+                             size_t workspace_bytes, uint32_t *dev_err, void *stream)
+{
+    int st = check_attn_shape(num_reqs, num_tokens, num_q_heads, num_kv_heads, head_dim, max_kv_splits);
+    if (st != CPSA_OK)
+        return st;
+    if (!pow2_in(page_size, 8, 256))
+        return CPSA_ERR_UNSUPPORTED;
+    if (max_blocks_per_req < 0 || num_pages < 0 || num_pages * num_kv_heads >= (int64_t)1 << 31)
+        return CPSA_ERR_BAD_SHAPE;
+    if (num_reqs == 0 || num_tokens == 0)
+        return num_tokens == 0 ? CPSA_OK : CPSA_ERR_BAD_SHAPE;
+    if (!q || !k_cache || !v_cache || !query_lens || !seq_lens || !block_table || !out || !workspace || !dev_err)
+        return CPSA_ERR_NULL_ARG;
+    if (!aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache) || !aligned16(out) || !aligned16(workspace))
+        return CPSA_ERR_MISALIGNED;
+    const int group = num_q_heads / num_kv_heads;
+    const int nq = nq_for_group(group);
+    WsLayout L = ws_layout(num_reqs, num_tokens, num_q_heads, num_kv_heads, head_dim, max_kv_splits, nq);
+    if (workspace_bytes < L.end_meta)
+        return CPSA_ERR_WORKSPACE_TOO_SMALL;
+    int64_t cap = max_kv_splits > 1 ? ws_partial_capacity(L, workspace_bytes, head_dim) : 0;
+    if (cap > L.max_prows_full)
+        cap = L.max_prows_full;
+    const int sms = sm_count();
+    if (sms <= 0)
+        return CPSA_ERR_NO_DEVICE;
+    if (num_pages == 0)
+        return CPSA_ERR_BAD_SHAPE;
+
+    uint8_t *ws = static_cast<uint8_t *>(workspace);
+    int32_t *counts = reinterpret_cast<int32_t *>(ws + L.off_counts);
+    int32_t *cu_q = reinterpret_cast<int32_t *>(ws + L.off_cuq);
+    PrefillItem *pitems = reinterpret_cast<PrefillItem *>(ws + L.off_pitems);
+    DecodeItem *ditems = reinterpret_cast<DecodeItem *>(ws + L.off_ditems);
+    CombineItem *citems = reinterpret_cast<CombineItem *>(ws + L.off_citems);
+    float *part_ml = reinterpret_cast<float *>(ws + L.end_meta);
+    float *part_o = reinterpret_cast<float *>(ws + L.end_meta + ws_align(sizeof(float) * 2 * (size_t)cap));
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+
+    PlanParams pp{};
+    pp.query_lens = query_lens;
+    pp.seq_lens = seq_lens;
+    pp.num_reqs = num_reqs;
+    pp.num_tokens = num_tokens;
+    pp.max_blocks = max_blocks_per_req;
+    pp.page_size = page_size;
+    pp.Hq = num_q_heads;
+    pp.Hkv = num_kv_heads;
+    pp.group = group;
+    pp.nq = nq;
+    pp.max_splits = max_kv_splits;
+    pp.prow_capacity = cap;
+    pp.counts = counts;
+    pp.cu_q = cu_q;
+    pp.pitems = pitems;
+    pp.ditems = ditems;
+    pp.citems = citems;
+    pp.max_pitems = L.max_pitems;
+    pp.max_ditems = L.max_ditems;
+    pp.max_citems = L.max_citems;
+    pp.dev_err = dev_err;
+    launch_plan(pp, s);
+    if (cudaGetLastError() != cudaSuccess)
+        return CPSA_ERR_CUDA;
+
+    const float sc = scale > 0.f ? scale : 1.0f / sqrtf((float)head_dim);
+    AttnCommon ac{};
+    ac.counts = counts;
+    ac.cu_q = cu_q;
+    ac.query_lens = query_lens;
+    ac.seq_lens = seq_lens;
+    ac.block_table = block_table;
+    ac.max_blocks = max_blocks_per_req;
+    ac.page_size = page_size;
+    ac.num_pages = num_pages;
+    ac.num_q_heads = num_q_heads;
+    ac.num_kv_heads = num_kv_heads;
+    ac.group = group;
+    ac.scale_log2 = sc * 1.4426950408889634f;
+    ac.out = out;
+    ac.part_o = part_o;
+    ac.part_ml = part_ml;
+    ac.dev_err = dev_err;
+
+    const uint64_t D = (uint64_t)head_dim;
+    const uint64_t rows_kv = (uint64_t)num_pages * (uint64_t)num_kv_heads;
+    CUtensorMap tq, tk, tv, tkd, tvd;
+    const uint32_t pb_chunk = page_size < 128 ? page_size : 128;
+    const uint32_t pb_dec = page_size < kDecodeBoxRowsMax ? page_size : kDecodeBoxRowsMax;
+    if (!make_map(&tq, q, D, (uint64_t)num_q_heads, (uint64_t)num_tokens, D * 2, D * 2 * num_q_heads, 64, 1, 128) ||
+        !make_map(&tk, k_cache, D, (uint64_t)page_size, rows_kv, D * 2, D * 2 * page_size, 64, pb_chunk, 1) ||
+        !make_map(&tv, v_cache, D, (uint64_t)page_size, rows_kv, D * 2, D * 2 * page_size, 64, pb_chunk, 1) ||
+        !make_map(&tkd, k_cache, D, (uint64_t)page_size, rows_kv, D * 2, D * 2 * page_size, 64, pb_dec, 1) ||
+        !make_map(&tvd, v_cache, D, (uint64_t)page_size, rows_kv, D * 2, D * 2 * page_size, 64, pb_dec, 1))
+        return CPSA_ERR_CUDA;
+
+    ChunkParams cp;
+    static_cast<AttnCommon &>(cp) = ac;
+    cp.pitems = pitems;
+    int grid_c = (int)(L.max_pitems < sms ? L.max_pitems : sms);
+    if (grid_c > 0 && launch_chunk_attn(cp, tq, tk, tv, head_dim, nq, grid_c, s) != cudaSuccess)
+        return CPSA_ERR_CUDA;
+
+    DecodeParams dp;
+    static_cast<AttnCommon &>(dp) = ac;
+    dp.ditems = ditems;
+    dp.q = q;
+    int grid_d = (int)(L.max_ditems < sms ? L.max_ditems : sms);
+    if (grid_d > 0 && launch_decode_attn(dp, tkd, tvd, head_dim, grid_d, s) != cudaSuccess)
+        return CPSA_ERR_CUDA;
+
+    if (cap > 0) {
+        CombineParams cb{counts, citems, part_o, part_ml, out, num_q_heads};
+        int grid_m = (int)(L.max_citems < 2 * sms ? L.max_citems : 2 * sms);
+        if (grid_m > 0 && launch_combine(cb, head_dim, grid_m, s) != cudaSuccess)
+            return CPSA_ERR_CUDA;
+    }
+    return CPSA_OK;
+}
+
+int cpp_split_microbatch(const int32_t *query_lens, int num_reqs, float balance_threshold, int32_t length_threshold,
+                         int32_t *out3, void *stream)
+{
+    if (num_reqs < 0 || num_reqs >= (1 << 24))
+        return CPSA_ERR_BAD_SHAPE;
+    if (!out3 || (num_reqs > 0 && !query_lens))
+        return CPSA_ERR_NULL_ARG;
+    cudaError_t e = launch_split_microbatch(query_lens, num_reqs, balance_threshold, length_threshold, out3,
+                                            (cudaStream_t)stream);
+    return e == cudaSuccess ? CPSA_OK : CPSA_ERR_CUDA;
+}
+
+int cpp_read_device_error(uint32_t *dev_err, uint32_t *host_flags, int clear, void *stream)
+{
+    if (!dev_err || !host_flags)
+        return CPSA_ERR_NULL_ARG;
+    cudaStream_t s = (cudaStream_t)stream;
+    if (cudaMemcpyAsync(host_flags, dev_err, sizeof(uint32_t), cudaMemcpyDeviceToHost, s) != cudaSuccess)
+        return CPSA_ERR_CUDA;
+    if (cudaStreamSynchronize(s) != cudaSuccess)
+        return CPSA_ERR_CUDA;
+    if (clear && cudaMemsetAsync(dev_err, 0, sizeof(uint32_t), s) != cudaSuccess)
+        return CPSA_ERR_CUDA;
+    return CPSA_OK;
+}
+
+}  // extern "C"

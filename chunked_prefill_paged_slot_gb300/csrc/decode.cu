@@ -1,0 +1,370 @@
+// decode.cu -- split-KV attention of decode rows (query_len == 1) over the paged
+// cache. HBM-bound: every key and value of the row's context is read once per
+// kv head, for all q heads of that kv head at once (GQA grouping).
+//
+// What it computes ("vLLM Chunked-Prefills" article, section 3.1: decode rows
+// ride in the same step as the prefill chunk, one token each; attention per
+// section 3.2.1): for the single new token of request r and the q heads
+// kvh*G .. kvh*G+G-1, softmax(scale * q K^T) V over keys [key0, key1) of the
+// row's context (a whole context, or one split of it).
+//
+// CTA layout (160 threads, persistent over decode items):
+//   warp 4     TMA producer: 64-key stages of K and V (one box per page or per
+//              64 rows of a page), 128-byte swizzled, into a ring of stages.
+//   warps 0-3  consumers, round-robin over stages: S = q K^T and O += P V with
+//              mma.sync m16n8k16 (the G <= 16 q heads are the M rows), online softmax
+//              in fp32 (base-2 exponent), partial state per warp.
+// At the end of an item the four warps merge (max, sum, O) through shared
+// memory and write the bf16 row, or an fp32 partial when the row is split.
+#include "common.cuh"
+#include "kernels.cuh"
+#include "plan.cuh"
+
+namespace cpsa {
+
+namespace {
+
+constexpr int kKC = kDecodeChunk;   // keys per stage
+constexpr int kConsumers = 4;
+
+template <int D>
+struct DecCfg {
+    static constexpr int kHalves = D / 64;
+    static constexpr int kHalfBytes = kKC * 128;
+    static constexpr int kTileBytes = kHalves * kHalfBytes;   // K or V of one stage
+    static constexpr int kStageBytes = 2 * kTileBytes;
+    static constexpr int kStages = D == 128 ? 4 : 8;
+    static constexpr int kMergeOff = kStages * kStageBytes;
+    static constexpr int kMergeBytes = kConsumers * kMaxGroup * (D + 2) * 4;
+    static constexpr int kBarOff = kMergeOff + kMergeBytes;
+    static constexpr int kSmemBytes = kBarOff + 256 + 1024;
+    static constexpr int kThreads = 32 * (kConsumers + 1);
+};
+
+struct DecBars {
+    uint64_t full[8], empty[8];
+    int abort;
+};
+
+__device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t &r0, uint32_t &r1, uint32_t &r2, uint32_t &r3)
+{
+    asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
+                 : "r"(addr));
+}
+
+__device__ __forceinline__ void ldsm_x4_t(uint32_t addr, uint32_t &r0, uint32_t &r1, uint32_t &r2, uint32_t &r3)
+{
+    asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
+                 : "r"(addr));
+}
+
+__device__ __forceinline__ void mma_bf16(float (&d)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1)
+{
+    asm volatile("mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 "
+                 "{%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, {%0,%1,%2,%3};"
+                 : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+                 : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+
+// Byte address of element (row, col) of a [rows][D] bf16 tile stored as
+// 64-column halves with the 128-byte swizzle (16-byte chunk index ^ row % 8).
+template <int D>
+__device__ __forceinline__ uint32_t swz_addr(uint32_t base, int row, int col)
+{
+    const int half = col >> 6;
+    const int ch = (col & 63) >> 3;
+    return base + half * DecCfg<D>::kHalfBytes + row * 128 + ((ch ^ (row & 7)) << 4) + (col & 7) * 2;
+}
+
+template <int D, bool HI>
+__global__ void __launch_bounds__(DecCfg<D>::kThreads, 1)
+decode_attn_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap tm_k,
+                   const __grid_constant__ CUtensorMap tm_v)
+{
+    using C = DecCfg<D>;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
+    DecBars *bars = reinterpret_cast<DecBars *>(smem + C::kBarOff);
+    float *merge = reinterpret_cast<float *>(smem + C::kMergeOff);
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int n_items = p.counts[kCntDecode];
+    const int G = p.group;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < C::kStages; ++s) {
+            mbar_init(&bars->full[s], 1);
+            mbar_init(&bars->empty[s], 1);
+        }
+        bars->abort = 0;
+        fence_barrier_init();
+    }
+    __syncthreads();
+    volatile int *abort = &bars->abort;
+
+    if (warp == kConsumers) {
+        // ------------------------------------------------------------ producer
+        if (lane == 0) {
+            tma_prefetch_desc(&tm_k);
+            tma_prefetch_desc(&tm_v);
+        }
+        const int PB = p.page_size < kKC ? p.page_size : kKC;
+        const int NB = kKC / PB;
+        const uint32_t box_bytes = (uint32_t)PB * 128u;
+        uint32_t g = 0;
+        bool stop = false;
+        for (int it = blockIdx.x; it < n_items && !stop && !*abort; it += gridDim.x) {
+            const DecodeItem w = p.ditems[it];
+            const int32_t *bt_row = p.block_table + (int64_t)w.r * p.max_blocks;
+            for (int c0 = w.key0; c0 < w.key1; c0 += kKC, ++g) {
+                const int stage = g % C::kStages;
+                if (g >= (uint32_t)C::kStages &&
+                    !mbar_wait(&bars->empty[stage], ((g / C::kStages) - 1) & 1, abort)) {
+                    stop = true;
+                    break;
+                }
+                int page = -1, off = 0;
+                bool valid = false;
+                if (lane < NB) {
+                    const int key = c0 + lane * PB;
+                    if (key < w.key1) {
+                        page = bt_row[key / p.page_size];
+                        off = key % p.page_size;
+                        valid = page >= 0 && page < p.num_pages;
+                        if (!valid)
+                            set_dev_error(p.dev_err, CPSA_DEV_PAGE_OUT_OF_RANGE);
+                    }
+                }
+                const uint32_t vmask = __ballot_sync(0xffffffffu, valid);
+                const uint32_t bytes = (uint32_t)__popc(vmask) * box_bytes * C::kHalves * 2;
+                uint8_t *kdst = smem + stage * C::kStageBytes;
+                uint8_t *vdst = kdst + C::kTileBytes;
+                if (lane == 0)
+                    mbar_arrive_expect_tx(&bars->full[stage], bytes);
+                for (int j = 0; j < NB; ++j) {
+                    const int pj = __shfl_sync(0xffffffffu, page, j);
+                    const int oj = __shfl_sync(0xffffffffu, off, j);
+                    if (lane == 0 && ((vmask >> j) & 1u)) {
+                        const int z = pj * p.num_kv_heads + w.kvh;
+                        for (int c = 0; c < C::kHalves; ++c) {
+                            tma_load_3d(kdst + c * C::kHalfBytes + j * box_bytes, &tm_k, &bars->full[stage], c * 64, oj, z);
+                            tma_load_3d(vdst + c * C::kHalfBytes + j * box_bytes, &tm_v, &bars->full[stage], c * 64, oj, z);
+                        }
+                    }
+                }
+            }
+        }
+        return;   // the producer takes no part in the consumers' named barriers
+    }
+
+    // ---------------------------------------------------------------- consumers
+    // Thread layout of mma.sync m16n8k16: A/C rows lane/4 and lane/4 + 8 (the
+    // second only when HI, i.e. more than 8 q heads per kv head).
+    constexpr int R = HI ? 2 : 1;
+    const float sl2 = p.scale_log2;
+    const int qrow = lane >> 2;
+    const int qcol = (lane & 3) * 2;     // column pair within an 8-wide tile
+    uint32_t g = 0;
+    // every consumer warp walks every item (no early exit on abort: the named
+    // barriers below need all four; a failed wait returns at once instead)
+    for (int it = blockIdx.x; it < n_items; it += gridDim.x) {
+        const DecodeItem w = p.ditems[it];
+        const int nch = (w.key1 - w.key0 + kKC - 1) / kKC;
+        // q fragments (rows >= G are zero)
+        uint32_t qa[D / 16][4];
+        {
+            const uint32_t *qsrc = reinterpret_cast<const uint32_t *>(
+                reinterpret_cast<const __nv_bfloat16 *>(p.q) + ((int64_t)w.t * p.num_q_heads + w.kvh * G) * D);
+#pragma unroll
+            for (int kk = 0; kk < D / 16; ++kk) {
+#pragma unroll
+                for (int rr = 0; rr < 2; ++rr) {
+                    const int row = qrow + 8 * rr;
+                    const bool live = (rr == 0 || HI) && row < G;
+                    qa[kk][rr] = live ? __ldg(qsrc + (row * D + kk * 16 + qcol) / 2) : 0u;
+                    qa[kk][2 + rr] = live ? __ldg(qsrc + (row * D + kk * 16 + 8 + qcol) / 2) : 0u;
+                }
+            }
+        }
+        float m_run[R], l_run[R];
+#pragma unroll
+        for (int rr = 0; rr < R; ++rr) {
+            m_run[rr] = -INFINITY;
+            l_run[rr] = 0.f;
+        }
+        float o[D / 8][4];
+#pragma unroll
+        for (int nt = 0; nt < D / 8; ++nt) o[nt][0] = o[nt][1] = o[nt][2] = o[nt][3] = 0.f;
+
+        for (int j = 0; j < nch; ++j) {
+            const uint32_t gg = g + j;
+            if ((int)(gg % kConsumers) != warp)
+                continue;
+            const int stage = gg % C::kStages;
+            if (!mbar_wait(&bars->full[stage], (gg / C::kStages) & 1, abort))
+                break;
+            const int c0 = w.key0 + j * kKC;
+            const int nv = min(kKC, w.key1 - c0);
+            uint8_t *kst = smem + stage * C::kStageBytes;
+            uint8_t *vst = kst + C::kTileBytes;
+            if (nv < kKC) {
+                // value rows past the range may hold anything (NaN included): zero them
+                const int nchunks = (kKC - nv) * 8;
+                for (int c = 0; c < C::kHalves; ++c)
+                    for (int x = lane; x < nchunks; x += 32)
+                        reinterpret_cast<uint4 *>(vst + c * C::kHalfBytes + nv * 128)[x] = make_uint4(0, 0, 0, 0);
+                __syncwarp();
+            }
+            const uint32_t kb = smem_u32(kst), vb = smem_u32(vst);
+            // S = q K^T : 8 n-tiles of 8 keys
+            float s[8][4];
+#pragma unroll
+            for (int nt = 0; nt < 8; ++nt) s[nt][0] = s[nt][1] = s[nt][2] = s[nt][3] = 0.f;
+            const int mat = lane >> 3, mrow = lane & 7;
+#pragma unroll
+            for (int kk = 0; kk < D / 16; ++kk) {
+#pragma unroll
+                for (int np = 0; np < 4; ++np) {
+                    uint32_t b0, b1, b2, b3;
+                    const int key = np * 16 + mrow + (mat >> 1) * 8;
+                    const int col = kk * 16 + (mat & 1) * 8;
+                    ldsm_x4(swz_addr<D>(kb, key, col), b0, b1, b2, b3);
+                    mma_bf16(s[2 * np], qa[kk], b0, b1);
+                    mma_bf16(s[2 * np + 1], qa[kk], b2, b3);
+                }
+            }
+            // mask and online softmax per row (C fragment: [2rr], [2rr+1] of row qrow + 8rr)
+            uint32_t pa[4][4];
+#pragma unroll
+            for (int rr = 0; rr < 2; ++rr)
+#pragma unroll
+                for (int kq = 0; kq < 4; ++kq) pa[kq][rr] = pa[kq][2 + rr] = 0u;
+#pragma unroll
+            for (int rr = 0; rr < R; ++rr) {
+                float mx = -INFINITY;
+#pragma unroll
+                for (int nt = 0; nt < 8; ++nt) {
+#pragma unroll
+                    for (int e = 0; e < 2; ++e) {
+                        if (nt * 8 + qcol + e >= nv) s[nt][2 * rr + e] = -INFINITY;
+                        mx = fmaxf(mx, s[nt][2 * rr + e]);
+                    }
+                }
+                mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
+                mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
+                const float m_new = fmaxf(m_run[rr], mx * sl2);
+                const float alpha = ex2_approx(m_run[rr] - m_new);   // m_run = -inf gives 0
+                m_run[rr] = m_new;
+                const float mref = m_new == -INFINITY ? 0.f : m_new;
+                float psum = 0.f;
+#pragma unroll
+                for (int nt = 0; nt < 8; ++nt) {
+                    const float p0 = ex2_approx(fmaf(s[nt][2 * rr], sl2, -mref));
+                    const float p1 = ex2_approx(fmaf(s[nt][2 * rr + 1], sl2, -mref));
+                    psum += p0 + p1;
+                    // A fragment of P for k-step nt/2: a[rr] keys 0-7, a[2+rr] keys 8-15
+                    pa[nt >> 1][(nt & 1) * 2 + rr] = pack_bf16x2(p0, p1);
+                }
+                l_run[rr] = l_run[rr] * alpha + psum;
+#pragma unroll
+                for (int nt = 0; nt < D / 8; ++nt) {
+                    o[nt][2 * rr] *= alpha;
+                    o[nt][2 * rr + 1] *= alpha;
+                }
+            }
+            // O += P V : A = P (keys as K), B = V rows via transposed ldmatrix
+#pragma unroll
+            for (int kk = 0; kk < 4; ++kk) {
+#pragma unroll
+                for (int np = 0; np < D / 16; ++np) {
+                    uint32_t b0, b1, b2, b3;
+                    const int key = kk * 16 + mrow + (mat & 1) * 8;
+                    const int col = np * 16 + (mat >> 1) * 8;
+                    ldsm_x4_t(swz_addr<D>(vb, key, col), b0, b1, b2, b3);
+                    mma_bf16(o[2 * np], pa[kk], b0, b1);
+                    mma_bf16(o[2 * np + 1], pa[kk], b2, b3);
+                }
+            }
+            if (nv < kKC)
+                fence_proxy_async_smem();   // our zeroing writes before the next TMA into this stage
+            __syncwarp();
+            if (lane == 0)
+                mbar_arrive(&bars->empty[stage]);
+        }
+        g += nch;
+        // merge the four warps' states: max, sum, O
+        float *mm = merge;                                   // [4][16]
+        float *ll = merge + kConsumers * kMaxGroup;          // [4][16]
+        float *oo = merge + 2 * kConsumers * kMaxGroup;      // [4][16][D]
+#pragma unroll
+        for (int rr = 0; rr < R; ++rr) {
+            float lq = l_run[rr];
+            lq += __shfl_xor_sync(0xffffffffu, lq, 1);
+            lq += __shfl_xor_sync(0xffffffffu, lq, 2);
+            const int row = qrow + 8 * rr;
+            if (row < G) {
+                if ((lane & 3) == 0) {
+                    mm[warp * kMaxGroup + row] = m_run[rr];
+                    ll[warp * kMaxGroup + row] = lq;
+                }
+#pragma unroll
+                for (int nt = 0; nt < D / 8; ++nt) {
+                    oo[(warp * kMaxGroup + row) * D + nt * 8 + qcol] = o[nt][2 * rr];
+                    oo[(warp * kMaxGroup + row) * D + nt * 8 + qcol + 1] = o[nt][2 * rr + 1];
+                }
+            }
+        }
+        named_bar_sync(1, 32 * kConsumers);
+        for (int e = threadIdx.x; e < G * D; e += 32 * kConsumers) {
+            const int row = e / D, d = e % D;
+            float M = -INFINITY;
+#pragma unroll
+            for (int x = 0; x < kConsumers; ++x) M = fmaxf(M, mm[x * kMaxGroup + row]);
+            const float Mref = M == -INFINITY ? 0.f : M;
+            float L = 0.f, acc = 0.f;
+#pragma unroll
+            for (int x = 0; x < kConsumers; ++x) {
+                const float f = ex2_approx(mm[x * kMaxGroup + row] - Mref);
+                L += f * ll[x * kMaxGroup + row];
+                acc += f * oo[(x * kMaxGroup + row) * D + d];
+            }
+            const int h = w.kvh * G + row;
+            if (w.nsplit > 1) {
+                const int64_t pr = (int64_t)w.pbase + (int64_t)h * w.nsplit + w.split;
+                p.part_o[pr * D + d] = acc;
+                if (d == 0)
+                    reinterpret_cast<float2 *>(p.part_ml)[pr] = make_float2(M, L);
+            } else {
+                reinterpret_cast<__nv_bfloat16 *>(p.out)[((int64_t)w.t * p.num_q_heads + h) * D + d] =
+                    __float2bfloat16_rn(L > 0.f ? acc / L : 0.f);
+            }
+        }
+        named_bar_sync(1, 32 * kConsumers);
+    }
+    if (threadIdx.x == 0 && *abort)
+        set_dev_error(p.dev_err, CPSA_DEV_WAIT_TIMEOUT);
+}
+
+template <int D>
+cudaError_t launch_decode_t(const DecodeParams &p, const CUtensorMap &tk, const CUtensorMap &tv, int grid,
+                            cudaStream_t s)
+{
+    using C = DecCfg<D>;
+    auto k = p.group > 8 ? decode_attn_kernel<D, true> : decode_attn_kernel<D, false>;
+    cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
+    if (e != cudaSuccess)
+        return e;
+    k<<<grid, C::kThreads, C::kSmemBytes, s>>>(p, tk, tv);
+    return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_decode_attn(const DecodeParams &p, const CUtensorMap &tk, const CUtensorMap &tv,
+                               int head_dim, int grid, cudaStream_t s)
+{
+    return head_dim == 128 ? launch_decode_t<128>(p, tk, tv, grid, s) : launch_decode_t<64>(p, tk, tv, grid, s);
+}
+
+}  // namespace cpsa

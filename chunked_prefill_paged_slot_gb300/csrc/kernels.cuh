@@ -1,0 +1,64 @@
+// kernels.cuh -- parameter blocks and launchers of the attention-step kernels.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "plan.cuh"
+
+namespace cpsa {
+
+// Fields common to the chunk (prefill) and decode kernels.
+struct AttnCommon {
+    const int32_t *counts;
+    const int32_t *cu_q;
+    const int32_t *query_lens;
+    const int32_t *seq_lens;
+    const int32_t *block_table;
+    int max_blocks;
+    int page_size;
+    int64_t num_pages;
+    int num_q_heads, num_kv_heads, group;
+    float scale_log2;          // scale * log2(e): scores go straight to the base-2 exponent
+    void *out;                 // bf16 [T][Hq][D]
+    float *part_o;             // fp32 [rows][D] partial outputs of split rows
+    float *part_ml;            // fp32 [rows][2]  (max in log2 units, row sum)
+    uint32_t *dev_err;
+};
+
+struct ChunkParams : AttnCommon {
+    const PrefillItem *pitems;
+};
+
+struct DecodeParams : AttnCommon {
+    const DecodeItem *ditems;
+    const void *q;             // bf16 [T][Hq][D]
+};
+
+struct CombineParams {
+    const int32_t *counts;
+    const CombineItem *citems;
+    const float *part_o;
+    const float *part_ml;
+    void *out;
+    int num_q_heads;
+};
+
+cudaError_t launch_chunk_attn(const ChunkParams &p, const CUtensorMap &tq, const CUtensorMap &tk,
+                              const CUtensorMap &tv, int head_dim, int nq, int grid, cudaStream_t s);
+cudaError_t launch_decode_attn(const DecodeParams &p, const CUtensorMap &tk, const CUtensorMap &tv,
+                               int head_dim, int grid, cudaStream_t s);
+cudaError_t launch_combine(const CombineParams &p, int head_dim, int grid, cudaStream_t s);
+
+cudaError_t launch_kv_cache_write(const void *k, const void *v, const int64_t *slot_mapping,
+                                  int64_t num_tokens, int num_kv_heads, int head_dim,
+                                  int page_size, int64_t num_pages, void *k_cache, void *v_cache,
+                                  uint32_t *dev_err, int num_sms, cudaStream_t s);
+cudaError_t launch_split_microbatch(const int32_t *query_lens, int num_reqs, float balance_threshold,
+                                    int32_t length_threshold, int32_t *out3, cudaStream_t s);
+
+// Rows of K/V per TMA box for the decode kernel (keys per pipeline stage cap).
+constexpr int kDecodeBoxRowsMax = 64;
+
+}  // namespace cpsa

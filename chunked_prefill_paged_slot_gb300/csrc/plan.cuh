@@ -1,0 +1,115 @@
+// plan.cuh -- work items and workspace layout shared by the metadata kernel and
+// the attention kernels.
+//
+// One call of cpp_chunked_prefill_attn runs:
+//   plan      one CTA: scan of query_lens, validation, work lists, split choice
+//   chunk     tensor-core kernel over prefill items (query_len >= 2)
+//   decode    split-KV kernel over decode items (query_len == 1)
+//   combine   merges the partial results of rows that were split along keys
+// The lists live in the caller's workspace; every kernel is persistent and reads
+// its item count from the workspace, so the host never needs the lengths.
+#pragma once
+
+#include <stddef.h>
+#include <stdint.h>
+
+namespace cpsa {
+
+// Split policy: constants only, so a row's split count depends on its own
+// (query_len, seq_len) and the caller's max_kv_splits.
+constexpr int kPrefillTilesPerSplit = 32;   // KV tiles of 128 keys per prefill split
+constexpr int kDecodeChunk = 64;            // keys per decode pipeline stage
+constexpr int kDecodeKeysPerSplit = 4096;   // keys per decode split (multiple of kDecodeChunk)
+
+// A prefill item: one 128-row query tile of request r, NQ q heads of kv head
+// `kvh` (q heads kvh*G + hp*NQ ...), KV tiles [kt0, kt1) of split `split`.
+struct PrefillItem {
+    int32_t r, i0, kvh_hp, kt0, kt1, split, nsplit, pbase;
+};
+
+// A decode item: the single new token (global row t) of request r, all q heads
+// of kv head kvh, keys [key0, key1) of split `split`.
+struct DecodeItem {
+    int32_t r, kvh, key0, key1, split, nsplit, pbase, t;
+};
+
+// Rows [t0, t0 + nrows) had nsplit partials each, at pbase + (row*Hq + h)*nsplit + s.
+struct CombineItem {
+    int32_t t0, nrows, pbase, nsplit;
+};
+
+enum CountSlot {
+    kCntPrefill = 0,
+    kCntDecode = 1,
+    kCntCombine = 2,
+    kCntPartialRows = 3,
+    kCntSlots = 16
+};
+
+struct WsLayout {
+    size_t off_counts, off_cuq, off_pitems, off_ditems, off_citems, off_pml, off_po, end_meta, end_full;
+    int64_t max_pitems, max_ditems, max_citems, max_prows_full;
+};
+
+__host__ __device__ inline size_t ws_align(size_t x) { return (x + 255) & ~(size_t)255; }
+
+// Upper bounds of the work lists for a batch of num_reqs requests and num_tokens
+// new tokens (every prefill request has >= 2 tokens, so at most num_tokens/2).
+inline WsLayout ws_layout(int num_reqs, int64_t num_tokens, int Hq, int Hkv, int D, int max_splits,
+                          int nq_per_cta)
+{
+    WsLayout L{};
+    int64_t B = num_reqs, T = num_tokens;
+    int64_t nprefill = B < T / 2 ? B : T / 2;
+    int64_t ndecode = B < T ? B : T;
+    int64_t qtiles = T / 128 + nprefill + 1;
+    int64_t pairs = (Hq / Hkv) / nq_per_cta;
+    L.max_pitems = qtiles * Hkv * pairs * max_splits;
+    L.max_ditems = ndecode * Hkv * max_splits;
+    L.max_citems = qtiles + ndecode;
+    L.max_prows_full = max_splits > 1 ? T * Hq * max_splits : 0;
+    size_t o = 0;
+    L.off_counts = o; o = ws_align(o + sizeof(int32_t) * kCntSlots);
+    L.off_cuq = o;    o = ws_align(o + sizeof(int32_t) * (size_t)(B + 1));
+    L.off_pitems = o; o = ws_align(o + sizeof(PrefillItem) * (size_t)L.max_pitems);
+    L.off_ditems = o; o = ws_align(o + sizeof(DecodeItem) * (size_t)L.max_ditems);
+    L.off_citems = o; o = ws_align(o + sizeof(CombineItem) * (size_t)L.max_citems);
+    L.end_meta = o;
+    L.off_pml = o;
+    size_t ml = ws_align(sizeof(float) * 2 * (size_t)L.max_prows_full);
+    L.off_po = o + ml;
+    L.end_full = L.off_po + ws_align(sizeof(float) * (size_t)D * (size_t)L.max_prows_full);
+    return L;
+}
+
+// Partial-row capacity that fits in `bytes` of workspace (m,l pairs + D floats each).
+inline int64_t ws_partial_capacity(const WsLayout &L, size_t bytes, int D)
+{
+    if (bytes <= L.end_meta + 512)
+        return 0;
+    size_t room = bytes - L.end_meta - 512;
+    return (int64_t)(room / (sizeof(float) * (2 + (size_t)D)));
+}
+
+struct PlanParams {
+    const int32_t *query_lens;
+    const int32_t *seq_lens;
+    int num_reqs;
+    int64_t num_tokens;
+    int max_blocks;
+    int page_size;
+    int Hq, Hkv, group, nq;    // nq: q heads per chunk-kernel CTA (1 or 2)
+    int max_splits;
+    int64_t prow_capacity;     // partial rows that fit
+    int32_t *counts;
+    int32_t *cu_q;
+    PrefillItem *pitems;
+    DecodeItem *ditems;
+    CombineItem *citems;
+    int64_t max_pitems, max_ditems, max_citems;
+    uint32_t *dev_err;
+};
+
+void launch_plan(const PlanParams &p, cudaStream_t s);
+
+}  // namespace cpsa

@@ -1,0 +1,460 @@
+// prefill_tc.cu -- causal chunked-prefill attention on the 5th-generation tensor
+// cores (tcgen05 + TMEM), K/V tiles gathered page by page from the paged cache
+// with TMA.
+//
+// What it computes ("vLLM Chunked-Prefills" article, section 3.2.1, chunked
+// attention; metadata from the "Ascend dual-stream parallel" article, section
+// 3.1): for a 128-row tile of one request's new tokens and NQ q heads that share
+// one kv head, softmax(scale * Q K^T) V over the keys 0 .. h_r + i of every row i,
+// the history keys and the chunk's own keys alike read from the cache pages
+// listed in block_table.
+//
+// CTA layout (320 threads, one CTA per SM, persistent over prefill items):
+//   warp 8       TMA producer: Q tiles once per item, then K_j, V_j into a ring
+//                of shared-memory slots; block_table lookups; zeroes the value
+//                rows past seq_len in the last tile (they may hold anything).
+//   warp 9       tcgen05 issuer (one lane): S_n = Q_n K_j^T into TMEM, then
+//                O_n += P_n V_j with P_n read from TMEM; TMEM alloc/dealloc.
+//   warps 0..7   softmax, one warpgroup per q head n; thread = query row:
+//                S row from TMEM, causal mask on the diagonal/tail tiles, online
+//                max/sum in fp32 (base-2 exponent, scale folded in), P as bf16
+//                back into TMEM over S; final O / l epilogue.
+// Rescaling of O is lazy: the running maximum is only raised when a tile's
+// maximum exceeds it by more than 8 (a factor 256 in the exponent), which keeps
+// p <= 256 and leaves the final O / l unchanged.
+// TMEM columns: S_0 [0,128) S_1 [128,256) O_0 [256,256+D) O_1 [256+D, 256+2D).
+#include "common.cuh"
+#include "kernels.cuh"
+#include "plan.cuh"
+
+namespace cpsa {
+
+namespace {
+
+template <int D, int NQ>
+struct ChunkCfg {
+    static constexpr int kHalves = D / 64;             // 128-byte swizzle atoms across a row
+    static constexpr int kHalfBytes = 128 * 128;       // 128 rows x 64 bf16
+    static constexpr int kTileBytes = kHalves * kHalfBytes;
+    static constexpr int kSlots = D == 128 ? 4 : 8;
+    static constexpr int kQOff = 0;
+    static constexpr int kSlotOff = NQ * kTileBytes;
+    static constexpr int kBarOff = kSlotOff + kSlots * kTileBytes;
+    static constexpr int kSmemBytes = kBarOff + 1024 + 1024;   // barriers + alignment slack
+    static constexpr int kThreads = 320;
+    static constexpr int kLoadWarp = 8;
+    static constexpr int kMmaWarp = 9;
+    static constexpr uint32_t kTmemCols = 512;
+    __host__ __device__ static constexpr uint32_t s_col(int n) { return (uint32_t)n * 128u; }
+    __host__ __device__ static constexpr uint32_t o_col(int n) { return 256u + (uint32_t)n * D; }
+};
+
+struct ChunkBars {
+    uint64_t q_full, q_empty, tail, drain;
+    uint64_t s_full[2], p_full[2], o_done[2];
+    uint64_t slot_full[8], slot_empty[8];
+    uint32_t tmem_base;
+    int abort;
+};
+
+template <int D, int NQ>
+__global__ void __launch_bounds__(320, 1)
+chunk_attn_kernel(const ChunkParams p, const __grid_constant__ CUtensorMap tm_q,
+                  const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v)
+{
+    using C = ChunkCfg<D, NQ>;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
+    ChunkBars *bars = reinterpret_cast<ChunkBars *>(smem + C::kBarOff);
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int n_items = p.counts[kCntPrefill];
+
+    if (threadIdx.x == 0) {
+        mbar_init(&bars->q_full, 1);
+        mbar_init(&bars->q_empty, 1);
+        mbar_init(&bars->tail, 1);
+        mbar_init(&bars->drain, 1);
+        for (int n = 0; n < 2; ++n) {
+            mbar_init(&bars->s_full[n], 1);
+            mbar_init(&bars->p_full[n], 4);
+            mbar_init(&bars->o_done[n], 1);
+        }
+        for (int s = 0; s < C::kSlots; ++s) {
+            mbar_init(&bars->slot_full[s], 1);
+            mbar_init(&bars->slot_empty[s], 1);
+        }
+        bars->abort = 0;
+        fence_barrier_init();
+    }
+    if (warp == C::kLoadWarp && lane == 0) {
+        tma_prefetch_desc(&tm_q);
+        tma_prefetch_desc(&tm_k);
+        tma_prefetch_desc(&tm_v);
+    }
+    if (warp == C::kMmaWarp) {
+        tmem_alloc(&bars->tmem_base, C::kTmemCols);
+        tmem_relinquish();
+    }
+    tc_fence_before_sync();
+    __syncthreads();
+    tc_fence_after_sync();
+    const uint32_t tmem = bars->tmem_base;
+    volatile int *abort = &bars->abort;
+
+    if (warp == C::kLoadWarp) {
+        // ------------------------------------------------------------ producer
+        const int PB = p.page_size < 128 ? p.page_size : 128;   // rows per TMA box
+        const int NB = 128 / PB;                                 // boxes per tile
+        const uint32_t box_bytes = (uint32_t)PB * 128u;
+        uint32_t q_uses = 0, slot_it = 0, tail_uses = 0;
+        for (int it = blockIdx.x; it < n_items && !*abort; it += gridDim.x) {
+            const PrefillItem w = p.pitems[it];
+            const int kvh = w.kvh_hp & 0xFFFF, hp = w.kvh_hp >> 16;
+            const int h0 = kvh * p.group + hp * NQ;
+            const int cu = p.cu_q[w.r];
+            const int s_len = p.seq_lens[w.r];
+            if (q_uses > 0 && !mbar_wait(&bars->q_empty, (q_uses - 1) & 1, abort))
+                break;
+            if (lane == 0) {
+                mbar_arrive_expect_tx(&bars->q_full, NQ * C::kTileBytes);
+                for (int n = 0; n < NQ; ++n)
+                    for (int c = 0; c < C::kHalves; ++c)
+                        tma_load_3d(smem + C::kQOff + n * C::kTileBytes + c * C::kHalfBytes, &tm_q,
+                                    &bars->q_full, c * 64, h0 + n, cu + w.i0);
+            }
+            ++q_uses;
+            const int32_t *bt_row = p.block_table + (int64_t)w.r * p.max_blocks;
+            bool stop = false;
+            for (int kt = w.kt0; kt < w.kt1 && !stop; ++kt) {
+                const int key0 = kt * 128;
+                // lane j < NB looks up box j of this tile
+                int page = -1, off = 0;
+                bool valid = false;
+                if (lane < NB) {
+                    int key = key0 + lane * PB;
+                    if (key < s_len) {
+                        page = bt_row[key / p.page_size];
+                        off = key % p.page_size;
+                        valid = page >= 0 && page < p.num_pages;
+                        if (!valid)
+                            set_dev_error(p.dev_err, CPSA_DEV_PAGE_OUT_OF_RANGE);
+                    }
+                }
+                const uint32_t vmask = __ballot_sync(0xffffffffu, valid);
+                const uint32_t bytes = (uint32_t)__popc(vmask) * box_bytes * C::kHalves;
+                const bool tail = key0 + 128 > s_len;
+                for (int kv = 0; kv < 2 && !stop; ++kv) {
+                    const int slot = slot_it % C::kSlots;
+                    if (slot_it >= (uint32_t)C::kSlots &&
+                        !mbar_wait(&bars->slot_empty[slot], ((slot_it / C::kSlots) - 1) & 1, abort)) {
+                        stop = true;
+                        break;
+                    }
+                    uint8_t *dst = smem + C::kSlotOff + slot * C::kTileBytes;
+                    const CUtensorMap *map = kv == 0 ? &tm_k : &tm_v;
+                    const bool fix = kv == 1 && tail;
+                    uint64_t *bar = fix ? &bars->tail : &bars->slot_full[slot];
+                    if (lane == 0)
+                        mbar_arrive_expect_tx(bar, bytes);
+                    for (int j = 0; j < NB; ++j) {
+                        int pj = __shfl_sync(0xffffffffu, page, j);
+                        int oj = __shfl_sync(0xffffffffu, off, j);
+                        if (lane == 0 && ((vmask >> j) & 1u))
+                            for (int c = 0; c < C::kHalves; ++c)
+                                tma_load_3d(dst + c * C::kHalfBytes + j * box_bytes, map, bar, c * 64,
+                                            oj, pj * p.num_kv_heads + kvh);
+                    }
+                    if (fix) {
+                        // value rows >= seq_len must be zero: P is zero there, but the
+                        // bytes may be NaN and 0 * NaN would poison the row sums.
+                        if (!mbar_wait(&bars->tail, tail_uses & 1, abort)) {
+                            stop = true;
+                            break;
+                        }
+                        ++tail_uses;
+                        const int first = s_len - key0;   // 1 .. 127
+                        const int nchunks = (128 - first) * 8;   // 16-byte chunks per half
+                        for (int c = 0; c < C::kHalves; ++c)
+                            for (int x = lane; x < nchunks; x += 32) {
+                                uint4 *row = reinterpret_cast<uint4 *>(dst + c * C::kHalfBytes + first * 128);
+                                row[x] = make_uint4(0, 0, 0, 0);
+                            }
+                        fence_proxy_async_smem();
+                        __syncwarp();
+                        if (lane == 0)
+                            mbar_arrive(&bars->slot_full[slot]);
+                    }
+                    ++slot_it;
+                }
+            }
+            if (stop)
+                break;
+        }
+    } else if (warp == C::kMmaWarp) {
+        // ------------------------------------------------------------ MMA issuer
+        if (lane == 0) {
+            constexpr uint32_t idesc_qk = idesc_bf16_f32(128, 128, false);
+            constexpr uint32_t idesc_pv = idesc_bf16_f32(128, D, true);
+            const uint32_t q_addr = smem_u32(smem + C::kQOff);
+            const uint32_t slot_addr = smem_u32(smem + C::kSlotOff);
+            uint32_t q_uses = 0, slot_it = 0, p_uses[2] = {0, 0};
+            auto issue_qk = [&](int n, int slot) {
+#pragma unroll
+                for (int kk = 0; kk < D / 16; ++kk) {
+                    const uint32_t koff = (kk >> 2) * C::kHalfBytes + (kk & 3) * 32;
+                    uint64_t a = smem_desc_sw128(q_addr + n * C::kTileBytes + koff, 0, 1024);
+                    uint64_t b = smem_desc_sw128(slot_addr + slot * C::kTileBytes + koff, 0, 1024);
+                    umma_ss(tmem + C::s_col(n), a, b, idesc_qk, kk > 0);
+                }
+            };
+            auto issue_pv = [&](int n, int slot, bool acc) {
+#pragma unroll
+                for (int kk = 0; kk < 128 / 16; ++kk) {
+                    uint64_t b = smem_desc_sw128(slot_addr + slot * C::kTileBytes + kk * 16 * 128,
+                                                 C::kHalfBytes, 1024);
+                    umma_ts(tmem + C::o_col(n), tmem + C::s_col(n) + kk * 8, b, idesc_pv, (acc || kk > 0));
+                }
+            };
+            auto wait_slot = [&](int &slot) -> bool {
+                slot = slot_it % C::kSlots;
+                bool ok = mbar_wait(&bars->slot_full[slot], (slot_it / C::kSlots) & 1, abort);
+                ++slot_it;
+                tc_fence_after_sync();
+                return ok;
+            };
+            for (int it = blockIdx.x; it < n_items && !*abort; it += gridDim.x) {
+                const PrefillItem w = p.pitems[it];
+                const int n = w.kt1 - w.kt0;
+                if (!mbar_wait(&bars->q_full, q_uses & 1, abort))
+                    break;
+                ++q_uses;
+                tc_fence_after_sync();
+                int sK, sV;
+                if (!wait_slot(sK))
+                    break;
+                for (int qn = 0; qn < NQ; ++qn) {
+                    issue_qk(qn, sK);
+                    umma_commit(&bars->s_full[qn]);
+                }
+                umma_commit(&bars->slot_empty[sK]);
+                if (n == 1)
+                    umma_commit(&bars->q_empty);
+                bool ok = true;
+                for (int t = 0; t < n && ok; ++t) {
+                    if (!(ok = wait_slot(sV)))
+                        break;
+                    if (!(ok = mbar_wait(&bars->p_full[0], p_uses[0] & 1, abort)))
+                        break;
+                    ++p_uses[0];
+                    tc_fence_after_sync();
+                    issue_pv(0, sV, t > 0);
+                    umma_commit(&bars->o_done[0]);
+                    const bool more = t + 1 < n;
+                    if (more) {
+                        if (!(ok = wait_slot(sK)))
+                            break;
+                        issue_qk(0, sK);
+                        umma_commit(&bars->s_full[0]);
+                    }
+                    if (NQ == 2) {
+                        if (!(ok = mbar_wait(&bars->p_full[1], p_uses[1] & 1, abort)))
+                            break;
+                        ++p_uses[1];
+                        tc_fence_after_sync();
+                        issue_pv(1, sV, t > 0);
+                        umma_commit(&bars->o_done[1]);
+                    }
+                    umma_commit(&bars->slot_empty[sV]);
+                    if (more) {
+                        if (NQ == 2) {
+                            issue_qk(1, sK);
+                            umma_commit(&bars->s_full[1]);
+                        }
+                        umma_commit(&bars->slot_empty[sK]);
+                        if (t + 2 == n)
+                            umma_commit(&bars->q_empty);
+                    }
+                }
+                if (!ok)
+                    break;
+            }
+            if (*abort) {
+                // let every MMA issued so far finish before TMEM is released
+                umma_commit(&bars->drain);
+                uint64_t t0 = global_timer_ns();
+                while (!mbar_try_wait(&bars->drain, 0) && global_timer_ns() - t0 < 100000000ull) {
+                }
+            }
+        }
+        __syncwarp();
+    } else if (warp / 4 < NQ) {
+        // ------------------------------------------------------------ softmax
+        const int wg = warp / 4;
+        const int sub = warp & 3;
+        const int row = sub * 32 + lane;
+        const uint32_t lane_base = (uint32_t)(sub * 32) << 16;
+        const uint32_t tS = tmem + lane_base + C::s_col(wg);
+        const uint32_t tO = tmem + lane_base + C::o_col(wg);
+        const float sl2 = p.scale_log2;
+        uint32_t s_uses = 0, o_base = 0;
+        for (int it = blockIdx.x; it < n_items && !*abort; it += gridDim.x) {
+            const PrefillItem w = p.pitems[it];
+            const int kvh = w.kvh_hp & 0xFFFF, hp = w.kvh_hp >> 16;
+            const int h = kvh * p.group + hp * NQ + wg;
+            const int q_len = p.query_lens[w.r];
+            const int s_len = p.seq_lens[w.r];
+            const int hist = s_len - q_len;
+            const int i = w.i0 + row;
+            const int limit = min(hist + i, s_len - 1);   // last visible key of this row
+            const int n = w.kt1 - w.kt0;
+            float m_use = -INFINITY, l = 0.f;
+            bool ok = true;
+            for (int t = 0; t < n; ++t) {
+                const int key0 = (w.kt0 + t) * 128;
+                if (!(ok = mbar_wait(&bars->s_full[wg], s_uses & 1, abort)))
+                    break;
+                ++s_uses;
+                tc_fence_after_sync();
+                float sv[128];
+#pragma unroll
+                for (int c = 0; c < 4; ++c) {
+                    uint32_t r[32];
+                    tmem_ld32(tS + c * 32, r);
+                    tmem_wait_ld();
+#pragma unroll
+                    for (int x = 0; x < 32; ++x) sv[c * 32 + x] = __uint_as_float(r[x]);
+                }
+                if (key0 + 127 > limit) {
+#pragma unroll
+                    for (int x = 0; x < 128; ++x)
+                        if (key0 + x > limit) sv[x] = -INFINITY;
+                }
+                float mx = sv[0];
+#pragma unroll
+                for (int x = 1; x < 128; ++x) mx = fmaxf(mx, sv[x]);
+                const float m_tile = mx * sl2;
+                const bool need = m_tile > m_use + 8.f;
+                float alpha = 1.f;
+                if (need) {
+                    alpha = ex2_approx(m_use - m_tile);   // m_use = -inf gives 0
+                    l *= alpha;
+                    m_use = m_tile;
+                }
+                const float mref = m_use == -INFINITY ? 0.f : m_use;
+                float sum = 0.f;
+#pragma unroll
+                for (int hh = 0; hh < 2; ++hh) {
+                    uint32_t pk[32];
+#pragma unroll
+                    for (int x = 0; x < 32; ++x) {
+                        const float a = ex2_approx(fmaf(sv[64 * hh + 2 * x], sl2, -mref));
+                        const float b = ex2_approx(fmaf(sv[64 * hh + 2 * x + 1], sl2, -mref));
+                        sum += a + b;
+                        pk[x] = pack_bf16x2(a, b);
+                    }
+                    tmem_st32(tS + 32 * hh, pk);
+                }
+                l += sum;
+                tmem_wait_st();
+                if (__any_sync(0xffffffffu, need) && t > 0) {
+                    // O holds the sum through tile t-1: wait for that P.V, then rescale
+                    if (!(ok = mbar_wait(&bars->o_done[wg], (o_base + t - 1) & 1, abort)))
+                        break;
+                    tc_fence_after_sync();
+#pragma unroll
+                    for (int c = 0; c < D / 32; ++c) {
+                        uint32_t r[32];
+                        tmem_ld32(tO + c * 32, r);
+                        tmem_wait_ld();
+#pragma unroll
+                        for (int x = 0; x < 32; ++x) r[x] = __float_as_uint(__uint_as_float(r[x]) * alpha);
+                        tmem_st32(tO + c * 32, r);
+                    }
+                    tmem_wait_st();
+                }
+                tc_fence_before_sync();
+                __syncwarp();
+                if (lane == 0)
+                    mbar_arrive(&bars->p_full[wg]);
+            }
+            if (!ok)
+                break;
+            if (!mbar_wait(&bars->o_done[wg], (o_base + n - 1) & 1, abort))
+                break;
+            o_base += n;
+            tc_fence_after_sync();
+            const bool valid_row = i < q_len;
+            const int64_t t_row = (int64_t)p.cu_q[w.r] + i;
+            if (w.nsplit > 1) {
+                const int64_t pr = (int64_t)w.pbase + ((int64_t)row * p.num_q_heads + h) * w.nsplit + w.split;
+#pragma unroll
+                for (int c = 0; c < D / 32; ++c) {
+                    uint32_t r[32];
+                    tmem_ld32(tO + c * 32, r);
+                    tmem_wait_ld();
+                    if (valid_row) {
+                        float4 *dst = reinterpret_cast<float4 *>(p.part_o + pr * D + c * 32);
+#pragma unroll
+                        for (int x = 0; x < 8; ++x)
+                            dst[x] = make_float4(__uint_as_float(r[4 * x]), __uint_as_float(r[4 * x + 1]),
+                                                 __uint_as_float(r[4 * x + 2]), __uint_as_float(r[4 * x + 3]));
+                    }
+                }
+                if (valid_row)
+                    reinterpret_cast<float2 *>(p.part_ml)[pr] = make_float2(m_use, l);
+            } else {
+                const float inv_l = l > 0.f ? 1.f / l : 0.f;
+#pragma unroll
+                for (int c = 0; c < D / 32; ++c) {
+                    uint32_t r[32];
+                    tmem_ld32(tO + c * 32, r);
+                    tmem_wait_ld();
+                    if (valid_row) {
+                        uint4 *dst = reinterpret_cast<uint4 *>(
+                            reinterpret_cast<__nv_bfloat16 *>(p.out) + (t_row * p.num_q_heads + h) * D + c * 32);
+#pragma unroll
+                        for (int x = 0; x < 4; ++x)
+                            dst[x] = make_uint4(pack_bf16x2(__uint_as_float(r[8 * x + 0]) * inv_l, __uint_as_float(r[8 * x + 1]) * inv_l),
+                                                pack_bf16x2(__uint_as_float(r[8 * x + 2]) * inv_l, __uint_as_float(r[8 * x + 3]) * inv_l),
+                                                pack_bf16x2(__uint_as_float(r[8 * x + 4]) * inv_l, __uint_as_float(r[8 * x + 5]) * inv_l),
+                                                pack_bf16x2(__uint_as_float(r[8 * x + 6]) * inv_l, __uint_as_float(r[8 * x + 7]) * inv_l));
+                    }
+                }
+            }
+        }
+    }
+
+    if (threadIdx.x == 0 && bars->abort)
+        set_dev_error(p.dev_err, CPSA_DEV_WAIT_TIMEOUT);
+    tc_fence_before_sync();
+    __syncthreads();
+    if (warp == C::kMmaWarp) {
+        tc_fence_after_sync();
+        tmem_dealloc(tmem, C::kTmemCols);
+    }
+}
+
+template <int D, int NQ>
+cudaError_t launch_chunk_t(const ChunkParams &p, const CUtensorMap &tq, const CUtensorMap &tk,
+                           const CUtensorMap &tv, int grid, cudaStream_t s)
+{
+    using C = ChunkCfg<D, NQ>;
+    auto k = chunk_attn_kernel<D, NQ>;
+    cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
+    if (e != cudaSuccess)
+        return e;
+    k<<<grid, C::kThreads, C::kSmemBytes, s>>>(p, tq, tk, tv);
+    return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_chunk_attn(const ChunkParams &p, const CUtensorMap &tq, const CUtensorMap &tk,
+                              const CUtensorMap &tv, int head_dim, int nq, int grid, cudaStream_t s)
+{
+    if (head_dim == 128)
+        return nq == 2 ? launch_chunk_t<128, 2>(p, tq, tk, tv, grid, s) : launch_chunk_t<128, 1>(p, tq, tk, tv, grid, s);
+    return nq == 2 ? launch_chunk_t<64, 2>(p, tq, tk, tv, grid, s) : launch_chunk_t<64, 1>(p, tq, tk, tv, grid, s);
+}
+
+}  // namespace cpsa

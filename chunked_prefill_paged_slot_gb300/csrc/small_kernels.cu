@@ -1,0 +1,220 @@
+// small_kernels.cu -- the KV write, the split-KV combine and the micro-batch split.
+#include "common.cuh"
+#include "kernels.cuh"
+#include "plan.cuh"
+
+namespace cpsa {
+
+namespace {
+
+// ---------------------------------------------------------------------------
+// KV write ("Ascend dual-stream parallel" article, section 3.1, slot_mapping:
+// every new token goes to its own cache slot). A bit copy in 16-byte vectors:
+// thread x of a (token, kv head) row moves bytes [16x, 16x+16) of k and of v.
+// Consecutive threads read consecutive bytes of k/v and write consecutive bytes
+// of one cache row, so both sides are coalesced.
+// ---------------------------------------------------------------------------
+template <int VEC_PER_ROW>
+__global__ void __launch_bounds__(256) kv_write_kernel(const uint4 *__restrict__ k, const uint4 *__restrict__ v,
+                                                       const int64_t *__restrict__ slot_mapping, int64_t num_tokens,
+                                                       int num_kv_heads, int page_size, int64_t num_pages,
+                                                       uint4 *__restrict__ k_cache, uint4 *__restrict__ v_cache,
+                                                       uint32_t *dev_err)
+{
+    const int64_t rows = num_tokens * num_kv_heads;
+    const int64_t total = rows * VEC_PER_ROW;
+    const int64_t slots = num_pages * page_size;
+    for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < total; i += (int64_t)gridDim.x * blockDim.x) {
+        const int64_t row = i / VEC_PER_ROW;
+        const int x = (int)(i % VEC_PER_ROW);
+        const int64_t t = row / num_kv_heads;
+        const int h = (int)(row % num_kv_heads);
+        const int64_t slot = __ldg(slot_mapping + t);
+        if (slot < 0)
+            continue;   // padding token
+        if (slot >= slots) {
+            if (h == 0 && x == 0)
+                set_dev_error(dev_err, CPSA_DEV_SLOT_OUT_OF_RANGE);
+            continue;
+        }
+        const int64_t page = slot / page_size;
+        const int64_t off = slot - page * page_size;
+        const int64_t dst = ((page * num_kv_heads + h) * page_size + off) * VEC_PER_ROW + x;
+        const uint4 kv = __ldcs(k + i);
+        const uint4 vv = __ldcs(v + i);
+        k_cache[dst] = kv;
+        v_cache[dst] = vv;
+    }
+}
+
+// ---------------------------------------------------------------------------
+// Combine of split rows: O = sum_s 2^(m_s - M) O_s / sum_s 2^(m_s - M) l_s,
+// M = max_s m_s (m in base-2 units). One warp per (row, q head).
+// ---------------------------------------------------------------------------
+template <int D>
+__global__ void __launch_bounds__(256) combine_kernel(const CombineParams p)
+{
+    const int n_items = p.counts[kCntCombine];
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    constexpr int PER_LANE = D / 32;
+    for (int ci = blockIdx.x; ci < n_items; ci += gridDim.x) {
+        const CombineItem c = p.citems[ci];
+        const int units = c.nrows * p.num_q_heads;
+        for (int u = warp; u < units; u += blockDim.x / 32) {
+            const int row = u / p.num_q_heads, h = u % p.num_q_heads;
+            const int64_t pr0 = (int64_t)c.pbase + (int64_t)u * c.nsplit;
+            float2 ml = lane < c.nsplit ? reinterpret_cast<const float2 *>(p.part_ml)[pr0 + lane]
+                                        : make_float2(-INFINITY, 0.f);
+            float M = ml.x;
+            for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
+            const float Mref = M == -INFINITY ? 0.f : M;
+            const float f = ex2_approx(ml.x - Mref);
+            float L = f * ml.y;
+            for (int o = 16; o > 0; o >>= 1) L += __shfl_xor_sync(0xffffffffu, L, o);
+            float acc[PER_LANE];
+#pragma unroll
+            for (int e = 0; e < PER_LANE; ++e) acc[e] = 0.f;
+            for (int s = 0; s < c.nsplit; ++s) {
+                const float fs = __shfl_sync(0xffffffffu, f, s);
+                const float *src = p.part_o + (pr0 + s) * D + lane * PER_LANE;
+#pragma unroll
+                for (int e = 0; e < PER_LANE; ++e) acc[e] += fs * src[e];
+            }
+            const float inv = L > 0.f ? 1.f / L : 0.f;
+            __nv_bfloat16 *dst = reinterpret_cast<__nv_bfloat16 *>(p.out) +
+                                 ((int64_t)(c.t0 + row) * p.num_q_heads + h) * D + lane * PER_LANE;
+#pragma unroll
+            for (int e = 0; e < PER_LANE; e += 2)
+                *reinterpret_cast<uint32_t *>(dst + e) = pack_bf16x2(acc[e] * inv, acc[e + 1] * inv);
+        }
+    }
+}
+
+// ---------------------------------------------------------------------------
+// Balanced micro-batch split ("Ascend dual-stream parallel" article, section
+// 3.1, advanced method): nearest request boundary to total/2 over cumulative
+// query_lens, smallest k on ties, then the balance and length thresholds.
+// One CTA: a chunked block scan gives every boundary's cumulative count, and a
+// lexicographic (distance, k) minimum picks the boundary.
+// ---------------------------------------------------------------------------
+constexpr int kSplitThreads = 1024;
+
+__global__ void __launch_bounds__(kSplitThreads, 1)
+split_kernel(const int32_t *__restrict__ query_lens, int num_reqs, float balance_threshold,
+             int32_t length_threshold, int32_t *out3)
+{
+    __shared__ long long warp_tot[kSplitThreads / 32];
+    __shared__ unsigned long long warp_best[kSplitThreads / 32];
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    if (num_reqs < 2) {
+        if (threadIdx.x == 0) {
+            out3[0] = 0;
+            out3[1] = 0;
+            out3[2] = 0;
+        }
+        return;
+    }
+    // total
+    long long tot = 0;
+    for (int r = threadIdx.x; r < num_reqs; r += kSplitThreads) tot += query_lens[r];
+    for (int o = 16; o > 0; o >>= 1) tot += __shfl_xor_sync(0xffffffffu, tot, o);
+    if (lane == 0) warp_tot[warp] = tot;
+    __syncthreads();
+    long long total = 0;
+    for (int w = 0; w < kSplitThreads / 32; ++w) total += warp_tot[w];
+    __syncthreads();
+    const long long best = total / 2;
+    // cum_k = sum of query_lens[0 .. k-1] for k = 1 .. num_reqs-1, i.e. the
+    // inclusive prefix at r = k-1; key = (|cum_k - best| << 24 | k) -- k < 2^24
+    unsigned long long my_best = ~0ull;
+    long long carry = 0;
+    for (int base = 0; base < num_reqs - 1; base += kSplitThreads) {
+        const int r = base + threadIdx.x;
+        long long x = r < num_reqs - 1 ? query_lens[r] : 0;
+        for (int o = 1; o < 32; o <<= 1) {
+            long long y = __shfl_up_sync(0xffffffffu, x, o);
+            if (lane >= o) x += y;
+        }
+        if (lane == 31) warp_tot[warp] = x;
+        __syncthreads();
+        long long before = 0, chunk = 0;
+        for (int w = 0; w < kSplitThreads / 32; ++w) {
+            if (w < warp) before += warp_tot[w];
+            chunk += warp_tot[w];
+        }
+        __syncthreads();
+        if (r < num_reqs - 1) {
+            const long long cum = carry + before + x;
+            const long long diff = cum > best ? cum - best : best - cum;
+            const unsigned long long key = ((unsigned long long)diff << 24) | (unsigned long long)(r + 1);
+            if (key < my_best) my_best = key;
+        }
+        carry += chunk;
+    }
+    for (int o = 16; o > 0; o >>= 1) {
+        unsigned long long y = __shfl_xor_sync(0xffffffffu, my_best, o);
+        if (y < my_best) my_best = y;
+    }
+    if (lane == 0) warp_best[warp] = my_best;
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        unsigned long long b = ~0ull;
+        for (int w = 0; w < kSplitThreads / 32; ++w)
+            if (warp_best[w] < b) b = warp_best[w];
+        const int k = (int)(b & 0xFFFFFFull);
+        long long n1 = 0;
+        for (int r = 0; r < k; ++r) n1 += query_lens[r];
+        const long long n2 = total - n1;
+        const long long small = n1 < n2 ? n1 : n2;
+        int use_two = 0;
+        if (small > 0) {
+            const long long gap = n1 > n2 ? n1 - n2 : n2 - n1;
+            const bool balanced = (double)gap / (double)small <= (double)balance_threshold;
+            use_two = balanced && small >= (long long)length_threshold;
+        }
+        out3[0] = k;
+        out3[1] = (int32_t)n1;
+        out3[2] = use_two;
+    }
+}
+
+}  // namespace
+
+cudaError_t launch_kv_cache_write(const void *k, const void *v, const int64_t *slot_mapping, int64_t num_tokens,
+                                  int num_kv_heads, int head_dim, int page_size, int64_t num_pages, void *k_cache,
+                                  void *v_cache, uint32_t *dev_err, int num_sms, cudaStream_t s)
+{
+    const int64_t total = num_tokens * num_kv_heads * (head_dim / 8);
+    if (total == 0)
+        return cudaSuccess;
+    int64_t blocks = (total + 255) / 256;
+    const int64_t cap = (int64_t)num_sms * 8;
+    if (blocks > cap) blocks = cap;
+    if (head_dim == 128)
+        kv_write_kernel<16><<<(int)blocks, 256, 0, s>>>((const uint4 *)k, (const uint4 *)v, slot_mapping, num_tokens,
+                                                        num_kv_heads, page_size, num_pages, (uint4 *)k_cache,
+                                                        (uint4 *)v_cache, dev_err);
+    else
+        kv_write_kernel<8><<<(int)blocks, 256, 0, s>>>((const uint4 *)k, (const uint4 *)v, slot_mapping, num_tokens,
+                                                       num_kv_heads, page_size, num_pages, (uint4 *)k_cache,
+                                                       (uint4 *)v_cache, dev_err);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_combine(const CombineParams &p, int head_dim, int grid, cudaStream_t s)
+{
+    if (head_dim == 128)
+        combine_kernel<128><<<grid, 256, 0, s>>>(p);
+    else
+        combine_kernel<64><<<grid, 256, 0, s>>>(p);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_split_microbatch(const int32_t *query_lens, int num_reqs, float balance_threshold,
+                                    int32_t length_threshold, int32_t *out3, cudaStream_t s)
+{
+    split_kernel<<<1, kSplitThreads, 0, s>>>(query_lens, num_reqs, balance_threshold, length_threshold, out3);
+    return cudaGetLastError();
+}
+
+}  // namespace cpsa

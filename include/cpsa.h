@@ -1,0 +1,194 @@
+/*
+ * cpsa.h -- C ABI of libcpsa.so: chunked-prefill attention over a paged KV cache
+ * for NVIDIA GB300 (sm_103a).
+ *
+ * Sources of the operations (web pages, by title and section):
+ *   [CP]  "vLLM Chunked-Prefills" article (Sarathi-Serve chunked prefill), section
+ *         3.1 (chunks of a long prompt, each caching its KV; decode rows first in
+ *         the token budget) and 3.2.1 (chunked attention: a chunk's queries against
+ *         the cached history keys concatenated with its own keys, softmax, values).
+ *   [DS]  Ascend "dual-stream parallel for Qwen3 dense" article, section 3.1:
+ *         attn_metadata (num_actual_tokens, slot_mapping, seq_lens, query_lens,
+ *         block_table) and the choice of the micro-batch split point.
+ *   [CPP] vllm-ascend design page "Dynamic Chunked Pipeline Parallel (CPP)":
+ *         quadratic latency model, chunk-size solver, online calibration.
+ *
+ * Conventions for every entry point:
+ *   - bf16 tensors are passed as void* and hold IEEE bfloat16 values.
+ *   - Device pointers belong to the caller; the library never allocates device
+ *     memory, keeps no device state between calls, and never synchronises the
+ *     stream except in cpp_read_device_error.
+ *   - `stream` is a cudaStream_t (NULL = legacy default stream); all work is
+ *     enqueued on it in order.
+ *   - Return value: CPSA_OK, or a negative CPSA_ERR_* detected on the host, in
+ *     which case nothing was launched.
+ *   - Data-dependent problems found on the device (an index out of range, a bad
+ *     length) set bits in the caller's 32-bit device word `dev_err` with
+ *     atomicOr; the offending item is skipped and no kernel traps. Read and
+ *     clear the word with cpp_read_device_error.
+ *
+ * Layouts (row-major, innermost last):
+ *   q            [num_tokens][num_q_heads][head_dim]      bf16, token-major
+ *   k, v         [num_tokens][num_kv_heads][head_dim]     bf16, the new tokens' K/V
+ *   k/v_cache    [num_pages][num_kv_heads][page_size][head_dim] bf16
+ *   out          [num_tokens][num_q_heads][head_dim]      bf16
+ *   slot_mapping [num_tokens] int64: slot = page * page_size + offset; < 0 = padding
+ *   block_table  [num_reqs][max_blocks_per_req] int32 page indices; entries past a
+ *                request's last page are never read (any value, e.g. -1)
+ *   query_lens, seq_lens [num_reqs] int32: seq_len counts the cached history plus
+ *                the request's new tokens; the new tokens are the last query_len
+ *                positions and sit contiguously in q in request order.
+ * Supported shapes: head_dim 64 or 128; num_q_heads a multiple of num_kv_heads
+ * with at most 16 q heads per kv head; page_size a power of two in [8, 256];
+ * all base pointers 16-byte aligned.
+ */
+#ifndef CPSA_H
+#define CPSA_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* ---- host status codes ---------------------------------------------------- */
+#define CPSA_OK 0
+#define CPSA_ERR_NULL_ARG (-1)            /* a required pointer is NULL */
+#define CPSA_ERR_BAD_SHAPE (-2)           /* a size or count is negative / inconsistent */
+#define CPSA_ERR_MISALIGNED (-3)          /* a base pointer is not 16-byte aligned */
+#define CPSA_ERR_UNSUPPORTED (-4)         /* head_dim, head grouping or page_size not supported */
+#define CPSA_ERR_WORKSPACE_TOO_SMALL (-5) /* workspace below cpp_attn_workspace_min_bytes */
+#define CPSA_ERR_CUDA (-6)                /* a CUDA runtime call or launch failed */
+#define CPSA_ERR_NO_DEVICE (-7)           /* no usable sm_103 device is current */
+
+/* ---- device error flags (bits of *dev_err) --------------------------------- */
+#define CPSA_DEV_SLOT_OUT_OF_RANGE 0x01u  /* slot >= num_pages * page_size: token skipped */
+#define CPSA_DEV_PAGE_OUT_OF_RANGE 0x02u  /* block_table entry outside [0, num_pages): tile skipped */
+#define CPSA_DEV_SEQ_LT_QUERY 0x04u       /* seq_len < query_len or query_len < 0: request skipped */
+#define CPSA_DEV_TOKENS_MISMATCH 0x08u    /* sum(query_lens) != num_tokens: nothing computed */
+#define CPSA_DEV_SEQ_GT_TABLE 0x10u       /* seq_len > max_blocks_per_req * page_size: request skipped */
+#define CPSA_DEV_SPLITS_CLAMPED 0x20u     /* info: partials did not fit the workspace, one KV split used */
+#define CPSA_DEV_WAIT_TIMEOUT 0x40u       /* an on-chip wait hit its limit; outputs of this call invalid */
+
+/*
+ * Write the new tokens' K and V into their cache slots ([DS] section 3.1,
+ * slot_mapping: "map each token position to its slot").
+ *
+ * For each token t with s = slot_mapping[t] >= 0:
+ *   k_cache[s / page_size][h][s % page_size][:] = k[t][h][:]  for every kv head h,
+ *   and the same for v. A bit copy; other cache bytes are untouched.
+ * Tokens with s < 0 are padding and skipped; s >= num_pages * page_size sets
+ * CPSA_DEV_SLOT_OUT_OF_RANGE and the token is skipped. Duplicate slots within
+ * one call leave an unspecified one of the writers' values.
+ * Run it before cpp_chunked_prefill_attn on the same stream: attention reads the
+ * chunk's own K/V from the cache.
+ */
+int cpp_kv_cache_write(const void *k, const void *v, const int64_t *slot_mapping,
+                       int64_t num_tokens, int num_kv_heads, int head_dim, int page_size,
+                       int64_t num_pages, void *k_cache, void *v_cache, uint32_t *dev_err,
+                       void *stream);
+
+/*
+ * Workspace for cpp_chunked_prefill_attn, in bytes.
+ *
+ * cpp_attn_workspace_bytes is the size that lets every row use up to
+ * max_kv_splits KV splits (partial results are stored for every token and head
+ * in the worst case); cpp_attn_workspace_min_bytes is the metadata part alone.
+ * Any size in between is accepted: when a call's partial results do not fit,
+ * the call runs every row with one split and sets CPSA_DEV_SPLITS_CLAMPED.
+ * Returns 0 for invalid arguments.
+ */
+size_t cpp_attn_workspace_bytes(int num_reqs, int64_t num_tokens, int num_q_heads,
+                                int num_kv_heads, int head_dim, int max_kv_splits);
+size_t cpp_attn_workspace_min_bytes(int num_reqs, int64_t num_tokens, int num_q_heads,
+                                    int num_kv_heads, int head_dim, int max_kv_splits);
+
+/*
+ * Causal chunked-prefill attention over the paged cache, mixed with decode rows
+ * ([CP] section 3.2.1 for the computation, [DS] section 3.1 for the metadata).
+ *
+ * For request r with q_r = query_lens[r], s_r = seq_lens[r], h_r = s_r - q_r, new
+ * token i (0 <= i < q_r, global row t = sum_{r'<r} q_r' + i) and q head h:
+ *   keys j = 0 .. h_r + i of kv head h / (num_q_heads / num_kv_heads), key j at
+ *   k_cache[block_table[r][j / page_size]][kvh][j % page_size];
+ *   out[t][h] = sum_j softmax_j(scale * q[t][h] . k_j) * v_j      (bf16 result)
+ * scale <= 0 selects 1 / sqrt(head_dim). A request with q_r = 1 is a decode row
+ * and takes the split-KV decode kernel; q_r >= 2 takes the tensor-core chunk
+ * kernel; q_r = 0 contributes nothing. Arithmetic: bf16 inputs, fp32
+ * accumulation and softmax, probabilities rounded to bf16 before P.V.
+ *
+ * max_kv_splits (>= 1) caps the number of KV splits of one row; the split count
+ * of a row depends only on its own (query_len, seq_len) and max_kv_splits, so a
+ * request's output does not depend on the rest of the batch.
+ * workspace: device memory of at least cpp_attn_workspace_min_bytes(...) with
+ * the same (num_reqs, num_tokens, heads, head_dim, max_kv_splits); it is
+ * scratch, overwritten by each call; calls that share it must be stream-ordered.
+ */
+int cpp_chunked_prefill_attn(const void *q, const void *k_cache, const void *v_cache,
+                             const int32_t *query_lens, const int32_t *seq_lens,
+                             const int32_t *block_table, int num_reqs, int64_t num_tokens,
+                             int max_blocks_per_req, int num_q_heads, int num_kv_heads,
+                             int head_dim, int page_size, int64_t num_pages, float scale,
+                             int max_kv_splits, void *out, void *workspace,
+                             size_t workspace_bytes, uint32_t *dev_err, void *stream);
+
+/*
+ * Balanced micro-batch split point ([DS] section 3.1, "advanced method").
+ *
+ * total = sum(query_lens); best = total / 2 (integer); over request boundaries
+ * k = 1 .. num_reqs-1 with cum_k = sum_{r<k} query_lens[r], pick the k nearest to
+ * best (smallest k on ties); n1 = cum_k, n2 = total - n1;
+ * use_two = |n1 - n2| / min(n1, n2) <= balance_threshold and
+ *           min(n1, n2) >= length_threshold (and min > 0).
+ * Writes out3[0] = k (batch split), out3[1] = n1 (token split), out3[2] = use_two
+ * into DEVICE memory; num_reqs < 2 gives (0, 0, 0). query_lens must be >= 0.
+ */
+int cpp_split_microbatch(const int32_t *query_lens, int num_reqs, float balance_threshold,
+                         int32_t length_threshold, int32_t *out3, void *stream);
+
+/*
+ * Copy the device error word to *host_flags (synchronises `stream`), and reset
+ * it to zero when clear != 0.
+ */
+int cpp_read_device_error(uint32_t *dev_err, uint32_t *host_flags, int clear, void *stream);
+
+/*
+ * Host-side chunk planner ([CPP] "runtime phase: dynamic prediction").
+ *
+ * Latency model f(l) = a l^2 + b l + c; target T = f(base_chunk_size) - f(0).
+ * From prefix L, the next chunk x solves f(L + x) - f(L) = T (positive root,
+ * evaluated as 2T / ((2aL+b) + sqrt((2aL+b)^2 + 4aT)); a <= 0 gives T / b, and
+ * b <= 0 as well gives base_chunk_size); then x is blended with base by
+ * smooth_factor (x_s = s x + (1 - s) base), rounded down to a multiple of
+ * page_size (relative slack 1e-9) with a minimum of min_chunk, capped at
+ * max_model_len - L and max_num_scheduled_tokens (values <= 0 mean no cap), and
+ * at the remaining prompt. Writes up to max_chunks sizes; *n_chunks gets the
+ * count needed. Returns CPSA_ERR_BAD_SHAPE if chunks was too short.
+ */
+int cpp_plan_chunk_sizes(double a, double b, double c, int64_t prompt_len,
+                         int64_t base_chunk_size, int page_size, int64_t min_chunk,
+                         int64_t max_model_len, int64_t max_num_scheduled_tokens,
+                         double smooth_factor, int64_t *chunks, int64_t max_chunks,
+                         int64_t *n_chunks);
+
+/*
+ * Least-squares fits of the latency models ([CPP] "startup phase: profiling" and
+ * "online calibration"). n samples; coef[3] = (a, b, c).
+ *   quadratic: f(l) = a l^2 + b l + c, samples (l[i], t[i]);
+ *   two-variable: f(C, H) = a C (C + H) + b (C + H) + c, with per-sample
+ *   features x0 = sum C (C + H), x1 = sum (C + H), x2 = number of chunks.
+ * Returns CPSA_ERR_BAD_SHAPE when n < 3 or the system is singular.
+ */
+int cpp_fit_latency_quadratic(const double *l, const double *t, int n, double *coef);
+int cpp_fit_latency_two_var(const double *x0, const double *x1, const double *x2,
+                            const double *t, int n, double *coef);
+
+/* Human-readable name of a status code. */
+const char *cpp_status_string(int status);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* CPSA_H */

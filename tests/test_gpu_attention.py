@@ -1,0 +1,131 @@
+"""GPU parity of cpp_chunked_prefill_attn against the fp64 oracle.
+
+Every batch here is small enough for the oracle to compute every row; the
+caches start as NaN patterns, so a kernel that touches an unwritten slot
+without masking it produces NaN and fails. Bound: max-abs 2e-2 and relative
+Frobenius 5e-3 (bf16 inputs, fp32 accumulation, bf16 P and output)."""
+import numpy as np
+import pytest
+
+import oracle
+import workloads as W
+from helpers import compare, oracle_caches, run_gpu_batch
+
+pytestmark = pytest.mark.gpu
+
+
+def check(cpsa, spec, max_kv_splits=8, workspace_bytes=None, scale=0.0, expect_flags=0):
+    b = W.make_batch(spec)
+    got, flags, _, _ = run_gpu_batch(cpsa, b, max_kv_splits=max_kv_splits, workspace_bytes=workspace_bytes,
+                                     scale=scale)
+    assert flags == expect_flags, f"device flags {flags:#x}"
+    kc, vc = oracle_caches(b)
+    ref = oracle.paged_attention(b.q, kc, vc, b.query_lens, b.seq_lens, b.block_table, scale=scale)
+    return compare(got, ref, what=spec.name or str(spec.qlen))
+
+
+def test_small_chunk_workload(cuda_lib):
+    """History 256 + chunk 128, 4/4 heads, d=64, page 16."""
+    check(cuda_lib, W.spec_one_chunk_small())
+
+
+@pytest.mark.parametrize("d", [64, 128])
+@pytest.mark.parametrize("hq,hkv", [(4, 4), (8, 2), (32, 8), (6, 2), (16, 1)])
+def test_heads_and_dims(cuda_lib, d, hq, hkv):
+    spec = W.BatchSpec(hist=[130, 0, 7], qlen=[200, 129, 1], num_q_heads=hq, num_kv_heads=hkv, head_dim=d,
+                       page_size=16, seed=100 + hq + d)
+    check(cuda_lib, spec)
+
+
+@pytest.mark.parametrize("P", [8, 16, 32, 64, 128, 256])
+def test_page_sizes(cuda_lib, P):
+    spec = W.BatchSpec(hist=[300, 1000, 0], qlen=[77, 1, 260], num_q_heads=8, num_kv_heads=2, head_dim=128,
+                       page_size=P, seed=200 + P, extra_pages=5)
+    check(cuda_lib, spec)
+
+
+def test_ragged_mixed_batch(cuda_lib):
+    """Decode rows first, then chunks with ragged tails, a zero-length request inside."""
+    spec = W.BatchSpec(hist=[900, 33, 4000, 0, 511, 512, 513, 0, 77],
+                       qlen=[1, 1, 1, 2, 128, 127, 129, 0, 383],
+                       num_q_heads=32, num_kv_heads=8, head_dim=128, page_size=16, seed=300)
+    check(cuda_lib, spec)
+
+
+@pytest.mark.parametrize("splits", [1, 2, 8])
+def test_long_history_splits(cuda_lib, splits):
+    """Long histories: prefill tiles past 32 KV tiles and decode rows past 4096 keys split."""
+    spec = W.BatchSpec(hist=[9000, 5000, 6000], qlen=[1, 150, 1], num_q_heads=8, num_kv_heads=2,
+                       head_dim=128, page_size=16, seed=400 + splits)
+    check(cuda_lib, spec, max_kv_splits=splits)
+
+
+def test_workspace_clamp_still_correct(cuda_lib):
+    spec = W.BatchSpec(hist=[9000, 5000], qlen=[1, 150], num_q_heads=8, num_kv_heads=2, head_dim=128,
+                       page_size=16, seed=450)
+    minb = cuda_lib.cpp_attn_workspace_min_bytes(2, 151, 8, 2, 128, 8)
+    check(cuda_lib, spec, max_kv_splits=8, workspace_bytes=minb, expect_flags=cuda_lib.DEV_SPLITS_CLAMPED)
+
+
+def test_custom_scale(cuda_lib):
+    spec = W.BatchSpec(hist=[64], qlen=[64], num_q_heads=4, num_kv_heads=2, head_dim=64, page_size=16, seed=500)
+    check(cuda_lib, spec, scale=0.3)
+
+
+def test_decode_only_batch(cuda_lib):
+    rng = np.random.default_rng(3)
+    ctx = [int(x) for x in rng.integers(1, 3000, size=40)]
+    spec = W.BatchSpec(hist=[c - 1 for c in ctx], qlen=[1] * 40, num_q_heads=32, num_kv_heads=8, head_dim=128,
+                       page_size=16, seed=501)
+    check(cuda_lib, spec)
+
+
+def test_tiny_prefills(cuda_lib):
+    spec = W.BatchSpec(hist=[0, 1, 2, 15, 16, 17], qlen=[2, 2, 3, 1, 5, 16], num_q_heads=4, num_kv_heads=1,
+                       head_dim=64, page_size=8, seed=502)
+    check(cuda_lib, spec)
+
+
+def test_device_errors_are_flagged_not_faulted(cuda_lib):
+    import torch
+    spec = W.BatchSpec(hist=[10, 20], qlen=[5, 1], num_q_heads=4, num_kv_heads=2, head_dim=64, page_size=16,
+                       seed=503)
+    b = W.make_batch(spec)
+    # seq_len < query_len on request 0
+    bad = W.make_batch(spec)
+    bad.seq_lens = bad.seq_lens.copy()
+    bad.seq_lens[0] = 2
+    _, flags, _, _ = run_gpu_batch(cuda_lib, bad)
+    assert flags & cuda_lib.DEV_SEQ_LT_QUERY
+    # a block_table entry past the pool
+    bt = b.block_table.copy()
+    bt[1, 0] = b.num_pages + 5
+    _, flags, _, _ = run_gpu_batch(cuda_lib, b, block_table=bt)
+    assert flags & cuda_lib.DEV_PAGE_OUT_OF_RANGE
+    # sum(query_lens) != num_tokens
+    mm = W.make_batch(spec)
+    mm.query_lens = np.array([4, 1], dtype=np.int32)
+    _, flags, _, _ = run_gpu_batch(cuda_lib, mm)
+    assert flags & cuda_lib.DEV_TOKENS_MISMATCH
+    torch.cuda.synchronize()
+
+
+def test_host_argument_errors(cuda_lib):
+    import torch
+    q = torch.zeros((4, 4, 96), dtype=torch.bfloat16, device="cuda")
+    kc = torch.zeros((2, 2, 16, 96), dtype=torch.bfloat16, device="cuda")
+    ql = torch.tensor([4], dtype=torch.int32, device="cuda")
+    bt = torch.zeros((1, 2), dtype=torch.int32, device="cuda")
+    ws = torch.empty(1 << 20, dtype=torch.uint8, device="cuda")
+    e = torch.zeros(1, dtype=torch.int32, device="cuda")
+    with pytest.raises(cuda_lib.CpsaError):    # head_dim 96 unsupported
+        cuda_lib.cpp_chunked_prefill_attn(q, kc, kc.clone(), ql, ql.clone(), bt, q.clone(), ws, e)
+    q = torch.zeros((4, 4, 64), dtype=torch.bfloat16, device="cuda")
+    kc = torch.zeros((2, 2, 12, 64), dtype=torch.bfloat16, device="cuda")
+    with pytest.raises(cuda_lib.CpsaError):    # page size 12 unsupported
+        cuda_lib.cpp_chunked_prefill_attn(q, kc, kc.clone(), ql, ql.clone(), bt, q.clone(), ws, e)
+    kc = torch.zeros((2, 2, 16, 64), dtype=torch.bfloat16, device="cuda")
+    tiny = torch.empty(16, dtype=torch.uint8, device="cuda")
+    with pytest.raises(cuda_lib.CpsaError):    # workspace too small
+        cuda_lib.cpp_chunked_prefill_attn(q, kc, kc.clone(), ql, ql.clone(), bt, q.clone(), tiny, e)
+    assert cuda_lib.cpp_read_device_error(e) == 0
