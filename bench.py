@@ -1,0 +1,448 @@
+#!/usr/bin/env python
+"""Benchmark of the chunked-prefill attention hot path on GB300.
+
+Step = one pass of the whole path over the headline workload: a Llama-3-8B-shaped
+attention layer (32 q / 8 kv heads, head_dim 128, bf16, page 128) prefilling one
+32768-token sequence in 64 chunks of 512; per chunk the micro-batch split, the
+slot_mapping KV write and the causal attention over the paged cache.
+
+Prints one JSON line (rank 0). `value` is attention TFLOP/s of the whole step
+(algorithmic FLOPs: 4*d*Hq*sum_i (h + i + 1), unmasked pairs only) with inputs
+resident in HBM; `e2e` is the same metric through the C ABI with host buffers
+(pinned host->device copies of each chunk's q/k/v/slots and the device->host
+read of its output inside the timed region); `roofline` is the chunk kernel's
+own event-timed throughput against the measured bf16 peak; `cpu_baseline` is
+the fp64 oracle on a bounded sample of the same workload on the host cores.
+`--impl reference` times that oracle alone on the workload's own metric.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+SEQ, CHUNK, HQ, HKV, D, PAGE = 32768, 512, 32, 8, 128, 128
+N_CHUNKS = SEQ // CHUNK
+WORKLOAD = "llama3-8b-attn-layer 32768-token prefill in 64 chunks of 512 (32/8 heads, d128, bf16, page 128)"
+METRIC = "chunked-prefill attention TFLOP/s"
+
+
+def chunk_flops(h, c, hq=HQ, d=D):
+    """Algorithmic FLOPs of one chunk: QK^T and PV over the unmasked (query, key) pairs."""
+    pairs = c * h + c * (c + 1) // 2
+    return 4.0 * d * hq * pairs
+
+
+STEP_FLOPS = sum(chunk_flops(i * CHUNK, CHUNK) for i in range(N_CHUNKS))
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            p = json.load(f)
+        return float(p["bf16_tflops"]), float(p["hbm_gbs"]), "measured"
+    except Exception:
+        return 1900.0, 6800.0, "fallback"
+
+
+# ----------------------------------------------------------------------------- clocks
+class ClockSampler:
+    """nvidia-smi sampling of SM clock and throttle reasons during the timed region."""
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_id: str | None):
+        self.gpu_id = gpu_id
+        self.proc = None
+        self.lines = []
+
+    def start(self):
+        cmd = ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits", "-lms", "200"]
+        if self.gpu_id:
+            cmd += ["-i", self.gpu_id]
+        try:
+            self.proc = subprocess.Popen(cmd, stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.thread = threading.Thread(target=self._read, daemon=True)
+            self.thread.start()
+        except Exception:
+            self.proc = None
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        self.thread.join(timeout=2)
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            parts = [x.strip() for x in ln.split(",")]
+            if len(parts) < 8:
+                continue
+            try:
+                sm.append(float(parts[0]))
+                mx.append(float(parts[1]))
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[4:8]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        return {"sm_mhz": float(np.median(sm)) if sm else None, "sm_max_mhz": max(mx) if mx else None,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ----------------------------------------------------------------------------- GPU workload
+def draw_inputs(dev, seed=2):
+    """Seeded inputs of the headline workload (see workloads.device_sequence)."""
+    import workloads as W
+    return W.device_sequence(SEQ, PAGE, HQ, HKV, D, seed=seed, device=dev)
+
+
+class ChunkedPrefill:
+    """Device buffers of the headline workload and its step."""
+
+    def __init__(self, dev, seed=2, max_kv_splits=8):
+        import torch
+        import chunked_prefill_paged_slot_gb300 as cpsa
+        self.torch, self.cpsa, self.dev = torch, cpsa, dev
+        n_pages = SEQ // PAGE
+        bf = torch.bfloat16
+        self.q, self.k, self.v, self.slots, self.bt = draw_inputs(dev, seed)
+        self.k_cache = torch.zeros((n_pages, HKV, PAGE, D), dtype=bf, device=dev)
+        self.v_cache = torch.zeros_like(self.k_cache)
+        self.out = torch.empty_like(self.q)
+        self.qlens = torch.full((N_CHUNKS, 1), CHUNK, dtype=torch.int32, device=dev)
+        self.slens = torch.tensor([[CHUNK * (i + 1)] for i in range(N_CHUNKS)], dtype=torch.int32, device=dev)
+        self.max_kv_splits = max_kv_splits
+        self.ws = torch.empty(cpsa.cpp_attn_workspace_bytes(1, CHUNK, HQ, HKV, D, max_kv_splits),
+                              dtype=torch.uint8, device=dev)
+        self.err = torch.zeros(1, dtype=torch.int32, device=dev)
+        self.split_out = torch.zeros(3, dtype=torch.int32, device=dev)
+        self.marks = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(N_CHUNKS)]
+        self.host = None
+
+    def chunk(self, i, q, k, v, slots, out, stream, marks=None):
+        cpsa = self.cpsa
+        cpsa.cpp_split_microbatch(self.qlens[i], self.split_out, 0.1, 256, stream=stream)
+        cpsa.cpp_kv_cache_write(k, v, slots, self.k_cache, self.v_cache, self.err, stream=stream)
+        if marks is None:
+            cpsa.cpp_chunked_prefill_attn(q, self.k_cache, self.v_cache, self.qlens[i], self.slens[i], self.bt, out,
+                                          self.ws, self.err, max_kv_splits=self.max_kv_splits, stream=stream)
+        else:
+            cpsa.cpp_chunked_prefill_attn_events(q, self.k_cache, self.v_cache, self.qlens[i], self.slens[i], self.bt,
+                                                 out, self.ws, self.err, [None, marks[0], marks[1], None, None],
+                                                 max_kv_splits=self.max_kv_splits, stream=stream)
+
+    def step(self, stream, with_marks=False):
+        for i in range(N_CHUNKS):
+            a, b = i * CHUNK, (i + 1) * CHUNK
+            self.chunk(i, self.q[a:b], self.k[a:b], self.v[a:b], self.slots[a:b], self.out[a:b], stream,
+                       self.marks[i] if with_marks else None)
+
+    def chunk_kernel_ms(self):
+        return [self.marks[i][0].elapsed_time(self.marks[i][1]) for i in range(N_CHUNKS)]
+
+    # host-buffer variant for the end-to-end number
+    def make_host(self):
+        torch = self.torch
+        pin = lambda t: t.cpu().pin_memory()
+        self.host = dict(q=pin(self.q), k=pin(self.k), v=pin(self.v), slots=pin(self.slots),
+                         out=torch.empty(self.out.shape, dtype=self.out.dtype).pin_memory())
+        self.dq = torch.empty((CHUNK, HQ, D), dtype=torch.bfloat16, device=self.dev)
+        self.dk = torch.empty((CHUNK, HKV, D), dtype=torch.bfloat16, device=self.dev)
+        self.dv = torch.empty_like(self.dk)
+        self.ds = torch.empty(CHUNK, dtype=torch.int64, device=self.dev)
+        self.dout = torch.empty_like(self.dq)
+        h2d = (self.dq.numel() + self.dk.numel() + self.dv.numel()) * 2 + self.ds.numel() * 8
+        return h2d * N_CHUNKS, self.dout.numel() * 2 * N_CHUNKS
+
+    def step_e2e(self, stream):
+        h = self.host
+        with self.torch.cuda.stream(stream):
+            for i in range(N_CHUNKS):
+                a, b = i * CHUNK, (i + 1) * CHUNK
+                self.dq.copy_(h["q"][a:b], non_blocking=True)
+                self.dk.copy_(h["k"][a:b], non_blocking=True)
+                self.dv.copy_(h["v"][a:b], non_blocking=True)
+                self.ds.copy_(h["slots"][a:b], non_blocking=True)
+                self.chunk(i, self.dq, self.dk, self.dv, self.ds, self.dout, stream)
+                h["out"][a:b].copy_(self.dout, non_blocking=True)
+
+
+# ----------------------------------------------------------------------------- oracle (CPU) leg
+def oracle_sample(q, k, v, slots, bt, rows_per_chunk, rng, chunks=None):
+    """Run the fp64 oracle on sampled rows of the workload; returns (seconds, flops, rows)."""
+    import oracle
+    import workloads as W
+    n_pages = SEQ // PAGE
+    kc = np.full((n_pages, HKV, PAGE, D), W.BF16_NAN_SENTINEL, dtype=np.uint16)
+    vc = kc.copy()
+    oracle.kv_cache_write(k, v, slots, PAGE, kc, vc)   # whole sequence cached (history of every chunk)
+    chunks = range(N_CHUNKS) if chunks is None else chunks
+    total_s, flops, n = 0.0, 0.0, 0
+    for i in chunks:
+        h = i * CHUNK
+        rows = np.sort(rng.choice(CHUNK, size=rows_per_chunk, replace=False))
+        t0 = time.perf_counter()
+        oracle.paged_attention(q[h:h + CHUNK], kc, vc, [CHUNK], [h + CHUNK], bt, rows=rows)
+        total_s += time.perf_counter() - t0
+        flops += sum(4.0 * D * HQ * (h + int(r) + 1) for r in rows)
+        n += len(rows)
+    return total_s, flops, n
+
+
+def host_inputs(seed=2):
+    """Host copies (uint16 bit patterns) of the workload's inputs, drawn on the device."""
+    import torch
+    q, k, v, slots, bt = draw_inputs(torch.device("cuda"), seed)
+    to16 = lambda t: t.view(torch.int16).cpu().numpy().view(np.uint16)
+    return (to16(q), to16(k), to16(v), slots.cpu().numpy(), bt.cpu().numpy())
+
+
+def cpu_baseline(inputs, budget_s=12.0):
+    import oracle
+    q, k, v, slots, bt = inputs
+    rng = np.random.default_rng(0)
+    # calibrate on one row of the last chunk, then size the sample to ~budget_s
+    s1, f1, _ = oracle_sample(q, k, v, slots, bt, 1, rng, chunks=[N_CHUNKS - 1])
+    per_flop = s1 / f1
+    avg_row_flops = STEP_FLOPS / SEQ
+    rows_per_chunk = int(max(1, min(CHUNK, budget_s / (per_flop * avg_row_flops * N_CHUNKS))))
+    s, f, n = oracle_sample(q, k, v, slots, bt, rows_per_chunk, rng)
+    return {"value": f / s / 1e12, "unit": "TFLOP/s", "cores": oracle.num_threads(), "kind": "oracle",
+            "sample": f"{n} query rows ({rows_per_chunk} per chunk, all 32 heads) across the 64 chunks; "
+                      f"{f / 1e9:.1f} GFLOP fp64 in {s:.1f} s"}
+
+
+# ----------------------------------------------------------------------------- secondary: decode bandwidth
+def decode_bandwidth(dev, reps=5):
+    """Decode-row HBM GB/s on the Sarathi mixed step (1536 decode rows + one 512 chunk at h=8192)."""
+    import torch
+    import chunked_prefill_paged_slot_gb300 as cpsa
+    import workloads as W
+    spec = W.spec_sarathi_mixed()
+    d = W.device_batch(spec, device=dev)
+    B, T = len(spec.qlen), sum(spec.qlen)
+    ws = torch.empty(cpsa.cpp_attn_workspace_bytes(B, T, HQ, HKV, D, 8), dtype=torch.uint8, device=dev)
+    out = torch.empty_like(d["q"])
+    err = torch.zeros(1, dtype=torch.int32, device=dev)
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(5)]
+    cpsa.cpp_kv_cache_write(d["k"], d["v"], d["slot_mapping"], d["k_cache"], d["v_cache"], err)
+    dec_ms, chunk_ms, step_ms = [], [], []
+    for r in range(reps + 2):
+        flush.zero_()
+        cpsa.cpp_chunked_prefill_attn_events(d["q"], d["k_cache"], d["v_cache"], d["query_lens"], d["seq_lens"],
+                                             d["block_table"], out, ws, err, ev, max_kv_splits=8)
+        torch.cuda.synchronize()
+        if r >= 2:
+            chunk_ms.append(ev[1].elapsed_time(ev[2]))
+            dec_ms.append(ev[2].elapsed_time(ev[3]))
+            step_ms.append(ev[0].elapsed_time(ev[4]))
+    flags = cpsa.cpp_read_device_error(err)
+    n_dec = sum(1 for x in spec.qlen if x == 1)
+    ctx = np.array(spec.seq[:n_dec], dtype=np.float64)
+    dec_bytes = float(ctx.sum()) * HKV * D * 2 * 2 + n_dec * HQ * D * 2 * 2
+    chunk_f = chunk_flops(spec.hist[-1], spec.qlen[-1])
+    res = {"workload": "sarathi mixed step: 1536 decode rows (context U[1024,8192]) + one 512-token chunk at "
+                       "h=8192, 32/8 heads, d128, page 16, L2 flushed",
+           "decode_kernel_ms": float(np.median(dec_ms)),
+           "decode_hbm_gbs": dec_bytes / (np.median(dec_ms) * 1e-3) / 1e9,
+           "decode_bytes": dec_bytes,
+           "chunk_kernel_ms": float(np.median(chunk_ms)),
+           "chunk_tflops": chunk_f / (np.median(chunk_ms) * 1e-3) / 1e12,
+           "attn_call_ms": float(np.median(step_ms)), "device_flags": flags}
+    del d, ws, out, flush
+    torch.cuda.empty_cache()
+    return res
+
+
+# ----------------------------------------------------------------------------- main
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-secondary", action="store_true")
+    args = ap.parse_args()
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+
+    if args.impl == "reference":
+        return reference_arm(args, world, rank)
+
+    import torch
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=dev)
+    import chunked_prefill_paged_slot_gb300 as cpsa
+    cpsa.load()
+
+    wl = ChunkedPrefill(dev)
+    stream = torch.cuda.current_stream(dev)
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)   # > L2 (129 MB)
+    for _ in range(max(3, args.warmup)):
+        wl.step(stream)
+    torch.cuda.synchronize()
+    if cpsa.cpp_read_device_error(wl.err) != 0:
+        raise SystemExit("device error flags set during warm-up")
+
+    gpu_uuid = None
+    try:
+        gpu_uuid = str(torch.cuda.get_device_properties(dev).uuid)
+        gpu_uuid = gpu_uuid if gpu_uuid.startswith("GPU-") else "GPU-" + gpu_uuid
+    except Exception:
+        pass
+    clocks = ClockSampler(gpu_uuid)
+    ev0 = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    ev1 = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    kernel_ms = []
+    enqueue_s = []
+    if dist: dist.barrier()
+    torch.cuda.synchronize()
+    clocks.start()
+    t_wall = time.perf_counter()
+    for s in range(args.steps):
+        flush.zero_()
+        ev0[s].record(stream)
+        te = time.perf_counter()
+        wl.step(stream, with_marks=True)
+        enqueue_s.append(time.perf_counter() - te)
+        ev1[s].record(stream)
+        torch.cuda.synchronize()
+        kernel_ms.append(wl.chunk_kernel_ms())
+    torch.cuda.synchronize()
+    if dist: dist.barrier()
+    wall = time.perf_counter() - t_wall
+    clk = clocks.stop()
+    step_ms = [ev0[s].elapsed_time(ev1[s]) for s in range(args.steps)]
+    total_ms = float(sum(step_ms))
+    if dist:
+        t = torch.tensor([total_ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        total_ms = float(t.item())
+    flags = cpsa.cpp_read_device_error(wl.err)
+    ms_per_step = total_ms / args.steps
+    value = world * STEP_FLOPS * args.steps / (total_ms * 1e-3) / 1e12
+
+    # end-to-end through host buffers
+    h2d, d2h = wl.make_host()
+    for _ in range(2):
+        wl.step_e2e(stream)
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e2e_ms = []
+    for s in range(max(1, args.steps // 2)):
+        flush.zero_()
+        e0.record(stream)
+        wl.step_e2e(stream)
+        e1.record(stream)
+        torch.cuda.synchronize()
+        e2e_ms.append(e0.elapsed_time(e1))
+    e2e_val = world * STEP_FLOPS / (float(np.mean(e2e_ms)) * 1e-3) / 1e12
+
+    # roofline of the dominant kernel (the tensor-core chunk kernel)
+    peak_tf, peak_bw, peak_src = load_peaks()
+    km = np.asarray(kernel_ms)                       # [steps, chunks]
+    per_launch_ms = float(km.mean())
+    per_launch_flops = STEP_FLOPS / N_CHUNKS
+    achieved = per_launch_flops / (per_launch_ms * 1e-3) / 1e12
+    roofline = {"bound": "tensor", "achieved": round(achieved, 2), "peak": peak_tf, "unit": "TFLOP/s",
+                "frac": round(achieved / peak_tf, 4), "traffic": None,
+                "kernel": "chunk_attn_kernel<128,2>", "peak_source": f"{peak_src} bf16 dense (burst)",
+                "per_launch_flops": per_launch_flops, "per_launch_ms": round(per_launch_ms, 4),
+                "last_chunk_ms": round(float(km[:, -1].mean()), 4),
+                "last_chunk_tflops": round(chunk_flops((N_CHUNKS - 1) * CHUNK, CHUNK) / (km[:, -1].mean() * 1e-3) / 1e12, 2)}
+    launches = args.steps * N_CHUNKS * 6
+
+    line = {"metric": METRIC, "value": round(value, 3), "unit": "TFLOP/s", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_per_step, 4),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+            "data": "synthetic (seeded N(0,1) bf16 q/k/v, permuted page pool)",
+            "config": {"workload": WORKLOAD, "global_batch": world, "seq_len": SEQ, "chunk": CHUNK,
+                       "parallelism": "replicas" if world > 1 else "single-gpu",
+                       "l2": "flushed between steps (256 MB write)", "max_kv_splits": wl.max_kv_splits,
+                       "step_flops": STEP_FLOPS},
+            "e2e": {"value": round(e2e_val, 3), "unit": "TFLOP/s", "h2d_bytes_per_step": h2d,
+                    "d2h_bytes_per_step": d2h, "ms_per_step": round(float(np.mean(e2e_ms)), 4)},
+            "roofline": roofline, "gpu_launches": launches, "clocks": clk,
+            "wall_s": round(wall, 3), "host_enqueue_ms_per_step": round(1e3 * float(np.mean(enqueue_s)), 3),
+            "device_flags": flags}
+    if not args.no_secondary and rank == 0:
+        del wl
+        torch.cuda.empty_cache()
+        try:
+            line["secondary"] = decode_bandwidth(dev)
+            line["secondary"]["hbm_peak_gbs"] = peak_bw
+            line["secondary"]["decode_frac_of_hbm"] = round(line["secondary"]["decode_hbm_gbs"] / peak_bw, 4)
+        except Exception as e:  # keep the headline line even if the secondary run fails
+            line["secondary"] = {"error": repr(e)}
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(host_inputs())
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if dist:
+        dist.destroy_process_group()
+
+
+def reference_arm(args, world, rank):
+    """The oracle (fp64, host cores) timed on the same workload and metric."""
+    if rank != 0:
+        return
+    import torch
+    import oracle
+    oracle.build()
+    inputs = host_inputs()
+    q, k, v, slots, bt = inputs
+    rng = np.random.default_rng(1)
+    # size one step's sample to ~2 s of CPU work
+    s1, f1, _ = oracle_sample(q, k, v, slots, bt, 1, rng, chunks=[N_CHUNKS - 1])
+    rows = int(max(1, min(CHUNK, 2.0 / (s1 / f1 * STEP_FLOPS / SEQ * N_CHUNKS))))
+    for _ in range(args.warmup):
+        oracle_sample(q, k, v, slots, bt, 1, rng, chunks=[0])
+    tot_s, tot_f, tot_n = 0.0, 0.0, 0
+    for _ in range(args.steps):
+        s, f, n = oracle_sample(q, k, v, slots, bt, rows, rng)
+        tot_s += s
+        tot_f += f
+        tot_n += n
+    val = tot_f / tot_s / 1e12
+    sample = f"{rows} query rows per chunk x 64 chunks per step (all 32 heads); {tot_n} rows, {tot_f / 1e9:.1f} GFLOP"
+    print(json.dumps({"impl": "reference", "metric": METRIC, "value": val, "unit": "TFLOP/s", "n_gpus": world,
+                      "steps": args.steps, "warmup": args.warmup, "ms_per_step": tot_s * 1e3 / args.steps,
+                      "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+                      "data": "synthetic", "config": {"workload": WORKLOAD, "seq_len": SEQ, "chunk": CHUNK},
+                      "cpu_baseline": {"value": val, "unit": "TFLOP/s", "cores": oracle.num_threads(),
+                                       "kind": "oracle", "sample": sample},
+                      "e2e": {"value": val, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}),
+          flush=True)
+    del torch
+
+
+if __name__ == "__main__":
+    main()

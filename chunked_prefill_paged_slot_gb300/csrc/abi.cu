@@ -152,6 +152,27 @@ int cpp_chunked_prefill_attn(const void *q, const void *k_cache, const void *v_c
                              int64_t num_pages, float scale, int max_kv_splits, void *out, void *workspace,
                              size_t workspace_bytes, uint32_t *dev_err, void *stream)
 {
+    return cpp_chunked_prefill_attn_events(q, k_cache, v_cache, query_lens, seq_lens, block_table, num_reqs,
+                                           num_tokens, max_blocks_per_req, num_q_heads, num_kv_heads, head_dim,
+                                           page_size, num_pages, scale, max_kv_splits, out, workspace,
+                                           workspace_bytes, dev_err, stream, nullptr);
+}
+
+int cpp_chunked_prefill_attn_events(const void *q, const void *k_cache, const void *v_cache,
+                                    const int32_t *query_lens, const int32_t *seq_lens, const int32_t *block_table,
+                                    int num_reqs, int64_t num_tokens, int max_blocks_per_req, int num_q_heads,
+                                    int num_kv_heads, int head_dim, int page_size, int64_t num_pages, float scale,
+                                    int max_kv_splits, void *out, void *workspace, size_t workspace_bytes,
+                                    uint32_t *dev_err, void *stream, void *const *events)
+{
+    cudaEvent_t ev[5] = {nullptr, nullptr, nullptr, nullptr, nullptr};
+    if (events)
+        for (int i = 0; i < 5; ++i)
+            ev[i] = static_cast<cudaEvent_t>(events[i]);
+    auto mark = [&](int i, cudaStream_t st) {
+        if (ev[i])
+            cudaEventRecord(ev[i], st);
+    };
     int st = check_attn_shape(num_reqs, num_tokens, num_q_heads, num_kv_heads, head_dim, max_kv_splits);
     if (st != CPSA_OK)
         return st;
@@ -211,9 +232,11 @@ int cpp_chunked_prefill_attn(const void *q, const void *k_cache, const void *v_c
     pp.max_ditems = L.max_ditems;
     pp.max_citems = L.max_citems;
     pp.dev_err = dev_err;
+    mark(0, s);
     launch_plan(pp, s);
     if (cudaGetLastError() != cudaSuccess)
         return CPSA_ERR_CUDA;
+    mark(1, s);
 
     const float sc = scale > 0.f ? scale : 1.0f / sqrtf((float)head_dim);
     AttnCommon ac{};
@@ -252,6 +275,7 @@ int cpp_chunked_prefill_attn(const void *q, const void *k_cache, const void *v_c
     int grid_c = (int)(L.max_pitems < sms ? L.max_pitems : sms);
     if (grid_c > 0 && launch_chunk_attn(cp, tq, tk, tv, head_dim, nq, grid_c, s) != cudaSuccess)
         return CPSA_ERR_CUDA;
+    mark(2, s);
 
     DecodeParams dp;
     static_cast<AttnCommon &>(dp) = ac;
@@ -260,13 +284,15 @@ int cpp_chunked_prefill_attn(const void *q, const void *k_cache, const void *v_c
     int grid_d = (int)(L.max_ditems < sms ? L.max_ditems : sms);
     if (grid_d > 0 && launch_decode_attn(dp, tkd, tvd, head_dim, grid_d, s) != cudaSuccess)
         return CPSA_ERR_CUDA;
+    mark(3, s);
 
     if (cap > 0) {
         CombineParams cb{counts, citems, part_o, part_ml, out, num_q_heads};
-        int grid_m = (int)(L.max_citems < 2 * sms ? L.max_citems : 2 * sms);
+        const int grid_m = 4 * sms;
         if (grid_m > 0 && launch_combine(cb, head_dim, grid_m, s) != cudaSuccess)
             return CPSA_ERR_CUDA;
     }
+    mark(4, s);
     return CPSA_OK;
 }
 

@@ -26,16 +26,18 @@ struct ReqCounts {
     int ditems;
     int citems;
     int prows;
+    int cunits;   // (row, q head) units to combine
 };
+constexpr int kScan = 6;
 
 __device__ __forceinline__ int ceil_div(int a, int b) { return (a + b - 1) / b; }
 
 // Per-request work: counts (emit == false) or the lists themselves (emit == true).
 __device__ void request_work(const PlanParams &p, int r, int max_splits, bool emit, int q_off,
-                             int pitem_off, int ditem_off, int citem_off, int prow_off,
+                             int pitem_off, int ditem_off, int citem_off, int prow_off, int cunit_off,
                              ReqCounts &c)
 {
-    c = ReqCounts{0, 0, 0, 0, 0};
+    c = ReqCounts{0, 0, 0, 0, 0, 0};
     int q = p.query_lens[r];
     int s = p.seq_lens[r];
     bool valid = true;
@@ -61,66 +63,67 @@ __device__ void request_work(const PlanParams &p, int r, int max_splits, bool em
         if (ns > 1) {
             c.prows = p.Hq * ns;
             c.citems = 1;
+            c.cunits = p.Hq;
         }
         if (emit) {
             int k = 0;
-            for (int kvh = 0; kvh < p.Hkv; ++kvh)
-                for (int sp = 0; sp < ns; ++sp) {
-                    int c0 = (int)((int64_t)sp * nch / ns), c1 = (int)((int64_t)(sp + 1) * nch / ns);
-                    int key1 = c1 * kDecodeChunk;
-                    if (key1 > s) key1 = s;
+            for (int sp = 0; sp < ns; ++sp) {
+                const int c0 = sp * nch / ns, c1 = (sp + 1) * nch / ns;
+                const int key1 = min(c1 * kDecodeChunk, s);
+                for (int kvh = 0; kvh < p.Hkv; ++kvh)
                     p.ditems[ditem_off + k++] = DecodeItem{r, kvh, c0 * kDecodeChunk, key1, sp, ns,
                                                            ns > 1 ? prow_off : -1, q_off};
-                }
+            }
             if (ns > 1)
-                p.citems[citem_off] = CombineItem{q_off, 1, prow_off, ns};
+                p.citems[citem_off] = CombineItem{q_off, 1, prow_off, ns, cunit_off, 0, 0, 0};
         }
         return;
     }
     // prefill: 128-row query tiles, longest KV range first
     int nqt = ceil_div(q, kTileM);
     int pairs = p.group / p.nq;
-    int pi = 0, ci = 0, pr = 0;
+    int pi = 0, ci = 0, pr = 0, cu = 0;
     for (int qt = nqt - 1; qt >= 0; --qt) {
-        int i0 = qt * kTileM;
-        int rows = q - i0 < kTileM ? q - i0 : kTileM;
-        int nkv = ceil_div(hist + i0 + rows, kTileN);
+        const int i0 = qt * kTileM;
+        const int rows = q - i0 < kTileM ? q - i0 : kTileM;
+        const int nkv = ceil_div(hist + i0 + rows, kTileN);
         int ns = ceil_div(nkv, kPrefillTilesPerSplit);
         if (ns > max_splits) ns = max_splits;
         if (ns < 1) ns = 1;
-        int pbase = ns > 1 ? prow_off + pr : -1;
+        const int pbase = ns > 1 ? prow_off + pr : -1;
         if (emit) {
-            for (int kvh = 0; kvh < p.Hkv; ++kvh)
-                for (int hp = 0; hp < pairs; ++hp)
-                    for (int sp = 0; sp < ns; ++sp) {
-                        int kt0 = (int)((int64_t)sp * nkv / ns), kt1 = (int)((int64_t)(sp + 1) * nkv / ns);
-                        p.pitems[pitem_off + pi] =
-                            PrefillItem{r, i0, kvh | (hp << 16), kt0, kt1, sp, ns, pbase};
-                        ++pi;
-                    }
+            // splits outermost: items of one split sit together and cover all heads
+            for (int sp = 0; sp < ns; ++sp) {
+                const int kt0 = sp * nkv / ns, kt1 = (sp + 1) * nkv / ns;
+                for (int kvh = 0; kvh < p.Hkv; ++kvh)
+                    for (int hp = 0; hp < pairs; ++hp)
+                        p.pitems[pitem_off + pi++] = PrefillItem{r, i0, kvh | (hp << 16), kt0, kt1, sp, ns, pbase};
+            }
             if (ns > 1)
-                p.citems[citem_off + ci] = CombineItem{q_off + i0, rows, pbase, ns};
+                p.citems[citem_off + ci] = CombineItem{q_off + i0, rows, pbase, ns, cunit_off + cu, 0, 0, 0};
         } else {
             pi += p.Hkv * pairs * ns;
         }
         if (ns > 1) {
             pr += rows * p.Hq * ns;
+            cu += rows * p.Hq;
             ++ci;
         }
     }
     c.pitems = pi;
     c.citems = ci;
     c.prows = pr;
+    c.cunits = cu;
 }
 
-// Block-wide exclusive scan of 5 ints (kPlanThreads threads); returns the totals.
-__device__ void block_scan5(int (&v)[5], int (&tot)[5])
+// Block-wide exclusive scan of kScan ints (kPlanThreads threads); returns the totals.
+__device__ void block_scan(int (&v)[kScan], int (&tot)[kScan])
 {
-    __shared__ int warp_sums[kPlanThreads / 32][5];
+    __shared__ int warp_sums[kPlanThreads / 32][kScan];
     int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-    int incl[5];
+    int incl[kScan];
 #pragma unroll
-    for (int j = 0; j < 5; ++j) {
+    for (int j = 0; j < kScan; ++j) {
         int x = v[j];
 #pragma unroll
         for (int o = 1; o < 32; o <<= 1) {
@@ -130,10 +133,10 @@ __device__ void block_scan5(int (&v)[5], int (&tot)[5])
         incl[j] = x;
     }
     if (lane == 31)
-        for (int j = 0; j < 5; ++j) warp_sums[warp][j] = incl[j];
+        for (int j = 0; j < kScan; ++j) warp_sums[warp][j] = incl[j];
     __syncthreads();
     if (warp == 0) {
-        for (int j = 0; j < 5; ++j) {
+        for (int j = 0; j < kScan; ++j) {
             int x = warp_sums[lane][j];
 #pragma unroll
             for (int o = 1; o < 32; o <<= 1) {
@@ -145,7 +148,7 @@ __device__ void block_scan5(int (&v)[5], int (&tot)[5])
     }
     __syncthreads();
 #pragma unroll
-    for (int j = 0; j < 5; ++j) {
+    for (int j = 0; j < kScan; ++j) {
         int before = warp > 0 ? warp_sums[warp - 1][j] : 0;
         tot[j] = warp_sums[kPlanThreads / 32 - 1][j];
         v[j] = before + incl[j] - v[j];
@@ -160,9 +163,9 @@ __global__ void __launch_bounds__(kPlanThreads, 1) plan_kernel(PlanParams p)
     int64_t tok = 0, prows = 0;
     for (int base = 0; base < p.num_reqs; base += kPlanThreads) {
         int r = base + threadIdx.x;
-        ReqCounts c{0, 0, 0, 0, 0};
+        ReqCounts c{0, 0, 0, 0, 0, 0};
         if (r < p.num_reqs)
-            request_work(p, r, p.max_splits, false, 0, 0, 0, 0, 0, c);
+            request_work(p, r, p.max_splits, false, 0, 0, 0, 0, 0, 0, c);
         tok += c.q;
         prows += c.prows;
     }
@@ -201,15 +204,15 @@ __global__ void __launch_bounds__(kPlanThreads, 1) plan_kernel(PlanParams p)
     }
     int max_splits = s_clamp ? 1 : p.max_splits;
     // pass 2: scans and lists
-    int carry[5] = {0, 0, 0, 0, 0};
+    int carry[kScan] = {0, 0, 0, 0, 0, 0};
     for (int base = 0; base < p.num_reqs; base += kPlanThreads) {
         int r = base + threadIdx.x;
-        ReqCounts c{0, 0, 0, 0, 0};
+        ReqCounts c{0, 0, 0, 0, 0, 0};
         if (r < p.num_reqs)
-            request_work(p, r, max_splits, false, 0, 0, 0, 0, 0, c);
-        int v[5] = {c.q, c.pitems, c.ditems, c.citems, c.prows};
-        int tot[5];
-        block_scan5(v, tot);
+            request_work(p, r, max_splits, false, 0, 0, 0, 0, 0, 0, c);
+        int v[kScan] = {c.q, c.pitems, c.ditems, c.citems, c.prows, c.cunits};
+        int tot[kScan];
+        block_scan(v, tot);
         if (r < p.num_reqs) {
             p.cu_q[r] = carry[0] + v[0];
             bool fits = carry[1] + v[1] + c.pitems <= p.max_pitems &&
@@ -217,9 +220,9 @@ __global__ void __launch_bounds__(kPlanThreads, 1) plan_kernel(PlanParams p)
                         carry[3] + v[3] + c.citems <= p.max_citems;
             if (fits)
                 request_work(p, r, max_splits, true, carry[0] + v[0], carry[1] + v[1],
-                             carry[2] + v[2], carry[3] + v[3], carry[4] + v[4], c);
+                             carry[2] + v[2], carry[3] + v[3], carry[4] + v[4], carry[5] + v[5], c);
         }
-        for (int j = 0; j < 5; ++j) carry[j] += tot[j];
+        for (int j = 0; j < kScan; ++j) carry[j] += tot[j];
     }
     if (threadIdx.x == 0) {
         p.cu_q[p.num_reqs] = carry[0];
@@ -227,7 +230,8 @@ __global__ void __launch_bounds__(kPlanThreads, 1) plan_kernel(PlanParams p)
         p.counts[kCntDecode] = carry[2] < p.max_ditems ? carry[2] : (int)p.max_ditems;
         p.counts[kCntCombine] = carry[3] < p.max_citems ? carry[3] : (int)p.max_citems;
         p.counts[kCntPartialRows] = carry[4];
-        for (int j = 4; j < kCntSlots; ++j) p.counts[j] = 0;
+        p.counts[kCntCombineUnits] = carry[5];
+        for (int j = 5; j < kCntSlots; ++j) p.counts[j] = 0;
     }
 }
 

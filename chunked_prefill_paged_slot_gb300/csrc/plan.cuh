@@ -34,8 +34,9 @@ struct DecodeItem {
 };
 
 // Rows [t0, t0 + nrows) had nsplit partials each, at pbase + (row*Hq + h)*nsplit + s.
+// u0: number of (row, q head) units of all earlier combine items.
 struct CombineItem {
-    int32_t t0, nrows, pbase, nsplit;
+    int32_t t0, nrows, pbase, nsplit, u0, pad0, pad1, pad2;
 };
 
 enum CountSlot {
@@ -43,6 +44,7 @@ enum CountSlot {
     kCntDecode = 1,
     kCntCombine = 2,
     kCntPartialRows = 3,
+    kCntCombineUnits = 4,
     kCntSlots = 16
 };
 

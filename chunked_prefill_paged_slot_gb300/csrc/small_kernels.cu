@@ -49,44 +49,70 @@ __global__ void __launch_bounds__(256) kv_write_kernel(const uint4 *__restrict__
 
 // ---------------------------------------------------------------------------
 // Combine of split rows: O = sum_s 2^(m_s - M) O_s / sum_s 2^(m_s - M) l_s,
-// M = max_s m_s (m in base-2 units). One warp per (row, q head).
+// M = max_s m_s (m in base-2 units). Persistent: the (row, q head) units of all
+// combine items are numbered consecutively (CombineItem::u0); warp w takes a
+// contiguous run of units, locating its first item by binary search.
 // ---------------------------------------------------------------------------
+constexpr int kCombineThreads = 256;
+
 template <int D>
-__global__ void __launch_bounds__(256) combine_kernel(const CombineParams p)
+__global__ void __launch_bounds__(kCombineThreads) combine_kernel(const CombineParams p)
 {
     const int n_items = p.counts[kCntCombine];
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int total = p.counts[kCntCombineUnits];
+    if (n_items == 0 || total == 0)
+        return;
+    const int lane = threadIdx.x & 31;
+    const int warps = gridDim.x * (kCombineThreads / 32);
+    const int gw = blockIdx.x * (kCombineThreads / 32) + (threadIdx.x >> 5);
+    const int per = (total + warps - 1) / warps;
+    const int u_begin = gw * per;
+    const int u_end = min(total, u_begin + per);
+    if (u_begin >= u_end)
+        return;
     constexpr int PER_LANE = D / 32;
-    for (int ci = blockIdx.x; ci < n_items; ci += gridDim.x) {
-        const CombineItem c = p.citems[ci];
-        const int units = c.nrows * p.num_q_heads;
-        for (int u = warp; u < units; u += blockDim.x / 32) {
-            const int row = u / p.num_q_heads, h = u % p.num_q_heads;
-            const int64_t pr0 = (int64_t)c.pbase + (int64_t)u * c.nsplit;
-            float2 ml = lane < c.nsplit ? reinterpret_cast<const float2 *>(p.part_ml)[pr0 + lane]
-                                        : make_float2(-INFINITY, 0.f);
-            float M = ml.x;
-            for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
-            const float Mref = M == -INFINITY ? 0.f : M;
-            const float f = ex2_approx(ml.x - Mref);
-            float L = f * ml.y;
-            for (int o = 16; o > 0; o >>= 1) L += __shfl_xor_sync(0xffffffffu, L, o);
-            float acc[PER_LANE];
+    const int Hq = p.num_q_heads;
+    // last item with u0 <= u_begin
+    int lo = 0, hi = n_items - 1;
+    while (lo < hi) {
+        const int mid = (lo + hi + 1) >> 1;
+        if (p.citems[mid].u0 <= u_begin) lo = mid; else hi = mid - 1;
+    }
+    int ci = lo;
+    CombineItem c = p.citems[ci];
+    for (int u = u_begin; u < u_end; ++u) {
+        while (u >= c.u0 + c.nrows * Hq) c = p.citems[++ci];
+        const int local = u - c.u0;
+        const int row = local / Hq, h = local % Hq;
+        const int64_t pr0 = (int64_t)c.pbase + (int64_t)local * c.nsplit;
+        const float2 ml = lane < c.nsplit ? reinterpret_cast<const float2 *>(p.part_ml)[pr0 + lane]
+                                          : make_float2(-INFINITY, 0.f);
+        float M = ml.x;
+        for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
+        const float Mref = M == -INFINITY ? 0.f : M;
+        const float f = ex2_approx(ml.x - Mref);
+        float L = f * ml.y;
+        for (int o = 16; o > 0; o >>= 1) L += __shfl_xor_sync(0xffffffffu, L, o);
+        float acc[PER_LANE];
 #pragma unroll
-            for (int e = 0; e < PER_LANE; ++e) acc[e] = 0.f;
-            for (int s = 0; s < c.nsplit; ++s) {
-                const float fs = __shfl_sync(0xffffffffu, f, s);
-                const float *src = p.part_o + (pr0 + s) * D + lane * PER_LANE;
+        for (int e = 0; e < PER_LANE; ++e) acc[e] = 0.f;
+        for (int s = 0; s < c.nsplit; ++s) {
+            const float fs = __shfl_sync(0xffffffffu, f, s);
+            const float *src = p.part_o + (pr0 + s) * D + lane * PER_LANE;
+            if (PER_LANE == 4) {
+                const float4 x = __ldcs(reinterpret_cast<const float4 *>(src));
+                acc[0] += fs * x.x; acc[1] += fs * x.y; acc[2] += fs * x.z; acc[3] += fs * x.w;
+            } else {
 #pragma unroll
                 for (int e = 0; e < PER_LANE; ++e) acc[e] += fs * src[e];
             }
-            const float inv = L > 0.f ? 1.f / L : 0.f;
-            __nv_bfloat16 *dst = reinterpret_cast<__nv_bfloat16 *>(p.out) +
-                                 ((int64_t)(c.t0 + row) * p.num_q_heads + h) * D + lane * PER_LANE;
-#pragma unroll
-            for (int e = 0; e < PER_LANE; e += 2)
-                *reinterpret_cast<uint32_t *>(dst + e) = pack_bf16x2(acc[e] * inv, acc[e + 1] * inv);
         }
+        const float inv = L > 0.f ? 1.f / L : 0.f;
+        __nv_bfloat16 *dst = reinterpret_cast<__nv_bfloat16 *>(p.out) +
+                             ((int64_t)(c.t0 + row) * Hq + h) * D + lane * PER_LANE;
+#pragma unroll
+        for (int e = 0; e < PER_LANE; e += 2)
+            *reinterpret_cast<uint32_t *>(dst + e) = pack_bf16x2(acc[e] * inv, acc[e + 1] * inv);
     }
 }
 
@@ -204,9 +230,9 @@ cudaError_t launch_kv_cache_write(const void *k, const void *v, const int64_t *s
 cudaError_t launch_combine(const CombineParams &p, int head_dim, int grid, cudaStream_t s)
 {
     if (head_dim == 128)
-        combine_kernel<128><<<grid, 256, 0, s>>>(p);
+        combine_kernel<128><<<grid, kCombineThreads, 0, s>>>(p);
     else
-        combine_kernel<64><<<grid, 256, 0, s>>>(p);
+        combine_kernel<64><<<grid, kCombineThreads, 0, s>>>(p);
     return cudaGetLastError();
 }
 

@@ -134,6 +134,22 @@ int cpp_chunked_prefill_attn(const void *q, const void *k_cache, const void *v_c
                              size_t workspace_bytes, uint32_t *dev_err, void *stream);
 
 /*
+ * cpp_chunked_prefill_attn with timing marks: when `events` is not NULL it
+ * points to 5 cudaEvent_t handles (any may be NULL) recorded on `stream`:
+ * [0] before the plan kernel, [1] before the chunk kernel, [2] after it,
+ * [3] after the decode kernel, [4] after the combine kernel. For profiling
+ * harnesses; the computation is identical.
+ */
+int cpp_chunked_prefill_attn_events(const void *q, const void *k_cache, const void *v_cache,
+                                    const int32_t *query_lens, const int32_t *seq_lens,
+                                    const int32_t *block_table, int num_reqs, int64_t num_tokens,
+                                    int max_blocks_per_req, int num_q_heads, int num_kv_heads,
+                                    int head_dim, int page_size, int64_t num_pages, float scale,
+                                    int max_kv_splits, void *out, void *workspace,
+                                    size_t workspace_bytes, uint32_t *dev_err, void *stream,
+                                    void *const *events);
+
+/*
  * Balanced micro-batch split point ([DS] section 3.1, "advanced method").
  *
  * total = sum(query_lens); best = total / 2 (integer); over request boundaries

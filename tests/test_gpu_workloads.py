@@ -1,0 +1,171 @@
+"""GPU parity at the full workload sizes, in the launch configuration bench.py
+times, on sampled rows that the fp64 oracle computes one by one.
+
+For every sampled request the oracle gets that request's own inputs: its
+history K/V (read from the cache pages BEFORE this step's KV write, i.e. the
+seeded input state) and its new tokens' q/k/v; it writes the new tokens with
+its own KV write into a compact cache and evaluates the sampled rows."""
+import numpy as np
+import pytest
+
+import oracle
+import workloads as W
+from helpers import compare
+
+pytestmark = pytest.mark.gpu
+
+
+def _u16(t):
+    import torch
+    return t.contiguous().view(torch.int16).cpu().numpy().view(np.uint16)
+
+
+def oracle_rows(q_req, k_new, v_new, hist_pages_k, hist_pages_v, hist, qlen, P, rows):
+    """Oracle attention of rows `rows` (0-based within the request) of one request.
+
+    hist_pages_*: uint16 [n_pages, Hkv, P, d] -- the request's pages in block
+    order, holding its history; new tokens go to positions hist .. hist+qlen-1."""
+    n_pages = hist_pages_k.shape[0]
+    kc = hist_pages_k.copy()
+    vc = hist_pages_v.copy()
+    pos = np.arange(hist, hist + qlen)
+    slots = (pos // P) * P + pos % P                      # identity page table 0..n-1
+    assert oracle.kv_cache_write(k_new, v_new, slots.astype(np.int64), P, kc, vc) == 0
+    bt = np.arange(n_pages, dtype=np.int32)[None, :]
+    return oracle.paged_attention(q_req, kc, vc, [qlen], [hist + qlen], bt, rows=np.asarray(rows))
+
+
+@pytest.mark.parametrize("history", [0, 512, 8192, 32256])
+def test_llama_chunk_sampled_rows(cuda_lib, history):
+    """One 512-token chunk of the 32768-token Llama-3-8B-shaped prefill (page 128)."""
+    import torch
+    SEQ, C, P = 32768, 512, 128
+    q, k, v, slots, bt = W.device_sequence(SEQ, P)
+    n_pages = bt.shape[1]
+    kc = torch.full((n_pages, 8, P, 128), float("nan"), dtype=torch.bfloat16, device="cuda")
+    vc = kc.clone()
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    # history written chunk by chunk, exactly as the step does
+    for a in range(0, history + C, C):
+        cuda_lib.cpp_kv_cache_write(k[a:a + C], v[a:a + C], slots[a:a + C], kc, vc, err)
+    out = torch.empty((C, 32, 128), dtype=torch.bfloat16, device="cuda")
+    ws = torch.empty(cuda_lib.cpp_attn_workspace_bytes(1, C, 32, 8, 128, 8), dtype=torch.uint8, device="cuda")
+    ql = torch.tensor([C], dtype=torch.int32, device="cuda")
+    sl = torch.tensor([history + C], dtype=torch.int32, device="cuda")
+    cuda_lib.cpp_chunked_prefill_attn(q[history:history + C], kc, vc, ql, sl, bt, out, ws, err, max_kv_splits=8)
+    torch.cuda.synchronize()
+    assert cuda_lib.cpp_read_device_error(err) == 0
+    rng = np.random.default_rng(history)
+    rows = np.unique(np.concatenate([[0, 1, 127, 128, 255, 256, 383, 384, 510, 511],
+                                     rng.choice(C, 22, replace=False)]))
+    # oracle: the sequence prefix in token order (its own KV write, identity pages)
+    s = history + C
+    npg = (s + P - 1) // P
+    kk = np.full((npg, 8, P, 128), W.BF16_NAN_SENTINEL, dtype=np.uint16)
+    vv = kk.copy()
+    if history:
+        pos = np.arange(0, history)
+        oracle.kv_cache_write(_u16(k[:history]), _u16(v[:history]), ((pos // P) * P + pos % P).astype(np.int64),
+                              P, kk, vv)
+    ref = oracle_rows(_u16(q[history:s]), _u16(k[history:s]), _u16(v[history:s]), kk, vv, history, C, P, rows)
+    got = out[torch.from_numpy(rows).cuda()].float().cpu().numpy().astype(np.float64)
+    compare(got, ref, what=f"llama chunk h={history}")
+
+
+def _sampled_parity(cuda_lib, spec, sample_reqs, rows_per_req, seed):
+    import torch
+    d = W.device_batch(spec)
+    B, T = len(spec.qlen), sum(spec.qlen)
+    P = spec.page_size
+    bt = d["block_table_host"]
+    # input state of the sampled requests' pages, before this step's KV write
+    saved = {}
+    for r in sample_reqs:
+        npg = (spec.seq[r] + P - 1) // P
+        idx = torch.from_numpy(bt[r, :npg].astype(np.int64)).cuda()
+        saved[r] = (_u16(d["k_cache"][idx]), _u16(d["v_cache"][idx]))
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    out = torch.empty_like(d["q"])
+    ws = torch.empty(cuda_lib.cpp_attn_workspace_bytes(B, T, spec.num_q_heads, spec.num_kv_heads, spec.head_dim, 8),
+                     dtype=torch.uint8, device="cuda")
+    cuda_lib.cpp_kv_cache_write(d["k"], d["v"], d["slot_mapping"], d["k_cache"], d["v_cache"], err)
+    cuda_lib.cpp_chunked_prefill_attn(d["q"], d["k_cache"], d["v_cache"], d["query_lens"], d["seq_lens"],
+                                      d["block_table"], out, ws, err, max_kv_splits=8)
+    torch.cuda.synchronize()
+    assert cuda_lib.cpp_read_device_error(err) == 0
+    cu = np.concatenate([[0], np.cumsum(spec.qlen)])
+    rng = np.random.default_rng(seed)
+    gots, refs = [], []
+    for r in sample_reqs:
+        ql, h = spec.qlen[r], spec.hist[r]
+        rows = np.arange(ql) if ql <= rows_per_req else np.unique(
+            np.concatenate([[0, ql - 1], rng.choice(ql, rows_per_req, replace=False)]))
+        t0, t1 = int(cu[r]), int(cu[r + 1])
+        hk, hv = saved[r]
+        ref = oracle_rows(_u16(d["q"][t0:t1]), _u16(d["k"][t0:t1]), _u16(d["v"][t0:t1]), hk, hv, h, ql, P, rows)
+        got = out[t0 + torch.from_numpy(rows).cuda()].float().cpu().numpy().astype(np.float64)
+        gots.append(got)
+        refs.append(ref)
+    return np.concatenate(gots), np.concatenate(refs), d, out
+
+
+def test_sarathi_mixed_sampled(cuda_lib):
+    """1536 decode rows (context U[1024, 8192]) + one 512-token chunk at h = 8192, page 16."""
+    spec = W.spec_sarathi_mixed()
+    rng = np.random.default_rng(33)
+    reqs = sorted(set(rng.choice(1536, 24, replace=False).tolist()) | {0, 1535, 1536})
+    got, ref, _, _ = _sampled_parity(cuda_lib, spec, reqs, rows_per_req=24, seed=34)
+    compare(got, ref, what="sarathi mixed")
+
+
+def test_microbatch_sampled(cuda_lib):
+    """128 decode rows (context U[2600, 5200]) + 64 prompts of 2600 tokens, page 16."""
+    spec = W.spec_microbatch()
+    reqs = [0, 5, 77, 127, 128, 150, 191]
+    got, ref, _, _ = _sampled_parity(cuda_lib, spec, reqs, rows_per_req=16, seed=35)
+    compare(got, ref, what="microbatch")
+
+
+def test_two_streams_bit_identical_to_one(cuda_lib):
+    """The micro-batch split run on two streams gives the same bits as one stream."""
+    import torch
+    spec = W.spec_microbatch()
+    d = W.device_batch(spec)
+    B, T = len(spec.qlen), sum(spec.qlen)
+    step = cuda_lib.AttentionStep(B, T, 32, 8, 128, max_kv_splits=8, two_stream=True)
+    # the first KV write happens in both runs; history pages are read-only afterwards
+    out1 = torch.empty_like(d["q"])
+    step.run(d["q"], d["k"], d["v"], d["slot_mapping"], d["k_cache"], d["v_cache"], d["query_lens"],
+             d["seq_lens"], d["block_table"], out1)
+    out2 = torch.empty_like(d["q"])
+    used = step.run_two_stream(d["q"], d["k"], d["v"], d["slot_mapping"], d["k_cache"], d["v_cache"],
+                               d["query_lens"], d["seq_lens"], d["block_table"], out2)
+    torch.cuda.synchronize()
+    assert used and step.last_split == (160, 83328, True)
+    assert step.read_errors() == 0
+    assert torch.equal(out1.view(torch.int16), out2.view(torch.int16))
+
+
+def test_gpu_chunk_invariance(cuda_lib):
+    """A 2048-token prompt prefilled as one chunk or as four chunks of 512 agrees."""
+    import torch
+    q, k, v, slots, bt = W.device_sequence(2048, 16, seed=9)
+    n_pages = bt.shape[1]
+    outs = []
+    for chunk in (2048, 512):
+        kc = torch.full((n_pages, 8, 16, 128), float("nan"), dtype=torch.bfloat16, device="cuda")
+        vc = kc.clone()
+        err = torch.zeros(1, dtype=torch.int32, device="cuda")
+        out = torch.empty_like(q)
+        ws = torch.empty(cuda_lib.cpp_attn_workspace_bytes(1, chunk, 32, 8, 128, 8), dtype=torch.uint8,
+                         device="cuda")
+        for a in range(0, 2048, chunk):
+            cuda_lib.cpp_kv_cache_write(k[a:a + chunk], v[a:a + chunk], slots[a:a + chunk], kc, vc, err)
+            cuda_lib.cpp_chunked_prefill_attn(q[a:a + chunk], kc, vc, torch.tensor([chunk], dtype=torch.int32,
+                                                                                    device="cuda"),
+                                              torch.tensor([a + chunk], dtype=torch.int32, device="cuda"), bt,
+                                              out[a:a + chunk], ws, err)
+        torch.cuda.synchronize()
+        assert cuda_lib.cpp_read_device_error(err) == 0
+        outs.append(out.float().cpu().numpy().astype(np.float64))
+    compare(outs[1], outs[0], atol=1e-2, rtol_f=3e-3, what="chunked vs whole")

@@ -243,3 +243,23 @@ def device_cache_fill(cache, gen, rows_per_fill: int = 1 << 14):
         slab = torch.randn(cache[p0:p1].shape, generator=gen, device=cache.device, dtype=torch.float32)
         cache[p0:p1].copy_(slab)
         del slab
+
+
+def device_sequence(total_len: int = 32768, page_size: int = 128, num_q_heads: int = 32, num_kv_heads: int = 8,
+                    head_dim: int = 128, seed: int = 2, device="cuda"):
+    """One long prompt for chunked prefill: q/k/v of every position ~ N(0,1) bf16
+    (seeded torch RNG on the device) and the slots of positions 0..total_len-1
+    through a permuted pool of total_len / page_size pages.
+    Returns (q, k, v, slot_mapping, block_table[1, pages]) device tensors."""
+    import torch
+    rng = np.random.Generator(np.random.PCG64(seed))
+    n_pages = (total_len + page_size - 1) // page_size
+    bt = rng.permutation(n_pages).astype(np.int32)[None, :]
+    slots = _slots_for(bt[0], np.arange(total_len), page_size)
+    g = torch.Generator(device=device)
+    g.manual_seed(seed)
+    bf = torch.bfloat16
+    q = torch.randn((total_len, num_q_heads, head_dim), generator=g, device=device, dtype=torch.float32).to(bf)
+    k = torch.randn((total_len, num_kv_heads, head_dim), generator=g, device=device, dtype=torch.float32).to(bf)
+    v = torch.randn((total_len, num_kv_heads, head_dim), generator=g, device=device, dtype=torch.float32).to(bf)
+    return q, k, v, torch.from_numpy(slots).to(device), torch.from_numpy(bt).to(device)
