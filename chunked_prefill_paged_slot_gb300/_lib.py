@@ -58,6 +58,10 @@ def load():
                                              _c_p, _c_p]
     lib.cpp_chunked_prefill_attn_events.restype = _c_int
     lib.cpp_chunked_prefill_attn_events.argtypes = lib.cpp_chunked_prefill_attn.argtypes + [_c_p]
+    lib.cpp_chunked_prefill_attn_noalloc.restype = _c_int
+    lib.cpp_chunked_prefill_attn_noalloc.argtypes = [_c_p, _c_p, _c_p, _c_p, _c_p, _c_p, _c_int, _c_i64, _c_int,
+                                                     _c_int, _c_int, _c_int, _c_int, _c_i64, _c_f, _c_int, _c_p,
+                                                     _c_p, _c_p]
     lib.cpp_split_microbatch.restype = _c_int
     lib.cpp_split_microbatch.argtypes = [_c_p, _c_int, _c_f, ctypes.c_int32, _c_p, _c_p]
     lib.cpp_read_device_error.restype = _c_int
@@ -165,6 +169,26 @@ def cpp_chunked_prefill_attn_events(q, k_cache, v_cache, query_lens, seq_lens, b
         _dev(out, torch.bfloat16, "out"), _dev(workspace, torch.uint8, "workspace"), workspace.numel(),
         _dev(dev_err, torch.int32, "dev_err"), _stream_ptr(stream), evs)
     _check(st, "cpp_chunked_prefill_attn_events")
+
+
+def cpp_chunked_prefill_attn_noalloc(q, k_cache, v_cache, query_lens, seq_lens, block_table, out, dev_err,
+                                     scale=0.0, max_kv_splits=8, stream=None):
+    """cpp_chunked_prefill_attn without a workspace: for callers that cannot
+    allocate device memory, the library's own fixed scratch area is used (see
+    include/cpsa.h: calls that overlap on the GPU must not share it)."""
+    T, Hq, d = q.shape
+    pages, Hkv, P, d2 = k_cache.shape
+    B = query_lens.shape[0]
+    if out.shape != q.shape or v_cache.shape != k_cache.shape or d2 != d or seq_lens.shape != (B,) \
+            or block_table.dim() != 2 or block_table.shape[0] != B:
+        raise CpsaError("cpp_chunked_prefill_attn_noalloc: inconsistent shapes")
+    st = load().cpp_chunked_prefill_attn_noalloc(
+        _dev(q, torch.bfloat16, "q"), _dev(k_cache, torch.bfloat16, "k_cache"),
+        _dev(v_cache, torch.bfloat16, "v_cache"), _dev(query_lens, torch.int32, "query_lens"),
+        _dev(seq_lens, torch.int32, "seq_lens"), _dev(block_table, torch.int32, "block_table"),
+        B, T, block_table.shape[1], Hq, Hkv, d, P, pages, float(scale), int(max_kv_splits),
+        _dev(out, torch.bfloat16, "out"), _dev(dev_err, torch.int32, "dev_err"), _stream_ptr(stream))
+    _check(st, "cpp_chunked_prefill_attn_noalloc")
 
 
 def cpp_split_microbatch(query_lens, out3, balance_threshold=0.1, length_threshold=256, stream=None):

@@ -98,6 +98,7 @@ const char *cpp_status_string(int status)
     case CPSA_ERR_WORKSPACE_TOO_SMALL: return "workspace too small";
     case CPSA_ERR_CUDA: return "CUDA error";
     case CPSA_ERR_NO_DEVICE: return "no usable device";
+    case CPSA_ERR_SCRATCH_TOO_SMALL: return "batch needs more than the library's built-in scratch area";
     default: return "unknown status";
     }
 }

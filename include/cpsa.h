@@ -61,6 +61,7 @@ extern "C" {
 #define CPSA_ERR_WORKSPACE_TOO_SMALL (-5) /* workspace below cpp_attn_workspace_min_bytes */
 #define CPSA_ERR_CUDA (-6)                /* a CUDA runtime call or launch failed */
 #define CPSA_ERR_NO_DEVICE (-7)           /* no usable sm_103 device is current */
+#define CPSA_ERR_SCRATCH_TOO_SMALL (-8)   /* batch needs more than the built-in scratch area */
 
 /* ---- device error flags (bits of *dev_err) --------------------------------- */
 #define CPSA_DEV_SLOT_OUT_OF_RANGE 0x01u  /* slot >= num_pages * page_size: token skipped */
@@ -148,6 +149,37 @@ int cpp_chunked_prefill_attn_events(const void *q, const void *k_cache, const vo
                                     int max_kv_splits, void *out, void *workspace,
                                     size_t workspace_bytes, uint32_t *dev_err, void *stream,
                                     void *const *events);
+
+/*
+ * cpp_chunked_prefill_attn for callers that cannot allocate device memory.
+ * (The pages have no counterpart of this call; it exists for library users.)
+ *
+ * Who needs it: code that runs inside a host application that owns all device
+ * memory and forbids allocation on its serving path, or C callers with no
+ * allocator of their own. Instead of a caller workspace it uses a scratch area
+ * the library owns: a fixed array of CPSA_NOALLOC_SCRATCH_BYTES in device
+ * global memory, reserved on every GPU that loads the library and kept until
+ * the process exits. The call itself allocates nothing.
+ *
+ * Same arguments, results and device flags as cpp_chunked_prefill_attn, minus
+ * the workspace. Returns CPSA_ERR_SCRATCH_TOO_SMALL when the batch's work lists
+ * (cpp_attn_workspace_min_bytes) exceed the scratch area; when only the split
+ * partials do not fit, every row runs with one KV split and
+ * CPSA_DEV_SPLITS_CLAMPED is set, as with a small workspace.
+ * The first call on a device looks up the scratch area's device address (with
+ * that device current) and caches it: make that first call before any stream
+ * capture. All calls in the process share the one area and find it holding the
+ * previous call's data (the call rewrites everything it reads), so calls whose
+ * execution overlaps on the GPU -- on different streams, or from different host
+ * threads -- race and must be ordered by the caller.
+ */
+#define CPSA_NOALLOC_SCRATCH_BYTES ((size_t)64 << 20)
+int cpp_chunked_prefill_attn_noalloc(const void *q, const void *k_cache, const void *v_cache,
+                                     const int32_t *query_lens, const int32_t *seq_lens,
+                                     const int32_t *block_table, int num_reqs, int64_t num_tokens,
+                                     int max_blocks_per_req, int num_q_heads, int num_kv_heads,
+                                     int head_dim, int page_size, int64_t num_pages, float scale,
+                                     int max_kv_splits, void *out, uint32_t *dev_err, void *stream);
 
 /*
  * Balanced micro-batch split point ([DS] section 3.1, "advanced method").
