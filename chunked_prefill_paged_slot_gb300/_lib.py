@@ -73,6 +73,8 @@ def load():
     lib.cpp_fit_latency_quadratic.argtypes = [_c_p, _c_p, _c_int, _c_p]
     lib.cpp_fit_latency_two_var.restype = _c_int
     lib.cpp_fit_latency_two_var.argtypes = [_c_p, _c_p, _c_p, _c_p, _c_int, _c_p]
+    lib.cpp_selftest_exp2.restype = _c_int
+    lib.cpp_selftest_exp2.argtypes = [_c_p, _c_p, _c_p, _c_i64, _c_p]
     lib.cpp_status_string.restype = ctypes.c_char_p
     lib.cpp_status_string.argtypes = [_c_int]
     _lib = lib
@@ -236,3 +238,13 @@ def cpp_fit_latency_two_var(x0, x1, x2, times):
     _check(load().cpp_fit_latency_two_var(_dbl(x0), _dbl(x1), _dbl(x2), _dbl(times), len(times), coef),
            "cpp_fit_latency_two_var")
     return [coef[0], coef[1], coef[2]]
+
+
+def cpp_selftest_exp2(x, stream=None):
+    """(poly, hw) = the attention kernels' FMA-pipe and hardware exp2 of the float32 CUDA tensor x."""
+    poly = torch.empty_like(x)
+    hw = torch.empty_like(x)
+    _check(load().cpp_selftest_exp2(_dev(x, torch.float32, "x"), _dev(poly, torch.float32, "poly"),
+                                    _dev(hw, torch.float32, "hw"), x.numel(), _stream_ptr(stream)),
+           "cpp_selftest_exp2")
+    return poly, hw

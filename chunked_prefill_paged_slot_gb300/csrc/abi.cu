@@ -204,6 +204,7 @@ int cpp_chunked_prefill_attn_events(const void *q, const void *k_cache, const vo
     uint8_t *ws = static_cast<uint8_t *>(workspace);
     int32_t *counts = reinterpret_cast<int32_t *>(ws + L.off_counts);
     int32_t *cu_q = reinterpret_cast<int32_t *>(ws + L.off_cuq);
+    int32_t *run_first = reinterpret_cast<int32_t *>(ws + L.off_runs);
     PrefillItem *pitems = reinterpret_cast<PrefillItem *>(ws + L.off_pitems);
     DecodeItem *ditems = reinterpret_cast<DecodeItem *>(ws + L.off_ditems);
     CombineItem *citems = reinterpret_cast<CombineItem *>(ws + L.off_citems);
@@ -223,9 +224,11 @@ int cpp_chunked_prefill_attn_events(const void *q, const void *k_cache, const vo
     pp.group = group;
     pp.nq = nq;
     pp.max_splits = max_kv_splits;
+    pp.chunk_grid = sms < kMaxChunkGrid ? sms : kMaxChunkGrid;
     pp.prow_capacity = cap;
     pp.counts = counts;
     pp.cu_q = cu_q;
+    pp.run_first = run_first;
     pp.pitems = pitems;
     pp.ditems = ditems;
     pp.citems = citems;
@@ -273,7 +276,8 @@ int cpp_chunked_prefill_attn_events(const void *q, const void *k_cache, const vo
     ChunkParams cp;
     static_cast<AttnCommon &>(cp) = ac;
     cp.pitems = pitems;
-    int grid_c = (int)(L.max_pitems < sms ? L.max_pitems : sms);
+    cp.run_first = run_first;
+    const int grid_c = pp.chunk_grid;   // one stream-K run per CTA
     if (grid_c > 0 && launch_chunk_attn(cp, tq, tk, tv, head_dim, nq, grid_c, s) != cudaSuccess)
         return CPSA_ERR_CUDA;
     mark(2, s);
@@ -307,6 +311,16 @@ int cpp_split_microbatch(const int32_t *query_lens, int num_reqs, float balance_
     cudaError_t e = launch_split_microbatch(query_lens, num_reqs, balance_threshold, length_threshold, out3,
                                             (cudaStream_t)stream);
     return e == cudaSuccess ? CPSA_OK : CPSA_ERR_CUDA;
+}
+
+int cpp_selftest_exp2(const float *x, float *out_poly, float *out_hw, int64_t n, void *stream)
+{
+    if (n < 0)
+        return CPSA_ERR_BAD_SHAPE;
+    if (n > 0 && (!x || !out_poly || !out_hw))
+        return CPSA_ERR_NULL_ARG;
+    return launch_exp2_selftest(x, out_poly, out_hw, n, (cudaStream_t)stream) == cudaSuccess ? CPSA_OK
+                                                                                             : CPSA_ERR_CUDA;
 }
 
 int cpp_read_device_error(uint32_t *dev_err, uint32_t *host_flags, int clear, void *stream)

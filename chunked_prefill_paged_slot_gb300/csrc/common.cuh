@@ -261,6 +261,69 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi)
     return r;
 }
 
+// ---------------------------------------------------------------------------
+// packed fp32 pairs (f32x2): one instruction for two lanes of arithmetic
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ uint64_t f2_pack(float lo, float hi)
+{
+    uint64_t r;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
+    return r;
+}
+
+__device__ __forceinline__ void f2_unpack(uint64_t v, float &lo, float &hi)
+{
+    asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(v));
+}
+
+__device__ __forceinline__ uint64_t f2_fma(uint64_t a, uint64_t b, uint64_t c)
+{
+    uint64_t d;
+    asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+    return d;
+}
+
+__device__ __forceinline__ uint64_t f2_add(uint64_t a, uint64_t b)
+{
+    uint64_t d;
+    asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+    return d;
+}
+
+__device__ __forceinline__ float fmax3(float a, float b, float c)
+{
+    float d;
+    asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+    return d;
+}
+
+// 2^x for two lanes on the FMA pipe (the MUFU unit does one lane per quarter
+// cycle per SM sub-partition, which is as slow as the tensor core on this path).
+// Method: Cody-Waite style range reduction x = j + f with j = round(x),
+// f in [-1/2, 1/2] (the 1.5*2^23 shift leaves round(x) in the low mantissa bits),
+// then a degree-3 minimax polynomial for 2^f (relative error 7.5e-5, fitted by a
+// Remez exchange, see exp2_poly_fit.py) and j added to the exponent field.
+// Valid for x in [-125, 127]: callers clamp.
+__device__ __forceinline__ uint64_t exp2_poly_x2(uint64_t x)
+{
+    const uint64_t shift = f2_pack(12582912.0f, 12582912.0f);
+    const uint64_t neg_one = f2_pack(-1.0f, -1.0f);
+    const uint64_t t = f2_add(x, shift);                       // 1.5*2^23 + round(x)
+    const uint64_t j = f2_fma(shift, neg_one, t);             // round(x) as a float
+    const uint64_t f = f2_fma(j, neg_one, x);                 // x - round(x)
+    uint64_t p = f2_fma(f2_pack(0.0551716685295105f, 0.0551716685295105f), f,
+                        f2_pack(0.2426111251115799f, 0.2426111251115799f));
+    p = f2_fma(p, f, f2_pack(0.6932609677314758f, 0.6932609677314758f));
+    p = f2_fma(p, f, f2_pack(0.9999280571937561f, 0.9999280571937561f));
+    float tl, th, pl, ph;
+    f2_unpack(t, tl, th);
+    f2_unpack(p, pl, ph);
+    // low bits of t are round(x); the shift constant's own bits vanish in << 23
+    const uint32_t rl = __float_as_uint(pl) + (__float_as_uint(tl) << 23);
+    const uint32_t rh = __float_as_uint(ph) + (__float_as_uint(th) << 23);
+    return f2_pack(__uint_as_float(rl), __uint_as_float(rh));
+}
+
 __device__ __forceinline__ void named_bar_sync(int id, int nthreads)
 {
     asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");

@@ -29,6 +29,7 @@ struct AttnCommon {
 
 struct ChunkParams : AttnCommon {
     const PrefillItem *pitems;
+    const int32_t *run_first;   // CTA c processes pieces [run_first[c], run_first[c + 1])
 };
 
 struct DecodeParams : AttnCommon {
@@ -57,6 +58,8 @@ cudaError_t launch_kv_cache_write(const void *k, const void *v, const int64_t *s
                                   uint32_t *dev_err, int num_sms, cudaStream_t s);
 cudaError_t launch_split_microbatch(const int32_t *query_lens, int num_reqs, float balance_threshold,
                                     int32_t length_threshold, int32_t *out3, cudaStream_t s);
+
+cudaError_t launch_exp2_selftest(const float *x, float *poly, float *hw, int64_t n, cudaStream_t s);
 
 // Rows of K/V per TMA box for the decode kernel (keys per pipeline stage cap).
 constexpr int kDecodeBoxRowsMax = 64;

@@ -15,16 +15,25 @@
 
 namespace cpsa {
 
-// Split policy: constants only, so a row's split count depends on its own
-// (query_len, seq_len) and the caller's max_kv_splits.
-constexpr int kPrefillTilesPerSplit = 32;   // KV tiles of 128 keys per prefill split
+// Split policy.
+// Prefill: stream-K. The KV tiles of all prefill units (one unit = a 128-row
+// query tile x kv head x head pair) are laid end to end and cut into equal runs
+// of max(ceil(W / grid), kMinRunTiles) tiles, one run per CTA of the chunk
+// kernel; a unit cut by a run boundary becomes several pieces whose partial
+// results the combine kernel merges. Every CTA gets the same amount of work.
+// Decode: a row splits into pieces of kDecodeKeysPerSplit keys (at most
+// max_kv_splits), depending only on its own length.
+constexpr int kMinRunTiles = 4;             // shortest run of KV tiles per CTA
+constexpr int kMaxChunkGrid = 256;          // upper bound of the chunk kernel's grid (SMs)
 constexpr int kDecodeChunk = 64;            // keys per decode pipeline stage
 constexpr int kDecodeKeysPerSplit = 4096;   // keys per decode split (multiple of kDecodeChunk)
 
-// A prefill item: one 128-row query tile of request r, NQ q heads of kv head
-// `kvh` (q heads kvh*G + hp*NQ ...), KV tiles [kt0, kt1) of split `split`.
+// A prefill piece: KV tiles [kt0, kt1) of the unit (request r, query tile at
+// row i0, kv head kvh, head pair hp), processed by CTA `owner`; piece `piece` of
+// `npieces` of that unit (partials at pbase when npieces > 1, merged by the
+// combine kernel).
 struct PrefillItem {
-    int32_t r, i0, kvh_hp, kt0, kt1, split, nsplit, pbase;
+    int32_t r, i0, kvh_hp, kt0, kt1, piece_np, pbase, owner;
 };
 
 // A decode item: the single new token (global row t) of request r, all q heads
@@ -33,10 +42,11 @@ struct DecodeItem {
     int32_t r, kvh, key0, key1, split, nsplit, pbase, t;
 };
 
-// Rows [t0, t0 + nrows) had nsplit partials each, at pbase + (row*Hq + h)*nsplit + s.
-// u0: number of (row, q head) units of all earlier combine items.
+// Rows [t0, t0 + nrows) x q heads [h0, h0 + nh) had nsplit partials each:
+// unit u = row * nh + (head - h0) at pbase + u * nsplit + s.
+// u0: number of (row, head) units of all earlier combine items.
 struct CombineItem {
-    int32_t t0, nrows, pbase, nsplit, u0, pad0, pad1, pad2;
+    int32_t t0, nrows, h0, nh, pbase, nsplit, u0, pad;
 };
 
 enum CountSlot {
@@ -45,11 +55,12 @@ enum CountSlot {
     kCntCombine = 2,
     kCntPartialRows = 3,
     kCntCombineUnits = 4,
+    kCntRunTiles = 5,
     kCntSlots = 16
 };
 
 struct WsLayout {
-    size_t off_counts, off_cuq, off_pitems, off_ditems, off_citems, off_pml, off_po, end_meta, end_full;
+    size_t off_counts, off_cuq, off_runs, off_pitems, off_ditems, off_citems, off_pml, off_po, end_meta, end_full;
     int64_t max_pitems, max_ditems, max_citems, max_prows_full;
 };
 
@@ -65,14 +76,18 @@ inline WsLayout ws_layout(int num_reqs, int64_t num_tokens, int Hq, int Hkv, int
     int64_t nprefill = B < T / 2 ? B : T / 2;
     int64_t ndecode = B < T ? B : T;
     int64_t qtiles = T / 128 + nprefill + 1;
-    int64_t pairs = (Hq / Hkv) / nq_per_cta;
-    L.max_pitems = qtiles * Hkv * pairs * max_splits;
+    int64_t units = qtiles * Hkv * ((Hq / Hkv) / nq_per_cta);
+    L.max_pitems = units + kMaxChunkGrid;
     L.max_ditems = ndecode * Hkv * max_splits;
-    L.max_citems = qtiles + ndecode;
-    L.max_prows_full = max_splits > 1 ? T * Hq * max_splits : 0;
+    L.max_citems = ndecode + 2 * kMaxChunkGrid;   // split decode rows + split prefill units
+    // prefill: a cut inside a unit adds one piece, at most 2 pieces' partials per cut
+    const int64_t prefill_rows = max_splits > 1 ? (int64_t)2 * kMaxChunkGrid * 128 * nq_per_cta : 0;
+    const int64_t decode_rows = max_splits > 1 ? ndecode * Hq * max_splits : 0;
+    L.max_prows_full = prefill_rows + decode_rows;
     size_t o = 0;
     L.off_counts = o; o = ws_align(o + sizeof(int32_t) * kCntSlots);
     L.off_cuq = o;    o = ws_align(o + sizeof(int32_t) * (size_t)(B + 1));
+    L.off_runs = o;   o = ws_align(o + sizeof(int32_t) * (size_t)(kMaxChunkGrid + 1));
     L.off_pitems = o; o = ws_align(o + sizeof(PrefillItem) * (size_t)L.max_pitems);
     L.off_ditems = o; o = ws_align(o + sizeof(DecodeItem) * (size_t)L.max_ditems);
     L.off_citems = o; o = ws_align(o + sizeof(CombineItem) * (size_t)L.max_citems);
@@ -102,9 +117,11 @@ struct PlanParams {
     int page_size;
     int Hq, Hkv, group, nq;    // nq: q heads per chunk-kernel CTA (1 or 2)
     int max_splits;
+    int chunk_grid;            // CTAs of the chunk kernel (stream-K runs)
     int64_t prow_capacity;     // partial rows that fit
     int32_t *counts;
     int32_t *cu_q;
+    int32_t *run_first;        // [chunk_grid + 1]: first piece of each CTA's run
     PrefillItem *pitems;
     DecodeItem *ditems;
     CombineItem *citems;

@@ -19,6 +19,9 @@
 //                S row from TMEM, causal mask on the diagonal/tail tiles, online
 //                max/sum in fp32 (base-2 exponent, scale folded in), P as bf16
 //                back into TMEM over S; final O / l epilogue.
+// Exponentials: in tiles without masked columns kFmaExpPairsPer8 of every 8
+// pairs go to the FMA pipe (exp2_poly_x2), the rest to MUFU ex2, so neither unit
+// sets the pace alone; the row sum and the exponent arguments use packed f32x2 arithmetic.
 // Rescaling of O is lazy: the running maximum is only raised when a tile's
 // maximum exceeds it by more than 8 (a factor 256 in the exponent), which keeps
 // p <= 256 and leaves the final O / l unchanged.
@@ -30,6 +33,12 @@
 namespace cpsa {
 
 namespace {
+
+// Of every 8 exponent pairs of an unmasked S row, this many go to the FMA pipe.
+#ifndef CPSA_FMA_EXP_PAIRS_PER_8
+#define CPSA_FMA_EXP_PAIRS_PER_8 0   // measured fastest on GB300: MUFU keeps up on this kernel
+#endif
+constexpr int kFmaExpPairsPer8 = CPSA_FMA_EXP_PAIRS_PER_8;
 
 template <int D, int NQ>
 struct ChunkCfg {
@@ -55,6 +64,7 @@ struct ChunkBars {
     uint64_t slot_full[8], slot_empty[8];
     uint32_t tmem_base;
     int abort;
+    int it_begin, it_end;    // this CTA's run of pieces
 };
 
 template <int D, int NQ>
@@ -67,8 +77,6 @@ chunk_attn_kernel(const ChunkParams p, const __grid_constant__ CUtensorMap tm_q,
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
     ChunkBars *bars = reinterpret_cast<ChunkBars *>(smem + C::kBarOff);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int n_items = p.counts[kCntPrefill];
-
     if (threadIdx.x == 0) {
         mbar_init(&bars->q_full, 1);
         mbar_init(&bars->q_empty, 1);
@@ -84,6 +92,9 @@ chunk_attn_kernel(const ChunkParams p, const __grid_constant__ CUtensorMap tm_q,
             mbar_init(&bars->slot_empty[s], 1);
         }
         bars->abort = 0;
+        // this CTA's run of pieces, from the plan's table
+        bars->it_begin = p.run_first[blockIdx.x];
+        bars->it_end = p.run_first[blockIdx.x + 1];
         fence_barrier_init();
     }
     if (warp == C::kLoadWarp && lane == 0) {
@@ -100,6 +111,7 @@ chunk_attn_kernel(const ChunkParams p, const __grid_constant__ CUtensorMap tm_q,
     tc_fence_after_sync();
     const uint32_t tmem = bars->tmem_base;
     volatile int *abort = &bars->abort;
+    const int it_begin = bars->it_begin, it_end = bars->it_end;
 
     if (warp == C::kLoadWarp) {
         // ------------------------------------------------------------ producer
@@ -107,7 +119,7 @@ chunk_attn_kernel(const ChunkParams p, const __grid_constant__ CUtensorMap tm_q,
         const int NB = 128 / PB;                                 // boxes per tile
         const uint32_t box_bytes = (uint32_t)PB * 128u;
         uint32_t q_uses = 0, slot_it = 0, tail_uses = 0;
-        for (int it = blockIdx.x; it < n_items && !*abort; it += gridDim.x) {
+        for (int it = it_begin; it < it_end && !*abort; ++it) {
             const PrefillItem w = p.pitems[it];
             const int kvh = w.kvh_hp & 0xFFFF, hp = w.kvh_hp >> 16;
             const int h0 = kvh * p.group + hp * NQ;
@@ -124,21 +136,27 @@ chunk_attn_kernel(const ChunkParams p, const __grid_constant__ CUtensorMap tm_q,
             }
             ++q_uses;
             const int32_t *bt_row = p.block_table + (int64_t)w.r * p.max_blocks;
+            // lane j < NB holds the page of box j of a tile; the lookup for tile
+            // kt + 1 is issued while tile kt's copies are set up (one tile ahead)
+            auto lookup = [&](int kt) -> int {
+                int pg = -1;
+                const int key = kt * 128 + lane * PB;
+                if (lane < NB && kt < w.kt1 && key < s_len)
+                    pg = __ldg(bt_row + key / p.page_size);
+                return pg;
+            };
+            int next_page = lookup(w.kt0);
             bool stop = false;
             for (int kt = w.kt0; kt < w.kt1 && !stop; ++kt) {
                 const int key0 = kt * 128;
-                // lane j < NB looks up box j of this tile
-                int page = -1, off = 0;
+                const int page = next_page;
+                next_page = lookup(kt + 1);
+                const int off = (key0 + lane * PB) % p.page_size;
                 bool valid = false;
-                if (lane < NB) {
-                    int key = key0 + lane * PB;
-                    if (key < s_len) {
-                        page = bt_row[key / p.page_size];
-                        off = key % p.page_size;
-                        valid = page >= 0 && page < p.num_pages;
-                        if (!valid)
-                            set_dev_error(p.dev_err, CPSA_DEV_PAGE_OUT_OF_RANGE);
-                    }
+                if (lane < NB && key0 + lane * PB < s_len) {
+                    valid = page >= 0 && page < p.num_pages;
+                    if (!valid)
+                        set_dev_error(p.dev_err, CPSA_DEV_PAGE_OUT_OF_RANGE);
                 }
                 const uint32_t vmask = __ballot_sync(0xffffffffu, valid);
                 const uint32_t bytes = (uint32_t)__popc(vmask) * box_bytes * C::kHalves;
@@ -222,7 +240,7 @@ chunk_attn_kernel(const ChunkParams p, const __grid_constant__ CUtensorMap tm_q,
                 tc_fence_after_sync();
                 return ok;
             };
-            for (int it = blockIdx.x; it < n_items && !*abort; it += gridDim.x) {
+            for (int it = it_begin; it < it_end && !*abort; ++it) {
                 const PrefillItem w = p.pitems[it];
                 const int n = w.kt1 - w.kt0;
                 if (!mbar_wait(&bars->q_full, q_uses & 1, abort))
@@ -297,7 +315,7 @@ chunk_attn_kernel(const ChunkParams p, const __grid_constant__ CUtensorMap tm_q,
         const uint32_t tO = tmem + lane_base + C::o_col(wg);
         const float sl2 = p.scale_log2;
         uint32_t s_uses = 0, o_base = 0;
-        for (int it = blockIdx.x; it < n_items && !*abort; it += gridDim.x) {
+        for (int it = it_begin; it < it_end && !*abort; ++it) {
             const PrefillItem w = p.pitems[it];
             const int kvh = w.kvh_hp & 0xFFFF, hp = w.kvh_hp >> 16;
             const int h = kvh * p.group + hp * NQ + wg;
@@ -315,23 +333,28 @@ chunk_attn_kernel(const ChunkParams p, const __grid_constant__ CUtensorMap tm_q,
                     break;
                 ++s_uses;
                 tc_fence_after_sync();
-                float sv[128];
+                // the S row straight from TMEM: four loads, one wait
+                uint32_t sr[4][32];
 #pragma unroll
-                for (int c = 0; c < 4; ++c) {
-                    uint32_t r[32];
-                    tmem_ld32(tS + c * 32, r);
-                    tmem_wait_ld();
-#pragma unroll
-                    for (int x = 0; x < 32; ++x) sv[c * 32 + x] = __uint_as_float(r[x]);
-                }
-                if (key0 + 127 > limit) {
+                for (int c = 0; c < 4; ++c) tmem_ld32(tS + c * 32, sr[c]);
+                tmem_wait_ld();
+#define SV(x) __uint_as_float(sr[(x) >> 5][(x) & 31])
+                // causal / tail mask: only tiles that reach past some row's last key
+                const bool masked = __any_sync(0xffffffffu, key0 + 127 > limit);
+                if (masked) {
 #pragma unroll
                     for (int x = 0; x < 128; ++x)
-                        if (key0 + x > limit) sv[x] = -INFINITY;
+                        if (key0 + x > limit) sr[x >> 5][x & 31] = 0xff800000u;   // -inf
                 }
-                float mx = sv[0];
+                // row max as 4 independent fmax3 chains joined at the end (short latency)
+                float mc[4];
 #pragma unroll
-                for (int x = 1; x < 128; ++x) mx = fmaxf(mx, sv[x]);
+                for (int c = 0; c < 4; ++c) mc[c] = fmaxf(SV(c), SV(c + 4));
+#pragma unroll
+                for (int x = 8; x < 128; x += 8)
+#pragma unroll
+                    for (int c = 0; c < 4; ++c) mc[c] = fmax3(mc[c], SV(x + c), SV(x + 4 + c));
+                const float mx = fmaxf(fmaxf(mc[0], mc[1]), fmaxf(mc[2], mc[3]));
                 const float m_tile = mx * sl2;
                 const bool need = m_tile > m_use + 8.f;
                 float alpha = 1.f;
@@ -341,20 +364,37 @@ chunk_attn_kernel(const ChunkParams p, const __grid_constant__ CUtensorMap tm_q,
                     m_use = m_tile;
                 }
                 const float mref = m_use == -INFINITY ? 0.f : m_use;
-                float sum = 0.f;
+                const uint64_t sl2x2 = f2_pack(sl2, sl2);
+                const uint64_t nref2 = f2_pack(-mref, -mref);
+                uint64_t sum2 = f2_pack(0.f, 0.f);
 #pragma unroll
                 for (int hh = 0; hh < 2; ++hh) {
                     uint32_t pk[32];
 #pragma unroll
                     for (int x = 0; x < 32; ++x) {
-                        const float a = ex2_approx(fmaf(sv[64 * hh + 2 * x], sl2, -mref));
-                        const float b = ex2_approx(fmaf(sv[64 * hh + 2 * x + 1], sl2, -mref));
-                        sum += a + b;
+                        // exponent of the pair (s * scale * log2e - m) in one packed FMA
+                        const uint64_t e2 = f2_fma(f2_pack(SV(64 * hh + 2 * x), SV(64 * hh + 2 * x + 1)), sl2x2, nref2);
+                        float a, b;
+                        if (!masked && (x & 7) < kFmaExpPairsPer8) {
+                            f2_unpack(e2, a, b);
+                            f2_unpack(exp2_poly_x2(f2_pack(fmaxf(a, -125.f), fmaxf(b, -125.f))), a, b);
+                        } else {
+                            f2_unpack(e2, a, b);
+                            a = ex2_approx(a);
+                            b = ex2_approx(b);
+                        }
+                        const uint64_t p2 = f2_pack(a, b);
+                        sum2 = f2_add(sum2, p2);
                         pk[x] = pack_bf16x2(a, b);
                     }
                     tmem_st32(tS + 32 * hh, pk);
                 }
-                l += sum;
+#undef SV
+                {
+                    float s0, s1;
+                    f2_unpack(sum2, s0, s1);
+                    l += s0 + s1;
+                }
                 tmem_wait_st();
                 if (__any_sync(0xffffffffu, need) && t > 0) {
                     // O holds the sum through tile t-1: wait for that P.V, then rescale
@@ -385,8 +425,10 @@ chunk_attn_kernel(const ChunkParams p, const __grid_constant__ CUtensorMap tm_q,
             tc_fence_after_sync();
             const bool valid_row = i < q_len;
             const int64_t t_row = (int64_t)p.cu_q[w.r] + i;
-            if (w.nsplit > 1) {
-                const int64_t pr = (int64_t)w.pbase + ((int64_t)row * p.num_q_heads + h) * w.nsplit + w.split;
+            const int npieces = w.piece_np >> 16;
+            if (npieces > 1) {
+                // partial of piece (piece_np & 0xffff) of this unit: unit-local (row, head) major
+                const int64_t pr = (int64_t)w.pbase + ((int64_t)row * NQ + wg) * npieces + (w.piece_np & 0xFFFF);
 #pragma unroll
                 for (int c = 0; c < D / 32; ++c) {
                     uint32_t r[32];

@@ -50,63 +50,85 @@ __global__ void __launch_bounds__(256) kv_write_kernel(const uint4 *__restrict__
 // ---------------------------------------------------------------------------
 // Combine of split rows: O = sum_s 2^(m_s - M) O_s / sum_s 2^(m_s - M) l_s,
 // M = max_s m_s (m in base-2 units). Persistent: the (row, q head) units of all
-// combine items are numbered consecutively (CombineItem::u0); warp w takes a
-// contiguous run of units, locating its first item by binary search.
+// combine items are numbered consecutively (CombineItem::u0; an item covers
+// nrows rows x nh heads from h0). Each CTA stages the items' first units in
+// shared memory and its warps take units in turn, one warp per unit, lane l
+// owning output columns [4l, 4l+4) (D = 128) or [2l, 2l+2) (D = 64); the
+// partial O loads of a unit are issued before its weights are formed.
 // ---------------------------------------------------------------------------
 constexpr int kCombineThreads = 256;
+constexpr int kCombineSmemItems = 4096;
+constexpr int kCombineMaxSplits = 32;
 
 template <int D>
 __global__ void __launch_bounds__(kCombineThreads) combine_kernel(const CombineParams p)
 {
+    __shared__ int s_u0[kCombineSmemItems];
     const int n_items = p.counts[kCntCombine];
     const int total = p.counts[kCntCombineUnits];
     if (n_items == 0 || total == 0)
         return;
+    const bool staged = n_items <= kCombineSmemItems;
+    if (staged) {
+        for (int i = threadIdx.x; i < n_items; i += kCombineThreads) s_u0[i] = p.citems[i].u0;
+        __syncthreads();
+    }
     const int lane = threadIdx.x & 31;
     const int warps = gridDim.x * (kCombineThreads / 32);
-    const int gw = blockIdx.x * (kCombineThreads / 32) + (threadIdx.x >> 5);
-    const int per = (total + warps - 1) / warps;
-    const int u_begin = gw * per;
-    const int u_end = min(total, u_begin + per);
-    if (u_begin >= u_end)
-        return;
     constexpr int PER_LANE = D / 32;
     const int Hq = p.num_q_heads;
-    // last item with u0 <= u_begin
-    int lo = 0, hi = n_items - 1;
-    while (lo < hi) {
-        const int mid = (lo + hi + 1) >> 1;
-        if (p.citems[mid].u0 <= u_begin) lo = mid; else hi = mid - 1;
-    }
-    int ci = lo;
-    CombineItem c = p.citems[ci];
-    for (int u = u_begin; u < u_end; ++u) {
-        while (u >= c.u0 + c.nrows * Hq) c = p.citems[++ci];
+    for (int u = blockIdx.x * (kCombineThreads / 32) + (threadIdx.x >> 5); u < total; u += warps) {
+        // last item with u0 <= u
+        int lo = 0, hi = n_items - 1;
+        while (lo < hi) {
+            const int mid = (lo + hi + 1) >> 1;
+            const int v = staged ? s_u0[mid] : p.citems[mid].u0;
+            if (v <= u) lo = mid; else hi = mid - 1;
+        }
+        const CombineItem c = p.citems[lo];
         const int local = u - c.u0;
-        const int row = local / Hq, h = local % Hq;
+        const int row = local / c.nh, h = c.h0 + local % c.nh;
         const int64_t pr0 = (int64_t)c.pbase + (int64_t)local * c.nsplit;
-        const float2 ml = lane < c.nsplit ? reinterpret_cast<const float2 *>(p.part_ml)[pr0 + lane]
-                                          : make_float2(-INFINITY, 0.f);
-        float M = ml.x;
-        for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
-        const float Mref = M == -INFINITY ? 0.f : M;
-        const float f = ex2_approx(ml.x - Mref);
-        float L = f * ml.y;
-        for (int o = 16; o > 0; o >>= 1) L += __shfl_xor_sync(0xffffffffu, L, o);
+        // partial O first (independent of the weights), then (m, l)
+        float o[kCombineMaxSplits / 4][PER_LANE];
         float acc[PER_LANE];
 #pragma unroll
         for (int e = 0; e < PER_LANE; ++e) acc[e] = 0.f;
-        for (int s = 0; s < c.nsplit; ++s) {
-            const float fs = __shfl_sync(0xffffffffu, f, s);
-            const float *src = p.part_o + (pr0 + s) * D + lane * PER_LANE;
-            if (PER_LANE == 4) {
-                const float4 x = __ldcs(reinterpret_cast<const float4 *>(src));
-                acc[0] += fs * x.x; acc[1] += fs * x.y; acc[2] += fs * x.z; acc[3] += fs * x.w;
-            } else {
+        const float2 ml = lane < c.nsplit ? __ldcs(reinterpret_cast<const float2 *>(p.part_ml) + pr0 + lane)
+                                          : make_float2(-INFINITY, 0.f);
+        float M = ml.x;
+        for (int s0 = 0; s0 < c.nsplit; s0 += kCombineMaxSplits / 4) {
+            const int cnt = min(kCombineMaxSplits / 4, c.nsplit - s0);
 #pragma unroll
-                for (int e = 0; e < PER_LANE; ++e) acc[e] += fs * src[e];
+            for (int j = 0; j < kCombineMaxSplits / 4; ++j) {
+                if (j < cnt) {
+                    const float *src = p.part_o + (pr0 + s0 + j) * D + lane * PER_LANE;
+                    if (PER_LANE == 4) {
+                        const float4 x = __ldcs(reinterpret_cast<const float4 *>(src));
+                        o[j][0] = x.x; o[j][1] = x.y; o[j][2 % PER_LANE] = x.z; o[j][3 % PER_LANE] = x.w;
+                    } else {
+                        const float2 x = __ldcs(reinterpret_cast<const float2 *>(src));
+                        o[j][0] = x.x; o[j][1 % PER_LANE] = x.y;
+                    }
+                }
+            }
+            if (s0 == 0) {
+                for (int off = 16; off > 0; off >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, off));
+            }
+            const float Mref = M == -INFINITY ? 0.f : M;
+            const float f = ex2_approx(ml.x - Mref);
+#pragma unroll
+            for (int j = 0; j < kCombineMaxSplits / 4; ++j) {
+                if (j < cnt) {
+                    const float fs = __shfl_sync(0xffffffffu, f, s0 + j);
+#pragma unroll
+                    for (int e = 0; e < PER_LANE; ++e) acc[e] += fs * o[j][e];
+                }
             }
         }
+        const float Mref = M == -INFINITY ? 0.f : M;
+        float L = ex2_approx(ml.x - Mref) * ml.y;
+        for (int off = 16; off > 0; off >>= 1) L += __shfl_xor_sync(0xffffffffu, L, off);
         const float inv = L > 0.f ? 1.f / L : 0.f;
         __nv_bfloat16 *dst = reinterpret_cast<__nv_bfloat16 *>(p.out) +
                              ((int64_t)(c.t0 + row) * Hq + h) * D + lane * PER_LANE;
@@ -204,7 +226,29 @@ split_kernel(const int32_t *__restrict__ query_lens, int num_reqs, float balance
     }
 }
 
+// Both exp2 paths of the attention kernels on an array: the FMA-pipe polynomial
+// (inputs clamped to [-125, 127] as the kernels do) and the hardware ex2.approx.
+__global__ void exp2_selftest_kernel(const float *x, float *poly, float *hw, int64_t n)
+{
+    for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n; i += (int64_t)gridDim.x * blockDim.x) {
+        const float v = x[i];
+        const float c = fminf(fmaxf(v, -125.0f), 127.0f);
+        float lo, hi;
+        f2_unpack(exp2_poly_x2(f2_pack(c, c)), lo, hi);
+        poly[i] = lo;
+        hw[i] = ex2_approx(v);
+    }
+}
+
 }  // namespace
+
+cudaError_t launch_exp2_selftest(const float *x, float *poly, float *hw, int64_t n, cudaStream_t s)
+{
+    if (n <= 0)
+        return cudaSuccess;
+    exp2_selftest_kernel<<<(int)((n + 255) / 256 < 1024 ? (n + 255) / 256 : 1024), 256, 0, s>>>(x, poly, hw, n);
+    return cudaGetLastError();
+}
 
 cudaError_t launch_kv_cache_write(const void *k, const void *v, const int64_t *slot_mapping, int64_t num_tokens,
                                   int num_kv_heads, int head_dim, int page_size, int64_t num_pages, void *k_cache,

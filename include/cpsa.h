@@ -232,6 +232,14 @@ int cpp_fit_latency_quadratic(const double *l, const double *t, int n, double *c
 int cpp_fit_latency_two_var(const double *x0, const double *x1, const double *x2,
                             const double *t, int n, double *coef);
 
+/*
+ * Self-test of the attention kernels' two base-2 exponentials on n device floats:
+ * out_poly[i] = the FMA-pipe polynomial path (x clamped to [-125, 127]; range
+ * reduction to f in [-1/2, 1/2] plus a degree-3 minimax polynomial, relative
+ * error 7.5e-5), out_hw[i] = the hardware ex2.approx. Stream-ordered.
+ */
+int cpp_selftest_exp2(const float *x, float *out_poly, float *out_hw, int64_t n, void *stream);
+
 /* Human-readable name of a status code. */
 const char *cpp_status_string(int status);
 

