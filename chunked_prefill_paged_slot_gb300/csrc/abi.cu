@@ -68,6 +68,24 @@ bool make_map(CUtensorMap *m, const void *base, uint64_t d0, uint64_t d1, uint64
     return r == CUDA_SUCCESS;
 }
 
+// 4-D bf16 view of a head_dim-128 cache, [cols 64][rows page][half 2][page-head
+// blocks], halves 128 bytes apart: one box of `rows` rows x both halves lands as
+// [half][rows][128 B] with the 128-byte swizzle.
+bool make_map4_halves(CUtensorMap *m, const void *base, int page_size, uint64_t blocks, uint32_t rows)
+{
+    auto enc = encode_fn();
+    if (!enc)
+        return false;
+    cuuint64_t dims[4] = {64, (cuuint64_t)page_size, 2, blocks};
+    cuuint64_t strides[3] = {256, 128, (cuuint64_t)page_size * 256};
+    cuuint32_t box[4] = {64, rows, 2, 1};
+    cuuint32_t estr[4] = {1, 1, 1, 1};
+    CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void *>(base), dims, strides, box, estr,
+                     CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                     CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
 int nq_for_group(int group) { return (group % 2 == 0) ? 2 : 1; }
 
 int check_attn_shape(int num_reqs, int64_t num_tokens, int num_q_heads, int num_kv_heads, int head_dim,
@@ -265,13 +283,20 @@ int cpp_chunked_prefill_attn_events(const void *q, const void *k_cache, const vo
     const uint64_t rows_kv = (uint64_t)num_pages * (uint64_t)num_kv_heads;
     CUtensorMap tq, tk, tv, tkd, tvd;
     const uint32_t pb_chunk = page_size < 128 ? page_size : 128;
-    const uint32_t pb_dec = page_size < kDecodeBoxRowsMax ? page_size : kDecodeBoxRowsMax;
     if (!make_map(&tq, q, D, (uint64_t)num_q_heads, (uint64_t)num_tokens, D * 2, D * 2 * num_q_heads, 64, 1, 128) ||
         !make_map(&tk, k_cache, D, (uint64_t)page_size, rows_kv, D * 2, D * 2 * page_size, 64, pb_chunk, 1) ||
-        !make_map(&tv, v_cache, D, (uint64_t)page_size, rows_kv, D * 2, D * 2 * page_size, 64, pb_chunk, 1) ||
-        !make_map(&tkd, k_cache, D, (uint64_t)page_size, rows_kv, D * 2, D * 2 * page_size, 64, pb_dec, 1) ||
-        !make_map(&tvd, v_cache, D, (uint64_t)page_size, rows_kv, D * 2, D * 2 * page_size, 64, pb_dec, 1))
+        !make_map(&tv, v_cache, D, (uint64_t)page_size, rows_kv, D * 2, D * 2 * page_size, 64, pb_chunk, 1))
         return CPSA_ERR_CUDA;
+    // decode: one box per page-head block (at most 64 rows) covering all of head_dim
+    const uint32_t pb_dec = page_size < kDecodeChunk ? page_size : kDecodeChunk;
+    if (head_dim == 128) {
+        if (!make_map4_halves(&tkd, k_cache, page_size, rows_kv, pb_dec) ||
+            !make_map4_halves(&tvd, v_cache, page_size, rows_kv, pb_dec))
+            return CPSA_ERR_CUDA;
+    } else if (!make_map(&tkd, k_cache, D, (uint64_t)page_size, rows_kv, D * 2, D * 2 * page_size, 64, pb_dec, 1) ||
+               !make_map(&tvd, v_cache, D, (uint64_t)page_size, rows_kv, D * 2, D * 2 * page_size, 64, pb_dec, 1)) {
+        return CPSA_ERR_CUDA;
+    }
 
     ChunkParams cp;
     static_cast<AttnCommon &>(cp) = ac;
@@ -286,6 +311,8 @@ int cpp_chunked_prefill_attn_events(const void *q, const void *k_cache, const vo
     static_cast<AttnCommon &>(dp) = ac;
     dp.ditems = ditems;
     dp.q = q;
+    dp.k_cache_ptr = k_cache;
+    dp.v_cache_ptr = v_cache;
     int grid_d = (int)(L.max_ditems < sms ? L.max_ditems : sms);
     if (grid_d > 0 && launch_decode_attn(dp, tkd, tvd, head_dim, grid_d, s) != cudaSuccess)
         return CPSA_ERR_CUDA;

@@ -9,11 +9,17 @@
 // row's context (a whole context, or one split of it).
 //
 // CTA layout (160 threads, persistent over decode items):
-//   warp 4     TMA producer: 64-key stages of K and V (one box per page or per
-//              64 rows of a page), 128-byte swizzled, into a ring of stages.
-//   warps 0-3  consumers, round-robin over stages: S = q K^T and O += P V with
-//              mma.sync m16n8k16 (the G <= 16 q heads are the M rows), online softmax
-//              in fp32 (base-2 exponent), partial state per warp.
+//   last warp  producer: 64-key stages of K and V through TMA, one box per
+//              page-head block (or per 64 rows of a larger page) that covers
+//              both 64-column halves of head_dim (a 4-D view: columns, rows,
+//              halves, page-head blocks), 128-byte swizzled; the stage holds
+//              [block][half][rows][128 B].
+//   consumers  one or two groups of 4 warps; groups take alternate stages and
+//              inside a group warp w takes keys [16w, 16w + 16) of the stage:
+//              S = q K^T and O += P V with mma.sync m16n8k16
+//              (the G <= 16 q heads are the M rows), online softmax in fp32
+//              (base-2 exponent), partial state per warp. A stage is refilled
+//              once its group's four warps are done with it.
 // At the end of an item the four warps merge (max, sum, O) through shared
 // memory and write the bf16 row, or an fp32 partial when the row is split.
 #include "common.cuh"
@@ -25,24 +31,29 @@ namespace cpsa {
 namespace {
 
 constexpr int kKC = kDecodeChunk;   // keys per stage
-constexpr int kConsumers = 4;
+constexpr int kLookahead = 4;       // stages of block_table lookups kept in flight
 
-template <int D>
+template <int D, bool HI>
 struct DecCfg {
+    // HI: up to 16 q heads per kv head (both halves of the mma rows); one group
+    // of 4 consumer warps. Otherwise two groups take alternate stages.
+    static constexpr int kGroups = HI ? 1 : 2;
+    static constexpr int kConsumers = 4 * kGroups;
     static constexpr int kHalves = D / 64;
-    static constexpr int kHalfBytes = kKC * 128;
-    static constexpr int kTileBytes = kHalves * kHalfBytes;   // K or V of one stage
+    static constexpr int kRowBytes = D * 2;
+    static constexpr int kTileBytes = kKC * kRowBytes;        // K or V of one stage
     static constexpr int kStageBytes = 2 * kTileBytes;
-    static constexpr int kStages = D == 128 ? 4 : 8;
+    static constexpr int kGroupRows = HI ? kMaxGroup : 8;      // q heads per kv head, upper bound
+    static constexpr int kStages = D == 128 ? 5 : 10;
     static constexpr int kMergeOff = kStages * kStageBytes;
-    static constexpr int kMergeBytes = kConsumers * kMaxGroup * (D + 2) * 4;
+    static constexpr int kMergeBytes = kConsumers * kGroupRows * (D + 2) * 4;
     static constexpr int kBarOff = kMergeOff + kMergeBytes;
     static constexpr int kSmemBytes = kBarOff + 256 + 1024;
     static constexpr int kThreads = 32 * (kConsumers + 1);
 };
 
 struct DecBars {
-    uint64_t full[8], empty[8];
+    uint64_t full[10], empty[10];
     int abort;
 };
 
@@ -68,22 +79,31 @@ __device__ __forceinline__ void mma_bf16(float (&d)[4], const uint32_t (&a)[4], 
                  : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
 }
 
-// Byte address of element (row, col) of a [rows][D] bf16 tile stored as
-// 64-column halves with the 128-byte swizzle (16-byte chunk index ^ row % 8).
+// Byte offset of the 128-byte half-row (row, half) in a stage tile laid out as
+// [block of 2^lg rows][64-column half][row in block][128 B]; blocks are >= 8 rows.
 template <int D>
-__device__ __forceinline__ uint32_t swz_addr(uint32_t base, int row, int col)
+__device__ __forceinline__ uint32_t half_row_off(int row, int half, int lg)
 {
-    const int half = col >> 6;
+    const int blk = row >> lg, r = row & ((1 << lg) - 1);
+    return ((uint32_t)(blk * (D / 64) + half) << (lg + 7)) + ((uint32_t)r << 7);
+}
+
+// Byte address of element (row, col) of such a tile, 128-byte swizzled: the
+// 16-byte chunk c of a row sits at c ^ (row % 8) inside its half-row.
+template <int D>
+__device__ __forceinline__ uint32_t swz_addr(uint32_t base, int row, int col, int lg)
+{
     const int ch = (col & 63) >> 3;
-    return base + half * DecCfg<D>::kHalfBytes + row * 128 + ((ch ^ (row & 7)) << 4) + (col & 7) * 2;
+    return base + half_row_off<D>(row, col >> 6, lg) + ((ch ^ (row & 7)) << 4) + (col & 7) * 2;
 }
 
 template <int D, bool HI>
-__global__ void __launch_bounds__(DecCfg<D>::kThreads, 1)
+__global__ void __launch_bounds__(DecCfg<D, HI>::kThreads, 1)
 decode_attn_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap tm_k,
                    const __grid_constant__ CUtensorMap tm_v)
 {
-    using C = DecCfg<D>;
+    using C = DecCfg<D, HI>;
+    constexpr int GR = C::kGroupRows;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
     DecBars *bars = reinterpret_cast<DecBars *>(smem + C::kBarOff);
@@ -95,7 +115,7 @@ decode_attn_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap tm_
     if (threadIdx.x == 0) {
         for (int s = 0; s < C::kStages; ++s) {
             mbar_init(&bars->full[s], 1);
-            mbar_init(&bars->empty[s], 1);
+            mbar_init(&bars->empty[s], 4);
         }
         bars->abort = 0;
         fence_barrier_init();
@@ -103,7 +123,7 @@ decode_attn_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap tm_
     __syncthreads();
     volatile int *abort = &bars->abort;
 
-    if (warp == kConsumers) {
+    if (warp == C::kConsumers) {
         // ------------------------------------------------------------ producer
         if (lane == 0) {
             tma_prefetch_desc(&tm_k);
@@ -111,33 +131,42 @@ decode_attn_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap tm_
         }
         const int PB = p.page_size < kKC ? p.page_size : kKC;
         const int NB = kKC / PB;
-        const uint32_t box_bytes = (uint32_t)PB * 128u;
+        const uint32_t box_bytes = (uint32_t)PB * C::kRowBytes;
         uint32_t g = 0;
         bool stop = false;
         for (int it = blockIdx.x; it < n_items && !stop && !*abort; it += gridDim.x) {
             const DecodeItem w = p.ditems[it];
             const int32_t *bt_row = p.block_table + (int64_t)w.r * p.max_blocks;
+            // page numbers of the next kLookahead stages stay in flight in registers
+            // (lane j < NB holds box j of a stage), so the block_table latency is
+            // paid once per item rather than once per stage
+            auto lookup = [&](int c) -> int {
+                const int key = c + lane * PB;
+                return (lane < NB && key < w.key1) ? __ldg(bt_row + key / p.page_size) : -1;
+            };
+            int pg[kLookahead];
+#pragma unroll
+            for (int k = 0; k < kLookahead; ++k) pg[k] = lookup(w.key0 + k * kKC);
             for (int c0 = w.key0; c0 < w.key1; c0 += kKC, ++g) {
+                const int page = pg[0];
+#pragma unroll
+                for (int k = 0; k + 1 < kLookahead; ++k) pg[k] = pg[k + 1];
+                pg[kLookahead - 1] = lookup(c0 + kLookahead * kKC);
                 const int stage = g % C::kStages;
                 if (g >= (uint32_t)C::kStages &&
                     !mbar_wait(&bars->empty[stage], ((g / C::kStages) - 1) & 1, abort)) {
                     stop = true;
                     break;
                 }
-                int page = -1, off = 0;
+                const int off = (c0 + lane * PB) % p.page_size;
                 bool valid = false;
-                if (lane < NB) {
-                    const int key = c0 + lane * PB;
-                    if (key < w.key1) {
-                        page = bt_row[key / p.page_size];
-                        off = key % p.page_size;
-                        valid = page >= 0 && page < p.num_pages;
-                        if (!valid)
-                            set_dev_error(p.dev_err, CPSA_DEV_PAGE_OUT_OF_RANGE);
-                    }
+                if (lane < NB && c0 + lane * PB < w.key1) {
+                    valid = page >= 0 && page < p.num_pages;
+                    if (!valid)
+                        set_dev_error(p.dev_err, CPSA_DEV_PAGE_OUT_OF_RANGE);
                 }
                 const uint32_t vmask = __ballot_sync(0xffffffffu, valid);
-                const uint32_t bytes = (uint32_t)__popc(vmask) * box_bytes * C::kHalves * 2;
+                const uint32_t bytes = (uint32_t)__popc(vmask) * box_bytes * 2;
                 uint8_t *kdst = smem + stage * C::kStageBytes;
                 uint8_t *vdst = kdst + C::kTileBytes;
                 if (lane == 0)
@@ -146,10 +175,14 @@ decode_attn_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap tm_
                     const int pj = __shfl_sync(0xffffffffu, page, j);
                     const int oj = __shfl_sync(0xffffffffu, off, j);
                     if (lane == 0 && ((vmask >> j) & 1u)) {
+                        // rows [oj, oj + PB) of page-head block (pj, kvh), both halves in one box
                         const int z = pj * p.num_kv_heads + w.kvh;
-                        for (int c = 0; c < C::kHalves; ++c) {
-                            tma_load_3d(kdst + c * C::kHalfBytes + j * box_bytes, &tm_k, &bars->full[stage], c * 64, oj, z);
-                            tma_load_3d(vdst + c * C::kHalfBytes + j * box_bytes, &tm_v, &bars->full[stage], c * 64, oj, z);
+                        if (C::kHalves == 2) {
+                            tma_load_4d(kdst + j * box_bytes, &tm_k, &bars->full[stage], 0, oj, 0, z);
+                            tma_load_4d(vdst + j * box_bytes, &tm_v, &bars->full[stage], 0, oj, 0, z);
+                        } else {
+                            tma_load_3d(kdst + j * box_bytes, &tm_k, &bars->full[stage], 0, oj, z);
+                            tma_load_3d(vdst + j * box_bytes, &tm_v, &bars->full[stage], 0, oj, z);
                         }
                     }
                 }
@@ -165,6 +198,8 @@ decode_attn_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap tm_
     const float sl2 = p.scale_log2;
     const int qrow = lane >> 2;
     const int qcol = (lane & 3) * 2;     // column pair within an 8-wide tile
+    const int group = warp >> 2;
+    const int lg = 31 - __clz(p.page_size < kKC ? p.page_size : kKC);   // log2 rows per block
     uint32_t g = 0;
     // every consumer warp walks every item (no early exit on abort: the named
     // barriers below need all four; a failed wait returns at once instead)
@@ -199,52 +234,52 @@ decode_attn_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap tm_
 
         for (int j = 0; j < nch; ++j) {
             const uint32_t gg = g + j;
-            if ((int)(gg % kConsumers) != warp)
+            if ((int)(gg % C::kGroups) != group)
                 continue;
             const int stage = gg % C::kStages;
             if (!mbar_wait(&bars->full[stage], (gg / C::kStages) & 1, abort))
                 break;
             const int c0 = w.key0 + j * kKC;
-            const int nv = min(kKC, w.key1 - c0);
+            const int kb0 = (warp & 3) * 16;               // this warp's keys in the stage
+            const int nv = min(16, w.key1 - c0 - kb0);     // valid keys of this warp (may be <= 0)
             uint8_t *kst = smem + stage * C::kStageBytes;
             uint8_t *vst = kst + C::kTileBytes;
-            if (nv < kKC) {
-                // value rows past the range may hold anything (NaN included): zero them
-                const int nchunks = (kKC - nv) * 8;
-                for (int c = 0; c < C::kHalves; ++c)
-                    for (int x = lane; x < nchunks; x += 32)
-                        reinterpret_cast<uint4 *>(vst + c * C::kHalfBytes + nv * 128)[x] = make_uint4(0, 0, 0, 0);
+            if (nv < 16) {
+                // value rows past the range may hold anything (NaN included): zero ours
+                // (whole 128-byte half-rows, so the swizzle does not matter)
+                const int first = kb0 + max(nv, 0);
+                const int nchunks = (kb0 + 16 - first) * C::kHalves * 8;
+                for (int x = lane; x < nchunks; x += 32) {
+                    const int row = first + x / (C::kHalves * 8);
+                    const int half = (x >> 3) % C::kHalves;
+                    *reinterpret_cast<uint4 *>(vst + half_row_off<D>(row, half, lg) + (x & 7) * 16) =
+                        make_uint4(0, 0, 0, 0);
+                }
                 __syncwarp();
             }
             const uint32_t kb = smem_u32(kst), vb = smem_u32(vst);
-            // S = q K^T : 8 n-tiles of 8 keys
-            float s[8][4];
-#pragma unroll
-            for (int nt = 0; nt < 8; ++nt) s[nt][0] = s[nt][1] = s[nt][2] = s[nt][3] = 0.f;
             const int mat = lane >> 3, mrow = lane & 7;
+            // S = q K^T : 2 n-tiles of 8 keys
+            float s[2][4];
+#pragma unroll
+            for (int nt = 0; nt < 2; ++nt) s[nt][0] = s[nt][1] = s[nt][2] = s[nt][3] = 0.f;
 #pragma unroll
             for (int kk = 0; kk < D / 16; ++kk) {
-#pragma unroll
-                for (int np = 0; np < 4; ++np) {
-                    uint32_t b0, b1, b2, b3;
-                    const int key = np * 16 + mrow + (mat >> 1) * 8;
-                    const int col = kk * 16 + (mat & 1) * 8;
-                    ldsm_x4(swz_addr<D>(kb, key, col), b0, b1, b2, b3);
-                    mma_bf16(s[2 * np], qa[kk], b0, b1);
-                    mma_bf16(s[2 * np + 1], qa[kk], b2, b3);
-                }
+                uint32_t b0, b1, b2, b3;
+                const int key = kb0 + mrow + (mat >> 1) * 8;
+                const int col = kk * 16 + (mat & 1) * 8;
+                ldsm_x4(swz_addr<D>(kb, key, col, lg), b0, b1, b2, b3);
+                mma_bf16(s[0], qa[kk], b0, b1);
+                mma_bf16(s[1], qa[kk], b2, b3);
             }
             // mask and online softmax per row (C fragment: [2rr], [2rr+1] of row qrow + 8rr)
-            uint32_t pa[4][4];
-#pragma unroll
-            for (int rr = 0; rr < 2; ++rr)
-#pragma unroll
-                for (int kq = 0; kq < 4; ++kq) pa[kq][rr] = pa[kq][2 + rr] = 0u;
+            uint32_t pa[4];
+            pa[0] = pa[1] = pa[2] = pa[3] = 0u;
 #pragma unroll
             for (int rr = 0; rr < R; ++rr) {
                 float mx = -INFINITY;
 #pragma unroll
-                for (int nt = 0; nt < 8; ++nt) {
+                for (int nt = 0; nt < 2; ++nt) {
 #pragma unroll
                     for (int e = 0; e < 2; ++e) {
                         if (nt * 8 + qcol + e >= nv) s[nt][2 * rr + e] = -INFINITY;
@@ -254,17 +289,18 @@ decode_attn_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap tm_
                 mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
                 mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
                 const float m_new = fmaxf(m_run[rr], mx * sl2);
-                const float alpha = ex2_approx(m_run[rr] - m_new);   // m_run = -inf gives 0
+                // m_run = -inf gives 0; an all-masked quarter (m_new = m_run = -inf) keeps 1
+                const float alpha = m_new == m_run[rr] ? 1.f : ex2_approx(m_run[rr] - m_new);
                 m_run[rr] = m_new;
                 const float mref = m_new == -INFINITY ? 0.f : m_new;
                 float psum = 0.f;
 #pragma unroll
-                for (int nt = 0; nt < 8; ++nt) {
+                for (int nt = 0; nt < 2; ++nt) {
                     const float p0 = ex2_approx(fmaf(s[nt][2 * rr], sl2, -mref));
                     const float p1 = ex2_approx(fmaf(s[nt][2 * rr + 1], sl2, -mref));
                     psum += p0 + p1;
-                    // A fragment of P for k-step nt/2: a[rr] keys 0-7, a[2+rr] keys 8-15
-                    pa[nt >> 1][(nt & 1) * 2 + rr] = pack_bf16x2(p0, p1);
+                    // A fragment of P: a[rr] keys 0-7, a[2+rr] keys 8-15
+                    pa[nt * 2 + rr] = pack_bf16x2(p0, p1);
                 }
                 l_run[rr] = l_run[rr] * alpha + psum;
 #pragma unroll
@@ -273,30 +309,27 @@ decode_attn_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap tm_
                     o[nt][2 * rr + 1] *= alpha;
                 }
             }
-            // O += P V : A = P (keys as K), B = V rows via transposed ldmatrix
+            // O += P V : A = P (16 keys as K), B = V rows via transposed ldmatrix
 #pragma unroll
-            for (int kk = 0; kk < 4; ++kk) {
-#pragma unroll
-                for (int np = 0; np < D / 16; ++np) {
-                    uint32_t b0, b1, b2, b3;
-                    const int key = kk * 16 + mrow + (mat & 1) * 8;
-                    const int col = np * 16 + (mat >> 1) * 8;
-                    ldsm_x4_t(swz_addr<D>(vb, key, col), b0, b1, b2, b3);
-                    mma_bf16(o[2 * np], pa[kk], b0, b1);
-                    mma_bf16(o[2 * np + 1], pa[kk], b2, b3);
-                }
+            for (int np = 0; np < D / 16; ++np) {
+                uint32_t b0, b1, b2, b3;
+                const int key = kb0 + mrow + (mat & 1) * 8;
+                const int col = np * 16 + (mat >> 1) * 8;
+                ldsm_x4_t(swz_addr<D>(vb, key, col, lg), b0, b1, b2, b3);
+                mma_bf16(o[2 * np], pa, b0, b1);
+                mma_bf16(o[2 * np + 1], pa, b2, b3);
             }
-            if (nv < kKC)
-                fence_proxy_async_smem();   // our zeroing writes before the next TMA into this stage
+            if (nv < 16)
+                fence_proxy_async_smem();   // our zeroing writes before the next copy into this stage
             __syncwarp();
             if (lane == 0)
                 mbar_arrive(&bars->empty[stage]);
         }
         g += nch;
         // merge the four warps' states: max, sum, O
-        float *mm = merge;                                   // [4][16]
-        float *ll = merge + kConsumers * kMaxGroup;          // [4][16]
-        float *oo = merge + 2 * kConsumers * kMaxGroup;      // [4][16][D]
+        float *mm = merge;                                   // [warps][GR]
+        float *ll = merge + C::kConsumers * GR;              // [warps][GR]
+        float *oo = merge + 2 * C::kConsumers * GR;          // [warps][GR][D]
 #pragma unroll
         for (int rr = 0; rr < R; ++rr) {
             float lq = l_run[rr];
@@ -305,29 +338,29 @@ decode_attn_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap tm_
             const int row = qrow + 8 * rr;
             if (row < G) {
                 if ((lane & 3) == 0) {
-                    mm[warp * kMaxGroup + row] = m_run[rr];
-                    ll[warp * kMaxGroup + row] = lq;
+                    mm[warp * GR + row] = m_run[rr];
+                    ll[warp * GR + row] = lq;
                 }
 #pragma unroll
                 for (int nt = 0; nt < D / 8; ++nt) {
-                    oo[(warp * kMaxGroup + row) * D + nt * 8 + qcol] = o[nt][2 * rr];
-                    oo[(warp * kMaxGroup + row) * D + nt * 8 + qcol + 1] = o[nt][2 * rr + 1];
+                    oo[(warp * GR + row) * D + nt * 8 + qcol] = o[nt][2 * rr];
+                    oo[(warp * GR + row) * D + nt * 8 + qcol + 1] = o[nt][2 * rr + 1];
                 }
             }
         }
-        named_bar_sync(1, 32 * kConsumers);
-        for (int e = threadIdx.x; e < G * D; e += 32 * kConsumers) {
+        named_bar_sync(1, 32 * C::kConsumers);
+        for (int e = threadIdx.x; e < G * D; e += 32 * C::kConsumers) {
             const int row = e / D, d = e % D;
             float M = -INFINITY;
 #pragma unroll
-            for (int x = 0; x < kConsumers; ++x) M = fmaxf(M, mm[x * kMaxGroup + row]);
+            for (int x = 0; x < C::kConsumers; ++x) M = fmaxf(M, mm[x * GR + row]);
             const float Mref = M == -INFINITY ? 0.f : M;
             float L = 0.f, acc = 0.f;
 #pragma unroll
-            for (int x = 0; x < kConsumers; ++x) {
-                const float f = ex2_approx(mm[x * kMaxGroup + row] - Mref);
-                L += f * ll[x * kMaxGroup + row];
-                acc += f * oo[(x * kMaxGroup + row) * D + d];
+            for (int x = 0; x < C::kConsumers; ++x) {
+                const float f = ex2_approx(mm[x * GR + row] - Mref);
+                L += f * ll[x * GR + row];
+                acc += f * oo[(x * GR + row) * D + d];
             }
             const int h = w.kvh * G + row;
             if (w.nsplit > 1) {
@@ -340,18 +373,18 @@ decode_attn_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap tm_
                     __float2bfloat16_rn(L > 0.f ? acc / L : 0.f);
             }
         }
-        named_bar_sync(1, 32 * kConsumers);
+        named_bar_sync(1, 32 * C::kConsumers);
     }
     if (threadIdx.x == 0 && *abort)
         set_dev_error(p.dev_err, CPSA_DEV_WAIT_TIMEOUT);
 }
 
-template <int D>
+template <int D, bool HI>
 cudaError_t launch_decode_t(const DecodeParams &p, const CUtensorMap &tk, const CUtensorMap &tv, int grid,
                             cudaStream_t s)
 {
-    using C = DecCfg<D>;
-    auto k = p.group > 8 ? decode_attn_kernel<D, true> : decode_attn_kernel<D, false>;
+    using C = DecCfg<D, HI>;
+    auto k = decode_attn_kernel<D, HI>;
     cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
     if (e != cudaSuccess)
         return e;
@@ -361,10 +394,14 @@ cudaError_t launch_decode_t(const DecodeParams &p, const CUtensorMap &tk, const 
 
 }  // namespace
 
-cudaError_t launch_decode_attn(const DecodeParams &p, const CUtensorMap &tk, const CUtensorMap &tv,
-                               int head_dim, int grid, cudaStream_t s)
+cudaError_t launch_decode_attn(const DecodeParams &p, const CUtensorMap &tk, const CUtensorMap &tv, int head_dim,
+                               int grid, cudaStream_t s)
 {
-    return head_dim == 128 ? launch_decode_t<128>(p, tk, tv, grid, s) : launch_decode_t<64>(p, tk, tv, grid, s);
+    if (p.group > 8)
+        return head_dim == 128 ? launch_decode_t<128, true>(p, tk, tv, grid, s)
+                               : launch_decode_t<64, true>(p, tk, tv, grid, s);
+    return head_dim == 128 ? launch_decode_t<128, false>(p, tk, tv, grid, s)
+                           : launch_decode_t<64, false>(p, tk, tv, grid, s);
 }
 
 }  // namespace cpsa

@@ -35,6 +35,8 @@ struct ChunkParams : AttnCommon {
 struct DecodeParams : AttnCommon {
     const DecodeItem *ditems;
     const void *q;             // bf16 [T][Hq][D]
+    const void *k_cache_ptr;   // bf16 [pages][Hkv][P][D]
+    const void *v_cache_ptr;
 };
 
 struct CombineParams {
@@ -48,8 +50,8 @@ struct CombineParams {
 
 cudaError_t launch_chunk_attn(const ChunkParams &p, const CUtensorMap &tq, const CUtensorMap &tk,
                               const CUtensorMap &tv, int head_dim, int nq, int grid, cudaStream_t s);
-cudaError_t launch_decode_attn(const DecodeParams &p, const CUtensorMap &tk, const CUtensorMap &tv,
-                               int head_dim, int grid, cudaStream_t s);
+cudaError_t launch_decode_attn(const DecodeParams &p, const CUtensorMap &tk, const CUtensorMap &tv, int head_dim,
+                               int grid, cudaStream_t s);
 cudaError_t launch_combine(const CombineParams &p, int head_dim, int grid, cudaStream_t s);
 
 cudaError_t launch_kv_cache_write(const void *k, const void *v, const int64_t *slot_mapping,
@@ -61,7 +63,5 @@ cudaError_t launch_split_microbatch(const int32_t *query_lens, int num_reqs, flo
 
 cudaError_t launch_exp2_selftest(const float *x, float *poly, float *hw, int64_t n, cudaStream_t s);
 
-// Rows of K/V per TMA box for the decode kernel (keys per pipeline stage cap).
-constexpr int kDecodeBoxRowsMax = 64;
 
 }  // namespace cpsa
