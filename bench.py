@@ -276,6 +276,136 @@ def decode_bandwidth(dev, reps=5):
     return res
 
 
+# ----------------------------------------------------------------------------- suite of the other workloads
+class ChunkTimer:
+    """Times one chunk (split + KV write + attention) of the headline sequence at
+    any (history, chunk size) with CUDA events; L2 flushed before each repetition."""
+
+    def __init__(self, dev):
+        import torch
+        import chunked_prefill_paged_slot_gb300 as cpsa
+        self.torch, self.cpsa, self.dev = torch, cpsa, dev
+        self.q, self.k, self.v, self.slots, self.bt = draw_inputs(dev)
+        n_pages = SEQ // PAGE
+        self.k_cache = torch.zeros((n_pages, HKV, PAGE, D), dtype=torch.bfloat16, device=dev)
+        self.v_cache = torch.zeros_like(self.k_cache)
+        self.err = torch.zeros(1, dtype=torch.int32, device=dev)
+        self.split_out = torch.zeros(3, dtype=torch.int32, device=dev)
+        self.ws = torch.empty(cpsa.cpp_attn_workspace_bytes(1, 8192, HQ, HKV, D, 8), dtype=torch.uint8, device=dev)
+        self.out = torch.empty_like(self.q)
+        self.flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+        # the whole sequence's K/V in the cache (history of any chunk)
+        for a in range(0, SEQ, 4096):
+            cpsa.cpp_kv_cache_write(self.k[a:a + 4096], self.v[a:a + 4096], self.slots[a:a + 4096],
+                                    self.k_cache, self.v_cache, self.err)
+        torch.cuda.synchronize()
+
+    def time(self, h, c, reps=5):
+        torch, cpsa = self.torch, self.cpsa
+        ql = torch.tensor([c], dtype=torch.int32, device=self.dev)
+        sl = torch.tensor([h + c], dtype=torch.int32, device=self.dev)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        ts = []
+        for r in range(reps + 2):
+            self.flush.zero_()
+            e0.record()
+            cpsa.cpp_split_microbatch(ql, self.split_out, 0.1, 256)
+            cpsa.cpp_kv_cache_write(self.k[h:h + c], self.v[h:h + c], self.slots[h:h + c], self.k_cache,
+                                    self.v_cache, self.err)
+            cpsa.cpp_chunked_prefill_attn(self.q[h:h + c], self.k_cache, self.v_cache, ql, sl, self.bt,
+                                          self.out[h:h + c], self.ws, self.err, max_kv_splits=8)
+            e1.record()
+            torch.cuda.synchronize()
+            if r >= 2:
+                ts.append(e0.elapsed_time(e1))
+        return float(np.median(ts))
+
+
+def fit_report(X, t):
+    X = np.asarray(X, dtype=np.float64)
+    t = np.asarray(t, dtype=np.float64)
+    coef, *_ = np.linalg.lstsq(X, t, rcond=None)
+    res = t - X @ coef
+    return [float(c) for c in coef], {"rms_ms": float(np.sqrt(np.mean(res ** 2))),
+                                      "max_rel": float(np.max(np.abs(res) / t))}
+
+
+def suite(dev):
+    """Dynamic chunking (profile, fit, plan, per-chunk times), the two-variable
+    latency fit, tile alignment, and the micro-batch workload on one vs two streams."""
+    import torch
+    import chunked_prefill_paged_slot_gb300 as cpsa
+    import workloads as W
+    out = {}
+    ct = ChunkTimer(dev)
+    # --- profile: 64 sizes base*i/64 at history 0, fit f(l) = a l^2 + b l + c
+    sizes = W.chunk_profile_sizes(4096, 64)
+    prof = [ct.time(0, l, reps=3) for l in sizes]
+    a, b, c = cpsa.cpp_fit_latency_quadratic(sizes, prof)
+    _, fr = fit_report(np.stack([np.square(sizes), sizes, np.ones(len(sizes))], 1), prof)
+    chunks = cpsa.cpp_plan_chunk_sizes(a, b, c, SEQ, 4096, PAGE, 64, 0, 0, 1.0)
+    L = 0
+    dyn = []
+    for x in chunks:
+        dyn.append(ct.time(L, x, reps=3))
+        L += x
+    body = dyn[:-1] if len(dyn) > 2 else dyn
+    out["dynamic_chunks"] = {
+        "workload": "32768-token prompt, chunk sizes from the solver on f(l) fitted to 64 profile sizes "
+                    "l = 64..4096 at history 0 (page 128, min 64, base 4096, smoothing 1)",
+        "fit_f_l": {"a": a, "b": b, "c": c, **fr}, "target_ms": a * 4096 ** 2 + b * 4096,
+        "chunks": chunks, "chunk_ms": [round(v, 4) for v in dyn],
+        "cv_excluding_last": float(np.std(body) / np.mean(body)), "total_ms": float(np.sum(dyn))}
+    # --- fixed 512 chunks (the headline sequence) for f(C, H)
+    fixed = [ct.time(512 * i, 512, reps=3) for i in range(N_CHUNKS)]
+    samples_C = [512] * N_CHUNKS + list(chunks) + list(sizes)
+    hs, L = [], 0
+    for x in chunks:
+        hs.append(L)
+        L += x
+    samples_H = [512 * i for i in range(N_CHUNKS)] + hs + [0] * len(sizes)
+    times = fixed + dyn + prof
+    Cs = np.asarray(samples_C, dtype=np.float64)
+    Hs = np.asarray(samples_H, dtype=np.float64)
+    a2, b2, c2 = cpsa.cpp_fit_latency_two_var(Cs * (Cs + Hs), Cs + Hs, np.ones_like(Cs), times)
+    _, fr2 = fit_report(np.stack([Cs * (Cs + Hs), Cs + Hs, np.ones_like(Cs)], 1), times)
+    out["fixed_chunks_512"] = {"chunk_ms": [round(v, 4) for v in fixed], "total_ms": float(np.sum(fixed))}
+    out["fit_f_C_H"] = {"a": a2, "b": b2, "c": c2, "samples": len(times), **fr2}
+    # --- tile alignment around 512 at history 8192
+    out["tile_alignment_h8192"] = {str(x): round(ct.time(8192, x, reps=5), 4) for x in (511, 512, 513)}
+    del ct
+    torch.cuda.empty_cache()
+    # --- micro-batch workload: one stream vs the balanced split on two streams
+    spec = W.spec_microbatch()
+    d = W.device_batch(spec, device=dev)
+    B, T = len(spec.qlen), sum(spec.qlen)
+    step = cpsa.AttentionStep(B, T, HQ, HKV, D, max_kv_splits=8, two_stream=True, device=dev)
+    o = torch.empty_like(d["q"])
+    args = (d["q"], d["k"], d["v"], d["slot_mapping"], d["k_cache"], d["v_cache"], d["query_lens"],
+            d["seq_lens"], d["block_table"], o)
+    def wall(fn, reps=5):
+        ts = []
+        for r in range(reps + 2):
+            torch.cuda.synchronize()
+            t0 = time.perf_counter()
+            fn()
+            torch.cuda.synchronize()
+            if r >= 2:
+                ts.append(1e3 * (time.perf_counter() - t0))
+        return float(np.median(ts))
+    one = wall(lambda: step.run(*args))
+    two = wall(lambda: step.run_two_stream(*args))
+    pf = sum(4.0 * D * HQ * (q * h + q * (q + 1) // 2) for q, h in zip(spec.qlen, spec.hist) if q > 1)
+    out["microbatch_two_streams"] = {
+        "workload": "128 decode rows (context U[2600,5200]) + 64 prompts of 2600 tokens, page 16",
+        "split": list(step.last_split), "one_stream_ms": one, "two_streams_ms": two,
+        "two_vs_one": two / one, "prefill_tflops_one_stream": pf / (one * 1e-3) / 1e12,
+        "tokens_per_s_one_stream": T / (one * 1e-3), "device_flags": step.read_errors()}
+    del d, step, o
+    torch.cuda.empty_cache()
+    return out
+
+
 # ----------------------------------------------------------------------------- main
 def main():
     ap = argparse.ArgumentParser()
@@ -285,6 +415,7 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-secondary", action="store_true")
+    ap.add_argument("--no-suite", action="store_true")
     args = ap.parse_args()
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
@@ -402,6 +533,11 @@ def main():
             line["secondary"]["decode_frac_of_hbm"] = round(line["secondary"]["decode_hbm_gbs"] / peak_bw, 4)
         except Exception as e:  # keep the headline line even if the secondary run fails
             line["secondary"] = {"error": repr(e)}
+    if not args.no_suite and not args.no_secondary and rank == 0:
+        try:
+            line["suite"] = suite(dev)
+        except Exception as e:
+            line["suite"] = {"error": repr(e)}
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(host_inputs())
     if rank == 0:
