@@ -204,6 +204,19 @@ __device__ __forceinline__ void umma_commit(uint64_t *bar)
                  : "memory");
 }
 
+// One lane of a converged warp, chosen by elect.sync. A tcgen05.mma or commit is
+// a one-thread instruction; issued from a branch on this, with its operands
+// computed by the whole (converged) warp, it issues faster than the tensor pipe
+// executes an M=N=128, K=16 MMA (64 clocks). Issued from a lane-0-only region it
+// costs about 60 clocks of the issuing thread each, so the pipe starves as soon
+// as the thread also waits on barriers.
+__device__ __forceinline__ bool elect_one_sync()
+{
+    uint32_t e;
+    asm volatile("{\n\t.reg .pred p;\n\telect.sync _|p, 0xffffffff;\n\tselp.u32 %0, 1, 0, p;\n\t}" : "=r"(e));
+    return e != 0;
+}
+
 // 32 lanes x 32 consecutive 32-bit columns: thread i gets lane (base lane + i).
 __device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32])
 {

@@ -13,8 +13,9 @@
 //   warp 8       TMA producer: Q tiles once per item, then K_j, V_j into a ring
 //                of shared-memory slots; block_table lookups; zeroes the value
 //                rows past seq_len in the last tile (they may hold anything).
-//   warp 9       tcgen05 issuer (one lane): S_n = Q_n K_j^T into TMEM, then
-//                O_n += P_n V_j with P_n read from TMEM; TMEM alloc/dealloc.
+//   warp 9       tcgen05 issuer (one elected lane per instruction, the warp
+//                converged): S_n = Q_n K_j^T into TMEM, then O_n += P_n V_j with
+//                P_n read from TMEM; TMEM alloc/dealloc.
 //   warps 0..7   softmax, one warpgroup per q head n; thread = query row:
 //                S row from TMEM, causal mask on the diagonal/tail tiles, online
 //                max/sum in fp32 (base-2 exponent, scale folded in), P as bf16
@@ -210,95 +211,109 @@ chunk_attn_kernel(const ChunkParams p, const __grid_constant__ CUtensorMap tm_q,
         }
     } else if (warp == C::kMmaWarp) {
         // ------------------------------------------------------------ MMA issuer
-        if (lane == 0) {
-            constexpr uint32_t idesc_qk = idesc_bf16_f32(128, 128, false);
-            constexpr uint32_t idesc_pv = idesc_bf16_f32(128, D, true);
-            const uint32_t q_addr = smem_u32(smem + C::kQOff);
-            const uint32_t slot_addr = smem_u32(smem + C::kSlotOff);
-            uint32_t q_uses = 0, slot_it = 0, p_uses[2] = {0, 0};
-            auto issue_qk = [&](int n, int slot) {
+        // The whole warp walks the loop; every MMA and commit is issued by one
+        // lane from an elect.sync branch. Waits are polled by all lanes and their
+        // verdicts combined, so the warp stays converged.
+        constexpr uint32_t idesc_qk = idesc_bf16_f32(128, 128, false);
+        constexpr uint32_t idesc_pv = idesc_bf16_f32(128, D, true);
+        const uint32_t q_addr = smem_u32(smem + C::kQOff);
+        const uint32_t slot_addr = smem_u32(smem + C::kSlotOff);
+        uint32_t q_uses = 0, slot_it = 0, p_uses[2] = {0, 0};
+        auto wait = [&](uint64_t *bar, uint32_t parity) -> bool {
+            const bool ok = mbar_wait(bar, parity, abort);
+            return __all_sync(0xffffffffu, ok);
+        };
+        auto aborted = [&]() -> bool { return __any_sync(0xffffffffu, *abort != 0); };
+        auto commit = [&](uint64_t *bar) {
+            if (elect_one_sync())
+                umma_commit(bar);
+        };
+        auto issue_qk = [&](int n, int slot) {
 #pragma unroll
-                for (int kk = 0; kk < D / 16; ++kk) {
-                    const uint32_t koff = (kk >> 2) * C::kHalfBytes + (kk & 3) * 32;
-                    uint64_t a = smem_desc_sw128(q_addr + n * C::kTileBytes + koff, 0, 1024);
-                    uint64_t b = smem_desc_sw128(slot_addr + slot * C::kTileBytes + koff, 0, 1024);
+            for (int kk = 0; kk < D / 16; ++kk) {
+                const uint32_t koff = (kk >> 2) * C::kHalfBytes + (kk & 3) * 32;
+                const uint64_t a = smem_desc_sw128(q_addr + n * C::kTileBytes + koff, 0, 1024);
+                const uint64_t b = smem_desc_sw128(slot_addr + slot * C::kTileBytes + koff, 0, 1024);
+                if (elect_one_sync())
                     umma_ss(tmem + C::s_col(n), a, b, idesc_qk, kk > 0);
-                }
-            };
-            auto issue_pv = [&](int n, int slot, bool acc) {
-#pragma unroll
-                for (int kk = 0; kk < 128 / 16; ++kk) {
-                    uint64_t b = smem_desc_sw128(slot_addr + slot * C::kTileBytes + kk * 16 * 128,
-                                                 C::kHalfBytes, 1024);
-                    umma_ts(tmem + C::o_col(n), tmem + C::s_col(n) + kk * 8, b, idesc_pv, (acc || kk > 0));
-                }
-            };
-            auto wait_slot = [&](int &slot) -> bool {
-                slot = slot_it % C::kSlots;
-                bool ok = mbar_wait(&bars->slot_full[slot], (slot_it / C::kSlots) & 1, abort);
-                ++slot_it;
-                tc_fence_after_sync();
-                return ok;
-            };
-            for (int it = it_begin; it < it_end && !*abort; ++it) {
-                const PrefillItem w = p.pitems[it];
-                const int n = w.kt1 - w.kt0;
-                if (!mbar_wait(&bars->q_full, q_uses & 1, abort))
-                    break;
-                ++q_uses;
-                tc_fence_after_sync();
-                int sK, sV;
-                if (!wait_slot(sK))
-                    break;
-                for (int qn = 0; qn < NQ; ++qn) {
-                    issue_qk(qn, sK);
-                    umma_commit(&bars->s_full[qn]);
-                }
-                umma_commit(&bars->slot_empty[sK]);
-                if (n == 1)
-                    umma_commit(&bars->q_empty);
-                bool ok = true;
-                for (int t = 0; t < n && ok; ++t) {
-                    if (!(ok = wait_slot(sV)))
-                        break;
-                    if (!(ok = mbar_wait(&bars->p_full[0], p_uses[0] & 1, abort)))
-                        break;
-                    ++p_uses[0];
-                    tc_fence_after_sync();
-                    issue_pv(0, sV, t > 0);
-                    umma_commit(&bars->o_done[0]);
-                    const bool more = t + 1 < n;
-                    if (more) {
-                        if (!(ok = wait_slot(sK)))
-                            break;
-                        issue_qk(0, sK);
-                        umma_commit(&bars->s_full[0]);
-                    }
-                    if (NQ == 2) {
-                        if (!(ok = mbar_wait(&bars->p_full[1], p_uses[1] & 1, abort)))
-                            break;
-                        ++p_uses[1];
-                        tc_fence_after_sync();
-                        issue_pv(1, sV, t > 0);
-                        umma_commit(&bars->o_done[1]);
-                    }
-                    umma_commit(&bars->slot_empty[sV]);
-                    if (more) {
-                        if (NQ == 2) {
-                            issue_qk(1, sK);
-                            umma_commit(&bars->s_full[1]);
-                        }
-                        umma_commit(&bars->slot_empty[sK]);
-                        if (t + 2 == n)
-                            umma_commit(&bars->q_empty);
-                    }
-                }
-                if (!ok)
-                    break;
             }
-            if (*abort) {
-                // let every MMA issued so far finish before TMEM is released
-                umma_commit(&bars->drain);
+        };
+        auto issue_pv = [&](int n, int slot, bool acc) {
+#pragma unroll
+            for (int kk = 0; kk < 128 / 16; ++kk) {
+                const uint64_t b = smem_desc_sw128(slot_addr + slot * C::kTileBytes + kk * 16 * 128,
+                                                   C::kHalfBytes, 1024);
+                if (elect_one_sync())
+                    umma_ts(tmem + C::o_col(n), tmem + C::s_col(n) + kk * 8, b, idesc_pv, (acc || kk > 0));
+            }
+        };
+        auto wait_slot = [&](int &slot) -> bool {
+            slot = slot_it % C::kSlots;
+            const bool ok = wait(&bars->slot_full[slot], (slot_it / C::kSlots) & 1);
+            ++slot_it;
+            tc_fence_after_sync();
+            return ok;
+        };
+        for (int it = it_begin; it < it_end && !aborted(); ++it) {
+            const PrefillItem w = p.pitems[it];
+            const int n = w.kt1 - w.kt0;
+            if (!wait(&bars->q_full, q_uses & 1))
+                break;
+            ++q_uses;
+            tc_fence_after_sync();
+            int sK, sV;
+            if (!wait_slot(sK))
+                break;
+            for (int qn = 0; qn < NQ; ++qn) {
+                issue_qk(qn, sK);
+                commit(&bars->s_full[qn]);
+            }
+            commit(&bars->slot_empty[sK]);
+            if (n == 1)
+                commit(&bars->q_empty);
+            bool ok = true;
+            for (int t = 0; t < n && ok; ++t) {
+                if (!(ok = wait_slot(sV)))
+                    break;
+                if (!(ok = wait(&bars->p_full[0], p_uses[0] & 1)))
+                    break;
+                ++p_uses[0];
+                tc_fence_after_sync();
+                issue_pv(0, sV, t > 0);
+                commit(&bars->o_done[0]);
+                const bool more = t + 1 < n;
+                if (more) {
+                    if (!(ok = wait_slot(sK)))
+                        break;
+                    issue_qk(0, sK);
+                    commit(&bars->s_full[0]);
+                }
+                if (NQ == 2) {
+                    if (!(ok = wait(&bars->p_full[1], p_uses[1] & 1)))
+                        break;
+                    ++p_uses[1];
+                    tc_fence_after_sync();
+                    issue_pv(1, sV, t > 0);
+                    commit(&bars->o_done[1]);
+                }
+                commit(&bars->slot_empty[sV]);
+                if (more) {
+                    if (NQ == 2) {
+                        issue_qk(1, sK);
+                        commit(&bars->s_full[1]);
+                    }
+                    commit(&bars->slot_empty[sK]);
+                    if (t + 2 == n)
+                        commit(&bars->q_empty);
+                }
+            }
+            if (!ok)
+                break;
+        }
+        if (aborted()) {
+            // let every MMA issued so far finish before TMEM is released
+            commit(&bars->drain);
+            if (lane == 0) {
                 uint64_t t0 = global_timer_ns();
                 while (!mbar_try_wait(&bars->drain, 0) && global_timer_ns() - t0 < 100000000ull) {
                 }
