@@ -302,7 +302,11 @@ int cpp_chunked_prefill_attn_events(const void *q, const void *k_cache, const vo
     static_cast<AttnCommon &>(cp) = ac;
     cp.pitems = pitems;
     cp.run_first = run_first;
-    const int grid_c = pp.chunk_grid;   // one stream-K run per CTA
+    // A single request is either one decode row or one prefill: the other
+    // kernel would find no items, so it is not launched.
+    const bool single_prefill = num_reqs == 1 && num_tokens >= 2;
+    const bool single_decode = num_reqs == 1 && num_tokens == 1;
+    const int grid_c = single_decode ? 0 : pp.chunk_grid;   // one stream-K run per CTA
     if (grid_c > 0 && launch_chunk_attn(cp, tq, tk, tv, head_dim, nq, grid_c, s) != cudaSuccess)
         return CPSA_ERR_CUDA;
     mark(2, s);
@@ -313,7 +317,7 @@ int cpp_chunked_prefill_attn_events(const void *q, const void *k_cache, const vo
     dp.q = q;
     dp.k_cache_ptr = k_cache;
     dp.v_cache_ptr = v_cache;
-    int grid_d = (int)(L.max_ditems < sms ? L.max_ditems : sms);
+    int grid_d = single_prefill ? 0 : (int)(L.max_ditems < sms ? L.max_ditems : sms);
     if (grid_d > 0 && launch_decode_attn(dp, tkd, tvd, head_dim, grid_d, s) != cudaSuccess)
         return CPSA_ERR_CUDA;
     mark(3, s);

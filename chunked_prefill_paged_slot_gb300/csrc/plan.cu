@@ -12,7 +12,8 @@
 // run length and whether the partials fit the workspace (if not, nothing is
 // split). Pass 2 walks the requests in chunks of 1024: one block scan gives each
 // request its token and tile offsets, a second gives its list offsets, and each
-// thread then writes its own request's entries.
+// thread then writes its own request's entries. Batches of at most 32 requests
+// take a one-warp kernel that builds the same lists without block barriers.
 #include "common.cuh"
 #include "plan.cuh"
 
@@ -140,8 +141,12 @@ __device__ Counts request_work(const PlanParams &p, int r, const Req &rq, int ti
                 const int kvh = j / pairs, hp = j % pairs;
                 const int pbase = split ? off.prows + c.prows + e_pr : -1;
                 const int pi = off.pieces + c.pieces + e_np;
+                // with cuts, every run starts a piece: the piece starting at tile
+                // c * run is the first of CTA c's run
                 if (!split) {
                     p.pitems[pi] = PrefillItem{r, i0, kvh | (hp << 16), 0, nkv, (1 << 16), -1, u0 / run};
+                    if (cut && u0 % run == 0)
+                        p.run_first[u0 / run] = pi;
                 } else {
                     int x = u0;
                     for (int pc = 0; pc < np; ++pc) {
@@ -149,6 +154,8 @@ __device__ Counts request_work(const PlanParams &p, int r, const Req &rq, int ti
                         const int end = min(u1, (owner + 1) * run);
                         p.pitems[pi + pc] =
                             PrefillItem{r, i0, kvh | (hp << 16), x - u0, end - u0, pc | (np << 16), pbase, owner};
+                        if (x == owner * run)
+                            p.run_first[owner] = pi + pc;
                         x = end;
                     }
                     p.citems[off.citems + c.citems + e_ci] =
@@ -164,6 +171,50 @@ __device__ Counts request_work(const PlanParams &p, int r, const Req &rq, int ti
         tile_run += upq * nkv;
     }
     return c;
+}
+
+// Stream-K run length; cuts inside units only when splitting is allowed and the
+// partials' bound fits the workspace (else nothing is split and the flag is set).
+struct SplitChoice {
+    int run, max_splits;
+    bool split_prefill, clamped;
+};
+
+__device__ SplitChoice choose_split(const PlanParams &p, long long tiles, long long dprows)
+{
+    const int grid = max(1, p.chunk_grid);
+    SplitChoice c;
+    c.run = max((int)((tiles + grid - 1) / grid), kMinRunTiles);
+    c.max_splits = p.max_splits;
+    c.split_prefill = p.max_splits > 1;
+    c.clamped = false;
+    const long long pbound = (long long)2 * grid * kTileM * p.nq;
+    if (p.max_splits > 1 && pbound + dprows > p.prow_capacity) {
+        c.max_splits = 1;
+        c.split_prefill = false;
+        c.clamped = true;
+    }
+    return c;
+}
+
+// run_first[c] = first piece whose owner is >= c (pieces are sorted by owner);
+// threads tid, tid + nthreads, ... of the caller share the entries. With cuts the
+// emission already wrote the entries of runs holding tiles (runs [0, ceil(W /
+// run))), and only the rest are set here; without cuts they are read back from
+// the pieces' owners.
+__device__ void fill_run_first(const PlanParams &p, int n_pieces, int grid, bool cut, long long tiles, int run,
+                               int tid, int nthreads)
+{
+    if (cut) {
+        const int first_empty = (int)((tiles + run - 1) / run);
+        for (int c = first_empty + tid; c <= grid; c += nthreads) p.run_first[c] = n_pieces;
+        return;
+    }
+    for (int i = tid; i <= n_pieces; i += nthreads) {
+        const int lo = i == 0 ? 0 : p.pitems[i - 1].owner + 1;
+        const int hi = i == n_pieces ? grid : p.pitems[i].owner;
+        for (int c = lo; c <= hi; ++c) p.run_first[c] = i;
+    }
 }
 
 // Block-wide exclusive scan of N ints; returns the totals.
@@ -246,19 +297,12 @@ __global__ void __launch_bounds__(kPlanThreads, 1) plan_kernel(PlanParams p)
         for (int c = threadIdx.x; c <= p.chunk_grid; c += kPlanThreads) p.run_first[c] = 0;
         return;
     }
-    // stream-K run length; cuts inside units only when splitting is allowed and
-    // the partials' bound fits the workspace
     const int grid = max(1, p.chunk_grid);
-    int run = (int)((tiles + grid - 1) / grid);
-    run = max(run, kMinRunTiles);
-    const long long pbound = (long long)2 * grid * kTileM * p.nq;
-    int max_splits = p.max_splits;
-    bool split_prefill = max_splits > 1;
-    if (max_splits > 1 && pbound + dprows > p.prow_capacity) {
-        if (threadIdx.x == 0) set_dev_error(p.dev_err, CPSA_DEV_SPLITS_CLAMPED);
-        max_splits = 1;
-        split_prefill = false;
-    }
+    const SplitChoice sc = choose_split(p, tiles, dprows);
+    const int run = sc.run, max_splits = sc.max_splits;
+    const bool split_prefill = sc.split_prefill;
+    if (sc.clamped && threadIdx.x == 0)
+        set_dev_error(p.dev_err, CPSA_DEV_SPLITS_CLAMPED);
 
     // ---- pass 2: offsets and lists, 1024 requests at a time
     __shared__ int s_qoff[kPlanThreads], s_toff[kPlanThreads];
@@ -321,14 +365,9 @@ __global__ void __launch_bounds__(kPlanThreads, 1) plan_kernel(PlanParams p)
         }
         __syncthreads();
     }
-    // run_first[c] = first piece whose owner is >= c (pieces are sorted by owner)
     __syncthreads();   // this block's piece writes are visible to the whole block
     const int n_pieces = (int)min((int64_t)carry_b[0], p.max_pitems);
-    for (int i = threadIdx.x; i <= n_pieces; i += kPlanThreads) {
-        const int lo = i == 0 ? 0 : p.pitems[i - 1].owner + 1;
-        const int hi = i == n_pieces ? grid : p.pitems[i].owner;
-        for (int c = lo; c <= hi; ++c) p.run_first[c] = i;
-    }
+    fill_run_first(p, n_pieces, grid, split_prefill, tiles, run, threadIdx.x, kPlanThreads);
     if (threadIdx.x == 0) {
         p.cu_q[p.num_reqs] = carry_a[0];
         p.counts[kCntPrefill] = (int)min((int64_t)carry_b[0], p.max_pitems);
@@ -341,11 +380,88 @@ __global__ void __launch_bounds__(kPlanThreads, 1) plan_kernel(PlanParams p)
     }
 }
 
+// The same lists for a batch of at most 32 requests, built by one warp: lane r
+// holds request r, warp scans give the token and tile offsets, and the warp then
+// walks the requests in order, so every request's list offsets are the running
+// totals of the ones before it (one pass, no block-wide barriers).
+__global__ void __launch_bounds__(32, 1) plan_small_kernel(PlanParams p)
+{
+    const int lane = threadIdx.x;
+    const bool mine = lane < p.num_reqs;
+    Req rq{false, 0, 0, 0};
+    if (mine)
+        rq = load_req(p, lane);
+    const int tok = mine && rq.q > 0 ? rq.q : 0;   // invalid requests still occupy their rows
+    const int tiles = mine ? prefill_tiles(p, rq) : 0;
+    int dprows = 0;
+    if (mine && rq.valid && rq.q == 1) {
+        const int ns = decode_splits(rq, p.max_splits);
+        if (ns > 1) dprows = p.Hq * ns;
+    }
+    // totals in 64 bits first: the 32-bit scans below are only used once they fit
+    long long tok_sum = tok, tile_sum = tiles, dprow_sum = dprows;
+    for (int o = 16; o > 0; o >>= 1) {
+        tok_sum += __shfl_xor_sync(0xffffffffu, tok_sum, o);
+        tile_sum += __shfl_xor_sync(0xffffffffu, tile_sum, o);
+        dprow_sum += __shfl_xor_sync(0xffffffffu, dprow_sum, o);
+    }
+    const int grid = max(1, p.chunk_grid);
+    if (tok_sum != p.num_tokens) {
+        if (lane == 0) set_dev_error(p.dev_err, CPSA_DEV_TOKENS_MISMATCH);
+        if (lane < kCntSlots) p.counts[lane] = 0;
+        for (int c = lane; c <= p.chunk_grid; c += 32) p.run_first[c] = 0;
+        return;
+    }
+    if (mine && !rq.valid)
+        set_dev_error(p.dev_err, (rq.q < 0 || rq.s < rq.q) ? CPSA_DEV_SEQ_LT_QUERY : CPSA_DEV_SEQ_GT_TABLE);
+    int tok_total, tile_total;
+    const int tok_off = warp_excl_scan(tok, lane, tok_total);
+    const int tile_off = warp_excl_scan(tiles, lane, tile_total);
+    if (mine)
+        p.cu_q[lane] = tok_off;
+    const SplitChoice sc = choose_split(p, tile_sum, dprow_sum);
+    if (sc.clamped && lane == 0)
+        set_dev_error(p.dev_err, CPSA_DEV_SPLITS_CLAMPED);
+    Counts off{0, 0, 0, 0, 0};
+    for (int r = 0; r < p.num_reqs; ++r) {
+        Req rr;
+        rr.valid = __shfl_sync(0xffffffffu, rq.valid ? 1 : 0, r) != 0;
+        rr.q = __shfl_sync(0xffffffffu, rq.q, r);
+        rr.s = __shfl_sync(0xffffffffu, rq.s, r);
+        rr.hist = __shfl_sync(0xffffffffu, rq.hist, r);
+        const int qoff = __shfl_sync(0xffffffffu, tok_off, r);
+        const int toff = __shfl_sync(0xffffffffu, tile_off, r);
+        const Counts c = request_work(p, r, rr, toff, sc.run, sc.split_prefill, sc.max_splits, true, qoff, off, lane);
+        off.pieces += c.pieces;
+        off.prows += c.prows;
+        off.cunits += c.cunits;
+        off.citems += c.citems;
+        off.ditems += c.ditems;
+    }
+    __syncwarp();   // the warp's piece writes are visible to all its lanes
+    const int n_pieces = (int)min((int64_t)off.pieces, p.max_pitems);
+    fill_run_first(p, n_pieces, grid, sc.split_prefill, tile_sum, sc.run, lane, 32);
+    if (lane == 0) {
+        p.cu_q[p.num_reqs] = tok_total;
+        p.counts[kCntPrefill] = n_pieces;
+        p.counts[kCntCombine] = (int)min((int64_t)off.citems, p.max_citems);
+        p.counts[kCntPartialRows] = off.prows;
+        p.counts[kCntCombineUnits] = off.cunits;
+        p.counts[kCntDecode] = (int)min((int64_t)off.ditems, p.max_ditems);
+        p.counts[kCntRunTiles] = sc.run;
+    } else if (lane > kCntRunTiles && lane < kCntSlots) {
+        p.counts[lane] = 0;
+    }
+}
+
 }  // namespace
 
 void launch_plan(const PlanParams &p, cudaStream_t s)
 {
-    plan_kernel<<<1, kPlanThreads, 0, s>>>(p);
+    if (p.num_reqs <= 32)
+        plan_small_kernel<<<1, 32, 0, s>>>(p);
+    else
+        plan_kernel<<<1, kPlanThreads, 0, s>>>(p);
 }
 
 }  // namespace cpsa

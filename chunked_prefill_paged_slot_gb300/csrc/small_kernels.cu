@@ -51,90 +51,137 @@ __global__ void __launch_bounds__(256) kv_write_kernel(const uint4 *__restrict__
 // Combine of split rows: O = sum_s 2^(m_s - M) O_s / sum_s 2^(m_s - M) l_s,
 // M = max_s m_s (m in base-2 units). Persistent: the (row, q head) units of all
 // combine items are numbered consecutively (CombineItem::u0; an item covers
-// nrows rows x nh heads from h0). Each CTA stages the items' first units in
-// shared memory and its warps take units in turn, one warp per unit, lane l
-// owning output columns [4l, 4l+4) (D = 128) or [2l, 2l+2) (D = 64); the
-// partial O loads of a unit are issued before its weights are formed.
+// nrows rows x nh heads from h0). Each CTA stages the items (all of them when
+// they fit, else their first units) in shared memory; each warp takes two
+// consecutive units at a time, lane l owning output columns [4l, 4l+4)
+// (D = 128) or [2l, 2l+2) (D = 64). Both units' (m, l) and first partial O
+// loads are in flight before any weight is formed: the kernel is bound by the
+// latency of those loads, not by bandwidth.
 // ---------------------------------------------------------------------------
 constexpr int kCombineThreads = 256;
-constexpr int kCombineSmemItems = 4096;
+constexpr int kCombineSmemItems = 4096;    // first units staged for up to this many items
+constexpr int kCombineFullItems = 512;     // whole items staged for up to this many
 constexpr int kCombineMaxSplits = 32;
+constexpr int kCombineRound = 4;           // partial O rows loaded per unit per round
+constexpr int kCombineUnits = 2;           // units per warp in flight
 
 template <int D>
-__global__ void __launch_bounds__(kCombineThreads) combine_kernel(const CombineParams p)
+__global__ void __launch_bounds__(kCombineThreads, 4) combine_kernel(const CombineParams p)
 {
     __shared__ int s_u0[kCombineSmemItems];
+    __shared__ CombineItem s_item[kCombineFullItems];
     const int n_items = p.counts[kCntCombine];
     const int total = p.counts[kCntCombineUnits];
     if (n_items == 0 || total == 0)
         return;
     const bool staged = n_items <= kCombineSmemItems;
-    if (staged) {
+    const bool full = n_items <= kCombineFullItems;
+    if (full) {
+        for (int i = threadIdx.x; i < n_items; i += kCombineThreads) {
+            s_item[i] = p.citems[i];
+            s_u0[i] = s_item[i].u0;
+        }
+    } else if (staged) {
         for (int i = threadIdx.x; i < n_items; i += kCombineThreads) s_u0[i] = p.citems[i].u0;
-        __syncthreads();
     }
+    __syncthreads();
     const int lane = threadIdx.x & 31;
     const int warps = gridDim.x * (kCombineThreads / 32);
     constexpr int PER_LANE = D / 32;
     const int Hq = p.num_q_heads;
-    for (int u = blockIdx.x * (kCombineThreads / 32) + (threadIdx.x >> 5); u < total; u += warps) {
-        // last item with u0 <= u
+    auto find = [&](int u) -> CombineItem {   // the last item with u0 <= u
         int lo = 0, hi = n_items - 1;
         while (lo < hi) {
             const int mid = (lo + hi + 1) >> 1;
             const int v = staged ? s_u0[mid] : p.citems[mid].u0;
             if (v <= u) lo = mid; else hi = mid - 1;
         }
-        const CombineItem c = p.citems[lo];
-        const int local = u - c.u0;
-        const int row = local / c.nh, h = c.h0 + local % c.nh;
-        const int64_t pr0 = (int64_t)c.pbase + (int64_t)local * c.nsplit;
-        // partial O first (independent of the weights), then (m, l)
-        float o[kCombineMaxSplits / 4][PER_LANE];
-        float acc[PER_LANE];
+        return full ? s_item[lo] : p.citems[lo];
+    };
+    auto load_o = [&](float (&dst)[PER_LANE], int64_t row) {
+        const float *src = p.part_o + row * D + lane * PER_LANE;
+        if (PER_LANE == 4) {
+            const float4 x = __ldcs(reinterpret_cast<const float4 *>(src));
+            dst[0] = x.x; dst[1 % PER_LANE] = x.y; dst[2 % PER_LANE] = x.z; dst[3 % PER_LANE] = x.w;
+        } else {
+            const float2 x = __ldcs(reinterpret_cast<const float2 *>(src));
+            dst[0] = x.x; dst[1 % PER_LANE] = x.y;
+        }
+    };
+    constexpr int NU = kCombineUnits;
+    for (int ub = (blockIdx.x * (kCombineThreads / 32) + (threadIdx.x >> 5)) * NU; ub < total; ub += warps * NU) {
+        int64_t pr0[NU];   // first partial row of the unit
+        int trow[NU], head[NU], ns[NU];
+        bool live[NU];
+        float2 ml[NU];
+        float o[NU][kCombineRound][PER_LANE];
 #pragma unroll
-        for (int e = 0; e < PER_LANE; ++e) acc[e] = 0.f;
-        const float2 ml = lane < c.nsplit ? __ldcs(reinterpret_cast<const float2 *>(p.part_ml) + pr0 + lane)
-                                          : make_float2(-INFINITY, 0.f);
-        float M = ml.x;
-        for (int s0 = 0; s0 < c.nsplit; s0 += kCombineMaxSplits / 4) {
-            const int cnt = min(kCombineMaxSplits / 4, c.nsplit - s0);
+        for (int k = 0; k < NU; ++k) {
+            live[k] = ub + k < total;
+            pr0[k] = 0;
+            trow[k] = head[k] = ns[k] = 0;
+            if (live[k]) {
+                const CombineItem c = find(ub + k);
+                const int local = ub + k - c.u0;
+                pr0[k] = (int64_t)c.pbase + (int64_t)local * c.nsplit;
+                trow[k] = c.t0 + local / c.nh;
+                head[k] = c.h0 + local % c.nh;
+                ns[k] = c.nsplit;
+            }
+        }
+        // every load of the first round, for all units, before any arithmetic
 #pragma unroll
-            for (int j = 0; j < kCombineMaxSplits / 4; ++j) {
-                if (j < cnt) {
-                    const float *src = p.part_o + (pr0 + s0 + j) * D + lane * PER_LANE;
-                    if (PER_LANE == 4) {
-                        const float4 x = __ldcs(reinterpret_cast<const float4 *>(src));
-                        o[j][0] = x.x; o[j][1] = x.y; o[j][2 % PER_LANE] = x.z; o[j][3 % PER_LANE] = x.w;
-                    } else {
-                        const float2 x = __ldcs(reinterpret_cast<const float2 *>(src));
-                        o[j][0] = x.x; o[j][1 % PER_LANE] = x.y;
+        for (int k = 0; k < NU; ++k) {
+            ml[k] = lane < ns[k] ? __ldcs(reinterpret_cast<const float2 *>(p.part_ml) + pr0[k] + lane)
+                                 : make_float2(-INFINITY, 0.f);
+#pragma unroll
+            for (int j = 0; j < kCombineRound; ++j)
+                if (j < ns[k])
+                    load_o(o[k][j], pr0[k] + j);
+        }
+#pragma unroll
+        for (int k = 0; k < NU; ++k) {
+            if (!live[k])
+                continue;
+            float M = ml[k].x;
+            for (int off = 16; off > 0; off >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, off));
+            const float Mref = M == -INFINITY ? 0.f : M;
+            const float f = ex2_approx(ml[k].x - Mref);   // lane s: weight of split s
+            float L = f * ml[k].y;
+            for (int off = 16; off > 0; off >>= 1) L += __shfl_xor_sync(0xffffffffu, L, off);
+            float acc[PER_LANE];
+#pragma unroll
+            for (int e = 0; e < PER_LANE; ++e) acc[e] = 0.f;
+#pragma unroll
+            for (int j = 0; j < kCombineRound; ++j) {
+                if (j < ns[k]) {
+                    const float fs = __shfl_sync(0xffffffffu, f, j);
+#pragma unroll
+                    for (int e = 0; e < PER_LANE; ++e) acc[e] += fs * o[k][j][e];
+                }
+            }
+            // more splits than one round (long decode rows): further rounds
+            for (int s0 = kCombineRound; s0 < ns[k]; s0 += kCombineRound) {
+#pragma unroll
+                for (int j = 0; j < kCombineRound; ++j)
+                    if (s0 + j < ns[k])
+                        load_o(o[k][j], pr0[k] + s0 + j);
+#pragma unroll
+                for (int j = 0; j < kCombineRound; ++j) {
+                    if (s0 + j < ns[k]) {
+                        const float fs = __shfl_sync(0xffffffffu, f, s0 + j);
+#pragma unroll
+                        for (int e = 0; e < PER_LANE; ++e) acc[e] += fs * o[k][j][e];
                     }
                 }
             }
-            if (s0 == 0) {
-                for (int off = 16; off > 0; off >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, off));
-            }
-            const float Mref = M == -INFINITY ? 0.f : M;
-            const float f = ex2_approx(ml.x - Mref);
+            const float inv = L > 0.f ? 1.f / L : 0.f;
+            __nv_bfloat16 *dst = reinterpret_cast<__nv_bfloat16 *>(p.out) +
+                                 ((int64_t)trow[k] * Hq + head[k]) * D + lane * PER_LANE;
 #pragma unroll
-            for (int j = 0; j < kCombineMaxSplits / 4; ++j) {
-                if (j < cnt) {
-                    const float fs = __shfl_sync(0xffffffffu, f, s0 + j);
-#pragma unroll
-                    for (int e = 0; e < PER_LANE; ++e) acc[e] += fs * o[j][e];
-                }
-            }
+            for (int e = 0; e < PER_LANE; e += 2)
+                *reinterpret_cast<uint32_t *>(dst + e) = pack_bf16x2(acc[e] * inv, acc[e + 1] * inv);
         }
-        const float Mref = M == -INFINITY ? 0.f : M;
-        float L = ex2_approx(ml.x - Mref) * ml.y;
-        for (int off = 16; off > 0; off >>= 1) L += __shfl_xor_sync(0xffffffffu, L, off);
-        const float inv = L > 0.f ? 1.f / L : 0.f;
-        __nv_bfloat16 *dst = reinterpret_cast<__nv_bfloat16 *>(p.out) +
-                             ((int64_t)(c.t0 + row) * Hq + h) * D + lane * PER_LANE;
-#pragma unroll
-        for (int e = 0; e < PER_LANE; e += 2)
-            *reinterpret_cast<uint32_t *>(dst + e) = pack_bf16x2(acc[e] * inv, acc[e + 1] * inv);
     }
 }
 
