@@ -46,6 +46,38 @@ def chunk_flops(h, c, hq=HQ, d=D):
 STEP_FLOPS = sum(chunk_flops(i * CHUNK, CHUNK) for i in range(N_CHUNKS))
 
 
+TRAFFIC_PROFILE = os.path.join(ROOT, "profiles", "chunk_attn_traffic_llama_chunked_prefill.md")
+KERNEL_SOURCES = [os.path.join(ROOT, "chunked_prefill_paged_slot_gb300", "csrc", x)
+                  for x in ("prefill_tc.cu", "common.cuh", "plan.cu", "plan.cuh")]
+
+
+def kernel_source_digest():
+    """sha256 over the chunk kernel's sources (the kernel and the plan that feeds it)."""
+    import hashlib
+    h = hashlib.sha256()
+    for p in KERNEL_SOURCES:
+        with open(p, "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()
+
+
+def load_traffic():
+    """DRAM bytes per chunk-kernel launch from the committed ncu summary, or None when
+    the kernel's sources changed since those counters were taken."""
+    try:
+        fields = {}
+        with open(TRAFFIC_PROFILE) as f:
+            for ln in f:
+                if ":" in ln and ln.strip().startswith("- "):
+                    k, v = ln.strip()[2:].split(":", 1)
+                    fields[k.strip()] = v.strip().strip("`")
+        if fields.get("kernel_source_sha256") != kernel_source_digest():
+            return None
+        return float(fields["dram_bytes_per_launch"])
+    except Exception:
+        return None
+
+
 def load_peaks():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     try:
@@ -66,10 +98,12 @@ class ClockSampler:
     def __init__(self, gpu_id: str | None):
         self.gpu_id = gpu_id
         self.proc = None
-        self.lines = []
+        self.lines = []          # (host time, csv line)
+        self.window = (0.0, 0.0)
 
     def start(self):
-        cmd = ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits", "-lms", "200"]
+        """Start sampling every 20 ms and wait (up to 5 s) until samples arrive."""
+        cmd = ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits", "-lms", "20"]
         if self.gpu_id:
             cmd += ["-i", self.gpu_id]
         try:
@@ -78,10 +112,18 @@ class ClockSampler:
             self.thread.start()
         except Exception:
             self.proc = None
+            return
+        t0 = time.perf_counter()
+        while not self.lines and time.perf_counter() - t0 < 5.0:
+            time.sleep(0.01)
 
     def _read(self):
         for line in self.proc.stdout:
-            self.lines.append(line.strip())
+            self.lines.append((time.perf_counter(), line.strip()))
+
+    def mark(self, begin: float, end: float):
+        """The timed region: only samples taken inside it are reported."""
+        self.window = (begin, end)
 
     def stop(self):
         if self.proc is None:
@@ -94,7 +136,10 @@ class ClockSampler:
         self.thread.join(timeout=2)
         sm, mx, reasons = [], [], set()
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        for ln in self.lines:
+        b, e = self.window
+        for ts, ln in self.lines:
+            if not (b <= ts <= e):
+                continue
             parts = [x.strip() for x in ln.split(",")]
             if len(parts) < 8:
                 continue
@@ -234,12 +279,12 @@ def cpu_baseline(inputs, budget_s=12.0):
 
 
 # ----------------------------------------------------------------------------- secondary: decode bandwidth
-def decode_bandwidth(dev, reps=5):
-    """Decode-row HBM GB/s on the Sarathi mixed step (1536 decode rows + one 512 chunk at h=8192)."""
+def decode_bandwidth(dev, reps=5, n_decode=1536):
+    """Decode-row HBM GB/s on the Sarathi mixed step (n_decode decode rows + one 512 chunk at h=8192)."""
     import torch
     import chunked_prefill_paged_slot_gb300 as cpsa
     import workloads as W
-    spec = W.spec_sarathi_mixed()
+    spec = W.spec_sarathi_mixed(n_decode=n_decode)
     d = W.device_batch(spec, device=dev)
     B, T = len(spec.qlen), sum(spec.qlen)
     ws = torch.empty(cpsa.cpp_attn_workspace_bytes(B, T, HQ, HKV, D, 8), dtype=torch.uint8, device=dev)
@@ -263,8 +308,8 @@ def decode_bandwidth(dev, reps=5):
     ctx = np.array(spec.seq[:n_dec], dtype=np.float64)
     dec_bytes = float(ctx.sum()) * HKV * D * 2 * 2 + n_dec * HQ * D * 2 * 2
     chunk_f = chunk_flops(spec.hist[-1], spec.qlen[-1])
-    res = {"workload": "sarathi mixed step: 1536 decode rows (context U[1024,8192]) + one 512-token chunk at "
-                       "h=8192, 32/8 heads, d128, page 16, L2 flushed",
+    res = {"workload": f"sarathi mixed step: {n_decode} decode rows (context U[1024,8192]) + one 512-token chunk "
+                       "at h=8192, 32/8 heads, d128, page 16, L2 flushed",
            "decode_kernel_ms": float(np.median(dec_ms)),
            "decode_hbm_gbs": dec_bytes / (np.median(dec_ms) * 1e-3) / 1e9,
            "decode_bytes": dec_bytes,
@@ -410,13 +455,22 @@ def suite(dev):
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--steps", type=int, default=30)
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-secondary", action="store_true")
     ap.add_argument("--no-suite", action="store_true")
+    ap.add_argument("--profile-decode", action="store_true",
+                    help="only the mixed decode step with 128 decode rows (about 2.5 GB of cache), "
+                         "a small case for ncu captures of the decode kernel")
     args = ap.parse_args()
+    if args.profile_decode:
+        import torch
+        dev = torch.device("cuda", 0)
+        torch.cuda.set_device(dev)
+        print(json.dumps(decode_bandwidth(dev, reps=3, n_decode=128)), flush=True)
+        return 0
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
     local = int(os.environ.get("LOCAL_RANK", "0"))
@@ -469,7 +523,9 @@ def main():
         kernel_ms.append(wl.chunk_kernel_ms())
     torch.cuda.synchronize()
     if dist: dist.barrier()
-    wall = time.perf_counter() - t_wall
+    t_end = time.perf_counter()
+    wall = t_end - t_wall
+    clocks.mark(t_wall, t_end)
     clk = clocks.stop()
     step_ms = [ev0[s].elapsed_time(ev1[s]) for s in range(args.steps)]
     total_ms = float(sum(step_ms))
@@ -504,12 +560,14 @@ def main():
     per_launch_flops = STEP_FLOPS / N_CHUNKS
     achieved = per_launch_flops / (per_launch_ms * 1e-3) / 1e12
     roofline = {"bound": "tensor", "achieved": round(achieved, 2), "peak": peak_tf, "unit": "TFLOP/s",
-                "frac": round(achieved / peak_tf, 4), "traffic": None,
+                "frac": round(achieved / peak_tf, 4), "traffic": load_traffic(),
                 "kernel": "chunk_attn_kernel<128,2>", "peak_source": f"{peak_src} bf16 dense (burst)",
                 "per_launch_flops": per_launch_flops, "per_launch_ms": round(per_launch_ms, 4),
                 "last_chunk_ms": round(float(km[:, -1].mean()), 4),
                 "last_chunk_tflops": round(chunk_flops((N_CHUNKS - 1) * CHUNK, CHUNK) / (km[:, -1].mean() * 1e-3) / 1e12, 2)}
-    launches = args.steps * N_CHUNKS * 6
+    # per chunk: split, KV write, plan, chunk attention, combine (a single prefill
+    # request launches no decode kernel)
+    launches = args.steps * N_CHUNKS * 5
 
     line = {"metric": METRIC, "value": round(value, 3), "unit": "TFLOP/s", "n_gpus": world,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_per_step, 4),

@@ -119,9 +119,14 @@ size_t cpp_attn_workspace_min_bytes(int num_reqs, int64_t num_tokens, int num_q_
  * kernel; q_r = 0 contributes nothing. Arithmetic: bf16 inputs, fp32
  * accumulation and softmax, probabilities rounded to bf16 before P.V.
  *
- * max_kv_splits (>= 1) caps the number of KV splits of one row; the split count
- * of a row depends only on its own (query_len, seq_len) and max_kv_splits, so a
- * request's output does not depend on the rest of the batch.
+ * max_kv_splits (>= 1) caps the number of KV splits of a decode row; that count
+ * depends only on the row's own seq_len and max_kv_splits. Prefill rows are split
+ * stream-K style: the KV tiles of all prefill units of the batch (128 query rows
+ * x kv head x q-head pair) are laid end to end and cut into equal runs, one per
+ * CTA of the chunk kernel, and a unit cut by a run boundary is merged from fp32
+ * partial results. Where the cuts fall depends on the whole batch, so a prefill
+ * row's last-bit rounding (not its value) can depend on the other requests.
+ * max_kv_splits = 1 turns off both kinds of split.
  * workspace: device memory of at least cpp_attn_workspace_min_bytes(...) with
  * the same (num_reqs, num_tokens, heads, head_dim, max_kv_splits); it is
  * scratch, overwritten by each call; calls that share it must be stream-ordered.
