@@ -506,7 +506,6 @@ def main():
     clocks = ClockSampler(gpu_uuid)
     ev0 = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
     ev1 = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
-    kernel_ms = []
     enqueue_s = []
     if dist: dist.barrier()
     torch.cuda.synchronize()
@@ -516,11 +515,10 @@ def main():
         flush.zero_()
         ev0[s].record(stream)
         te = time.perf_counter()
-        wl.step(stream, with_marks=True)
+        wl.step(stream)
         enqueue_s.append(time.perf_counter() - te)
         ev1[s].record(stream)
         torch.cuda.synchronize()
-        kernel_ms.append(wl.chunk_kernel_ms())
     torch.cuda.synchronize()
     if dist: dist.barrier()
     t_end = time.perf_counter()
@@ -553,7 +551,15 @@ def main():
         e2e_ms.append(e0.elapsed_time(e1))
     e2e_val = world * STEP_FLOPS / (float(np.mean(e2e_ms)) * 1e-3) / 1e12
 
-    # roofline of the dominant kernel (the tensor-core chunk kernel)
+    # roofline of the dominant kernel (the tensor-core chunk kernel): separate steps
+    # with events around every chunk-kernel launch (events between kernels keep
+    # the next kernel from launching early, so the headline steps carry none)
+    kernel_ms = []
+    for s in range(5):
+        flush.zero_()
+        wl.step(stream, with_marks=True)
+        torch.cuda.synchronize()
+        kernel_ms.append(wl.chunk_kernel_ms())
     peak_tf, peak_bw, peak_src = load_peaks()
     km = np.asarray(kernel_ms)                       # [steps, chunks]
     per_launch_ms = float(km.mean())

@@ -255,8 +255,7 @@ int cpp_chunked_prefill_attn_events(const void *q, const void *k_cache, const vo
     pp.max_citems = L.max_citems;
     pp.dev_err = dev_err;
     mark(0, s);
-    launch_plan(pp, s);
-    if (cudaGetLastError() != cudaSuccess)
+    if (launch_plan(pp, s) != cudaSuccess)
         return CPSA_ERR_CUDA;
     mark(1, s);
 

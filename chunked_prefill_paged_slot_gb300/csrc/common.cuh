@@ -3,6 +3,8 @@
 // commit) and bounded waits that give up with an error flag instead of hanging.
 #pragma once
 
+#include <utility>
+
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
@@ -202,6 +204,35 @@ __device__ __forceinline__ void umma_commit(uint64_t *bar)
     asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
                      smem_u32(bar))
                  : "memory");
+}
+
+// Programmatic dependent launch. Every kernel of a call is launched with
+// launch_pdl: it may be scheduled while the kernel before it in the stream is
+// still running. Each kernel lets its own dependents launch at once
+// (pdl_trigger) and, before it reads anything an earlier kernel wrote or writes
+// anything an earlier kernel may still read, waits for the kernel before it to
+// complete with its memory visible (pdl_wait). Every CTA calls pdl_wait before
+// it can exit, so a kernel never completes before its predecessor and the
+// ordering is transitive along the stream. The launch latency of each kernel
+// then overlaps the tail of the one before.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
+template <typename... KArgs, typename... Args>
+inline cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t s,
+                              Args &&...args)
+{
+    cudaLaunchConfig_t cfg{};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
 }
 
 // One lane of a converged warp, chosen by elect.sync. A tcgen05.mma or commit is

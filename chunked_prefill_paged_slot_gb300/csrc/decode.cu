@@ -109,7 +109,6 @@ decode_attn_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap tm_
     DecBars *bars = reinterpret_cast<DecBars *>(smem + C::kBarOff);
     float *merge = reinterpret_cast<float *>(smem + C::kMergeOff);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int n_items = p.counts[kCntDecode];
     const int G = p.group;
 
     if (threadIdx.x == 0) {
@@ -120,6 +119,10 @@ decode_attn_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap tm_
         bars->abort = 0;
         fence_barrier_init();
     }
+    // set-up above touches no global memory: from here on the plan's output
+    pdl_trigger();
+    pdl_wait();
+    const int n_items = p.counts[kCntDecode];
     __syncthreads();
     volatile int *abort = &bars->abort;
 
@@ -388,8 +391,7 @@ cudaError_t launch_decode_t(const DecodeParams &p, const CUtensorMap &tk, const 
     cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
     if (e != cudaSuccess)
         return e;
-    k<<<grid, C::kThreads, C::kSmemBytes, s>>>(p, tk, tv);
-    return cudaGetLastError();
+    return launch_pdl(k, dim3(grid), dim3(C::kThreads), C::kSmemBytes, s, p, tk, tv);
 }
 
 }  // namespace

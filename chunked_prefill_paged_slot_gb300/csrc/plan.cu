@@ -274,6 +274,8 @@ __device__ T block_sum(T x)
 
 __global__ void __launch_bounds__(kPlanThreads, 1) plan_kernel(PlanParams p)
 {
+    pdl_trigger();
+    pdl_wait();
     // ---- pass 1: tokens, prefill tiles, decode partial rows
     long long tok = 0, tiles = 0, dprows = 0;
     for (int base = 0; base < p.num_reqs; base += kPlanThreads) {
@@ -386,6 +388,8 @@ __global__ void __launch_bounds__(kPlanThreads, 1) plan_kernel(PlanParams p)
 // totals of the ones before it (one pass, no block-wide barriers).
 __global__ void __launch_bounds__(32, 1) plan_small_kernel(PlanParams p)
 {
+    pdl_trigger();
+    pdl_wait();
     const int lane = threadIdx.x;
     const bool mine = lane < p.num_reqs;
     Req rq{false, 0, 0, 0};
@@ -456,12 +460,11 @@ __global__ void __launch_bounds__(32, 1) plan_small_kernel(PlanParams p)
 
 }  // namespace
 
-void launch_plan(const PlanParams &p, cudaStream_t s)
+cudaError_t launch_plan(const PlanParams &p, cudaStream_t s)
 {
     if (p.num_reqs <= 32)
-        plan_small_kernel<<<1, 32, 0, s>>>(p);
-    else
-        plan_kernel<<<1, kPlanThreads, 0, s>>>(p);
+        return launch_pdl(plan_small_kernel, dim3(1), dim3(32), 0, s, p);
+    return launch_pdl(plan_kernel, dim3(1), dim3(kPlanThreads), 0, s, p);
 }
 
 }  // namespace cpsa

@@ -10,6 +10,7 @@
 // its item count from the workspace, so the host never needs the lengths.
 #pragma once
 
+#include <cuda_runtime.h>
 #include <stddef.h>
 #include <stdint.h>
 
@@ -129,6 +130,6 @@ struct PlanParams {
     uint32_t *dev_err;
 };
 
-void launch_plan(const PlanParams &p, cudaStream_t s);
+cudaError_t launch_plan(const PlanParams &p, cudaStream_t s);
 
 }  // namespace cpsa

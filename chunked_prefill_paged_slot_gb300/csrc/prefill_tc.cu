@@ -93,9 +93,6 @@ chunk_attn_kernel(const ChunkParams p, const __grid_constant__ CUtensorMap tm_q,
             mbar_init(&bars->slot_empty[s], 1);
         }
         bars->abort = 0;
-        // this CTA's run of pieces, from the plan's table
-        bars->it_begin = p.run_first[blockIdx.x];
-        bars->it_end = p.run_first[blockIdx.x + 1];
         fence_barrier_init();
     }
     if (warp == C::kLoadWarp && lane == 0) {
@@ -106,6 +103,14 @@ chunk_attn_kernel(const ChunkParams p, const __grid_constant__ CUtensorMap tm_q,
     if (warp == C::kMmaWarp) {
         tmem_alloc(&bars->tmem_base, C::kTmemCols);
         tmem_relinquish();
+    }
+    // the set-up above touches no global memory; from here on the plan's output
+    pdl_trigger();
+    pdl_wait();
+    if (threadIdx.x == 0) {
+        // this CTA's run of pieces, from the plan's table
+        bars->it_begin = p.run_first[blockIdx.x];
+        bars->it_end = p.run_first[blockIdx.x + 1];
     }
     tc_fence_before_sync();
     __syncthreads();
@@ -500,8 +505,7 @@ cudaError_t launch_chunk_t(const ChunkParams &p, const CUtensorMap &tq, const CU
     cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
     if (e != cudaSuccess)
         return e;
-    k<<<grid, C::kThreads, C::kSmemBytes, s>>>(p, tq, tk, tv);
-    return cudaGetLastError();
+    return launch_pdl(k, dim3(grid), dim3(C::kThreads), C::kSmemBytes, s, p, tq, tk, tv);
 }
 
 }  // namespace

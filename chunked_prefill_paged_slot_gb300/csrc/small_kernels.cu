@@ -21,6 +21,8 @@ __global__ void __launch_bounds__(256) kv_write_kernel(const uint4 *__restrict__
                                                        uint4 *__restrict__ k_cache, uint4 *__restrict__ v_cache,
                                                        uint32_t *dev_err)
 {
+    pdl_trigger();
+    pdl_wait();
     const int64_t rows = num_tokens * num_kv_heads;
     const int64_t total = rows * VEC_PER_ROW;
     const int64_t slots = num_pages * page_size;
@@ -70,6 +72,8 @@ __global__ void __launch_bounds__(kCombineThreads, 4) combine_kernel(const Combi
 {
     __shared__ int s_u0[kCombineSmemItems];
     __shared__ CombineItem s_item[kCombineFullItems];
+    pdl_trigger();
+    pdl_wait();
     const int n_items = p.counts[kCntCombine];
     const int total = p.counts[kCntCombineUnits];
     if (n_items == 0 || total == 0)
@@ -201,6 +205,8 @@ split_kernel(const int32_t *__restrict__ query_lens, int num_reqs, float balance
     __shared__ long long warp_tot[kSplitThreads / 32];
     __shared__ unsigned long long warp_best[kSplitThreads / 32];
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    pdl_trigger();
+    pdl_wait();
     if (num_reqs < 2) {
         if (threadIdx.x == 0) {
             out3[0] = 0;
@@ -308,30 +314,26 @@ cudaError_t launch_kv_cache_write(const void *k, const void *v, const int64_t *s
     const int64_t cap = (int64_t)num_sms * 8;
     if (blocks > cap) blocks = cap;
     if (head_dim == 128)
-        kv_write_kernel<16><<<(int)blocks, 256, 0, s>>>((const uint4 *)k, (const uint4 *)v, slot_mapping, num_tokens,
-                                                        num_kv_heads, page_size, num_pages, (uint4 *)k_cache,
-                                                        (uint4 *)v_cache, dev_err);
-    else
-        kv_write_kernel<8><<<(int)blocks, 256, 0, s>>>((const uint4 *)k, (const uint4 *)v, slot_mapping, num_tokens,
-                                                       num_kv_heads, page_size, num_pages, (uint4 *)k_cache,
-                                                       (uint4 *)v_cache, dev_err);
-    return cudaGetLastError();
+        return launch_pdl(kv_write_kernel<16>, dim3((unsigned)blocks), dim3(256), 0, s, (const uint4 *)k,
+                          (const uint4 *)v, slot_mapping, num_tokens, num_kv_heads, page_size, num_pages,
+                          (uint4 *)k_cache, (uint4 *)v_cache, dev_err);
+    return launch_pdl(kv_write_kernel<8>, dim3((unsigned)blocks), dim3(256), 0, s, (const uint4 *)k,
+                      (const uint4 *)v, slot_mapping, num_tokens, num_kv_heads, page_size, num_pages,
+                      (uint4 *)k_cache, (uint4 *)v_cache, dev_err);
 }
 
 cudaError_t launch_combine(const CombineParams &p, int head_dim, int grid, cudaStream_t s)
 {
     if (head_dim == 128)
-        combine_kernel<128><<<grid, kCombineThreads, 0, s>>>(p);
-    else
-        combine_kernel<64><<<grid, kCombineThreads, 0, s>>>(p);
-    return cudaGetLastError();
+        return launch_pdl(combine_kernel<128>, dim3(grid), dim3(kCombineThreads), 0, s, p);
+    return launch_pdl(combine_kernel<64>, dim3(grid), dim3(kCombineThreads), 0, s, p);
 }
 
 cudaError_t launch_split_microbatch(const int32_t *query_lens, int num_reqs, float balance_threshold,
                                     int32_t length_threshold, int32_t *out3, cudaStream_t s)
 {
-    split_kernel<<<1, kSplitThreads, 0, s>>>(query_lens, num_reqs, balance_threshold, length_threshold, out3);
-    return cudaGetLastError();
+    return launch_pdl(split_kernel, dim3(1), dim3(kSplitThreads), 0, s, query_lens, num_reqs, balance_threshold,
+                      length_threshold, out3);
 }
 
 }  // namespace cpsa
