@@ -321,6 +321,62 @@ def decode_bandwidth(dev, reps=5, n_decode=1536):
     return res
 
 
+def kv_write_bandwidth(dev, reps=5):
+    """KV write GB/s (algorithmic bytes 2*T*Hkv*d*2*2 + 8T: read k and v, write both
+    caches, read the slots) for the headline chunk (T = 512, page 128) and for the
+    micro-batch workload's token count (T = 166528, page 16), slots a permutation of
+    the cache's slots, L2 flushed before each repetition."""
+    import torch
+    import chunked_prefill_paged_slot_gb300 as cpsa
+    res = {}
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+    err = torch.zeros(1, dtype=torch.int32, device=dev)
+    g = torch.Generator(device=dev)
+    g.manual_seed(7)
+    for T, P in ((CHUNK, PAGE), (166528, 16)):
+        n_pages = (T + P - 1) // P
+        k = torch.randn((T, HKV, D), generator=g, device=dev).to(torch.bfloat16)
+        v = torch.randn((T, HKV, D), generator=g, device=dev).to(torch.bfloat16)
+        kc = torch.empty((n_pages, HKV, P, D), dtype=torch.bfloat16, device=dev)
+        vc = torch.empty_like(kc)
+        slots = torch.randperm(n_pages * P, generator=g, device=dev)[:T].to(torch.int64)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        ts = []
+        for r in range(reps + 2):
+            flush.zero_()
+            e0.record()
+            cpsa.cpp_kv_cache_write(k, v, slots, kc, vc, err)
+            e1.record()
+            torch.cuda.synchronize()
+            if r >= 2:
+                ts.append(e0.elapsed_time(e1))
+        ms = float(np.median(ts))
+        nbytes = 2.0 * T * HKV * D * 2 * 2 + 8 * T
+        res[f"T{T}_page{P}"] = {"ms": round(ms, 4), "bytes": nbytes, "gbs": round(nbytes / (ms * 1e-3) / 1e9, 1)}
+        del k, v, kc, vc, slots
+    res["device_flags"] = cpsa.cpp_read_device_error(err)
+    del flush
+    torch.cuda.empty_cache()
+    return res
+
+
+def step_roofline(ms_per_step, peak_tf, peak_gbs):
+    """t_roof of the headline step: per chunk max(F / peak_bf16, bytes_attn / BW) plus the KV
+    write's bytes / BW, bytes_attn = K and V of the chunk's keys once per kv head + q read and
+    out written + the block_table entries."""
+    t, tensor_bound = 0.0, 0
+    for i in range(N_CHUNKS):
+        s = (i + 1) * CHUNK
+        f = chunk_flops(i * CHUNK, CHUNK)
+        b_attn = s * HKV * D * 2 * 2 + 2 * CHUNK * HQ * D * 2 + 4 * ((s + PAGE - 1) // PAGE)
+        b_kvw = 2 * CHUNK * HKV * D * 2 * 2 + 8 * CHUNK
+        tf, tb = f / (peak_tf * 1e12), b_attn / (peak_gbs * 1e9)
+        tensor_bound += tf >= tb
+        t += max(tf, tb) + b_kvw / (peak_gbs * 1e9)
+    return {"t_roof_ms": round(t * 1e3, 4), "frac": round(t * 1e3 / ms_per_step, 4),
+            "chunks_tensor_bound": int(tensor_bound), "chunks": N_CHUNKS}
+
+
 # ----------------------------------------------------------------------------- suite of the other workloads
 class ChunkTimer:
     """Times one chunk (split + KV write + attention) of the headline sequence at
@@ -376,8 +432,9 @@ def fit_report(X, t):
 
 
 def suite(dev):
-    """Dynamic chunking (profile, fit, plan, per-chunk times), the two-variable
-    latency fit, tile alignment, and the micro-batch workload on one vs two streams."""
+    """Dynamic chunking (profile, fit, plan, per-chunk times), the online-calibrated
+    controller, the two-variable latency fit, tile alignment, and the micro-batch
+    workload on one vs two streams."""
     import torch
     import chunked_prefill_paged_slot_gb300 as cpsa
     import workloads as W
@@ -401,6 +458,25 @@ def suite(dev):
         "fit_f_l": {"a": a, "b": b, "c": c, **fr}, "target_ms": a * 4096 ** 2 + b * 4096,
         "chunks": chunks, "chunk_ms": [round(v, 4) for v in dyn],
         "cv_excluding_last": float(np.std(body) / np.mean(body)), "total_ms": float(np.sum(dyn))}
+    # --- online calibration: chunk sizes from the controller, fed back with each chunk's own time
+    oc = cpsa.OnlineChunker(a, b, c, 4096, PAGE, min_chunk=64, window=30, min_points=5)
+    L, och, oms = 0, [], []
+    while L < SEQ:
+        x = oc.next_chunk(L, SEQ - L)
+        t_ms = ct.time(L, x, reps=3)
+        oc.record([x], [L], t_ms)
+        och.append(x)
+        oms.append(t_ms)
+        L += x
+    (oa, ob, occ), n_rec, calibrated = oc.model()
+    oc.close()
+    obody = oms[:-1] if len(oms) > 2 else oms
+    out["online_calibration"] = {
+        "workload": "the same prompt, each next chunk from the online controller (startup model above, "
+                    "two-variable refit over the last 30 chunks from the 5th on), fed each chunk's measured time",
+        "chunks": och, "chunk_ms": [round(v, 4) for v in oms],
+        "cv_excluding_last": float(np.std(obody) / np.mean(obody)), "total_ms": float(np.sum(oms)),
+        "final_model": {"a": oa, "b": ob, "c": occ, "batches": n_rec, "calibrated": calibrated}}
     # --- fixed 512 chunks (the headline sequence) for f(C, H)
     fixed = [ct.time(512 * i, 512, reps=3) for i in range(N_CHUNKS)]
     samples_C = [512] * N_CHUNKS + list(chunks) + list(sizes)
@@ -586,11 +662,18 @@ def main():
             "e2e": {"value": round(e2e_val, 3), "unit": "TFLOP/s", "h2d_bytes_per_step": h2d,
                     "d2h_bytes_per_step": d2h, "ms_per_step": round(float(np.mean(e2e_ms)), 4)},
             "roofline": roofline, "gpu_launches": launches, "clocks": clk,
+            "tokens_per_s": round(world * SEQ / (ms_per_step * 1e-3), 1),
+            "step_roofline": step_roofline(ms_per_step, peak_tf, peak_bw),
             "wall_s": round(wall, 3), "host_enqueue_ms_per_step": round(1e3 * float(np.mean(enqueue_s)), 3),
             "device_flags": flags}
     if not args.no_secondary and rank == 0:
         del wl
         torch.cuda.empty_cache()
+        try:
+            line["kv_write"] = kv_write_bandwidth(dev)
+            line["kv_write"]["hbm_peak_gbs"] = peak_bw
+        except Exception as e:
+            line["kv_write"] = {"error": repr(e)}
         try:
             line["secondary"] = decode_bandwidth(dev)
             line["secondary"]["hbm_peak_gbs"] = peak_bw

@@ -66,6 +66,8 @@ def load():
     lib.cpp_split_microbatch.argtypes = [_c_p, _c_int, _c_f, ctypes.c_int32, _c_p, _c_p]
     lib.cpp_read_device_error.restype = _c_int
     lib.cpp_read_device_error.argtypes = [_c_p, _c_p, _c_int, _c_p]
+    lib.cpp_get_device_error.restype = _c_int
+    lib.cpp_get_device_error.argtypes = [_c_p, _c_p, _c_p]
     lib.cpp_plan_chunk_sizes.restype = _c_int
     lib.cpp_plan_chunk_sizes.argtypes = [_c_d, _c_d, _c_d, _c_i64, _c_i64, _c_int, _c_i64, _c_i64, _c_i64, _c_d,
                                          _c_p, _c_i64, _c_p]
@@ -73,6 +75,16 @@ def load():
     lib.cpp_fit_latency_quadratic.argtypes = [_c_p, _c_p, _c_int, _c_p]
     lib.cpp_fit_latency_two_var.restype = _c_int
     lib.cpp_fit_latency_two_var.argtypes = [_c_p, _c_p, _c_p, _c_p, _c_int, _c_p]
+    lib.cpp_online_create.restype = _c_p
+    lib.cpp_online_create.argtypes = [_c_d, _c_d, _c_d, _c_i64, _c_int, _c_i64, _c_i64, _c_i64, _c_d, _c_int, _c_int]
+    lib.cpp_online_destroy.restype = None
+    lib.cpp_online_destroy.argtypes = [_c_p]
+    lib.cpp_online_next_chunk.restype = _c_int
+    lib.cpp_online_next_chunk.argtypes = [_c_p, _c_i64, _c_i64, _c_p]
+    lib.cpp_online_record.restype = _c_int
+    lib.cpp_online_record.argtypes = [_c_p, _c_p, _c_p, _c_int, _c_d]
+    lib.cpp_online_model.restype = _c_int
+    lib.cpp_online_model.argtypes = [_c_p, _c_p, _c_p, _c_p]
     lib.cpp_selftest_exp2.restype = _c_int
     lib.cpp_selftest_exp2.argtypes = [_c_p, _c_p, _c_p, _c_i64, _c_p]
     lib.cpp_status_string.restype = ctypes.c_char_p
@@ -209,6 +221,14 @@ def cpp_read_device_error(dev_err, clear=True, stream=None) -> int:
     return int(host.value)
 
 
+def cpp_get_device_error(dev_err, stream=None) -> int:
+    """The device error word, left as it is (reading it synchronises the stream)."""
+    host = ctypes.c_uint32(0)
+    st = load().cpp_get_device_error(_dev(dev_err, torch.int32, "dev_err"), ctypes.byref(host), _stream_ptr(stream))
+    _check(st, "cpp_get_device_error")
+    return int(host.value)
+
+
 def cpp_plan_chunk_sizes(a, b, c, prompt_len, base_chunk_size, page_size, min_chunk=64, max_model_len=0,
                          max_num_scheduled_tokens=0, smooth_factor=1.0):
     lib = load()
@@ -238,6 +258,44 @@ def cpp_fit_latency_two_var(x0, x1, x2, times):
     _check(load().cpp_fit_latency_two_var(_dbl(x0), _dbl(x1), _dbl(x2), _dbl(times), len(times), coef),
            "cpp_fit_latency_two_var")
     return [coef[0], coef[1], coef[2]]
+
+
+class OnlineChunker:
+    """Handle of the library's online chunk-size controller (cpp_online_* in cpsa.h)."""
+
+    def __init__(self, a, b, c, base_chunk_size, page_size, min_chunk=64, max_model_len=0,
+                 max_num_scheduled_tokens=0, smooth_factor=1.0, window=30, min_points=5):
+        self._lib = load()
+        self._h = self._lib.cpp_online_create(a, b, c, base_chunk_size, page_size, min_chunk, max_model_len,
+                                              max_num_scheduled_tokens, smooth_factor, window, min_points)
+        if not self._h:
+            raise CpsaError("cpp_online_create: invalid arguments")
+
+    def next_chunk(self, history, remaining) -> int:
+        out = ctypes.c_int64(0)
+        _check(self._lib.cpp_online_next_chunk(self._h, history, remaining, ctypes.byref(out)),
+               "cpp_online_next_chunk")
+        return int(out.value)
+
+    def record(self, chunks, histories, time_ms):
+        cs = (ctypes.c_int64 * len(chunks))(*[int(x) for x in chunks])
+        hs = (ctypes.c_int64 * len(histories))(*[int(x) for x in histories])
+        _check(self._lib.cpp_online_record(self._h, cs, hs, len(chunks), float(time_ms)), "cpp_online_record")
+
+    def model(self):
+        """((a, b, c), batches recorded, calibrated)."""
+        coef = (ctypes.c_double * 3)()
+        n, cal = ctypes.c_int(0), ctypes.c_int(0)
+        _check(self._lib.cpp_online_model(self._h, coef, ctypes.byref(n), ctypes.byref(cal)), "cpp_online_model")
+        return (coef[0], coef[1], coef[2]), n.value, bool(cal.value)
+
+    def close(self):
+        if getattr(self, "_h", None):
+            self._lib.cpp_online_destroy(self._h)
+            self._h = None
+
+    def __del__(self):
+        self.close()
 
 
 def cpp_selftest_exp2(x, stream=None):

@@ -367,4 +367,9 @@ int cpp_read_device_error(uint32_t *dev_err, uint32_t *host_flags, int clear, vo
     return CPSA_OK;
 }
 
+int cpp_get_device_error(const uint32_t *dev_err, uint32_t *host_flags, void *stream)
+{
+    return cpp_read_device_error(const_cast<uint32_t *>(dev_err), host_flags, 0, stream);
+}
+
 }  // extern "C"

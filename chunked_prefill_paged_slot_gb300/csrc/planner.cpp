@@ -6,6 +6,9 @@
 #include <math.h>
 #include <stdint.h>
 
+#include <new>
+#include <vector>
+
 #include "../../include/cpsa.h"
 
 namespace {
@@ -69,9 +72,137 @@ int least_squares3(const double *x0, const double *x1, const double *x2, const d
     return CPSA_OK;
 }
 
+// Page alignment, minimum and caps of a solved chunk size (shared by the
+// planner and the online controller).
+int64_t postprocess_chunk(double x, int64_t L, int64_t remaining, double base, int page_size, int64_t min_chunk,
+                          int64_t max_model_len, int64_t max_num_scheduled_tokens, double smooth_factor)
+{
+    const double xs = smooth_factor * x + (1.0 - smooth_factor) * base;
+    int64_t units = (int64_t)floor(xs / (double)page_size * (1.0 + 1e-9));
+    int64_t sz = units * page_size;
+    if (sz < min_chunk)
+        sz = min_chunk;
+    if (max_model_len > 0 && sz > max_model_len - L)
+        sz = max_model_len - L;
+    if (max_num_scheduled_tokens > 0 && sz > max_num_scheduled_tokens)
+        sz = max_num_scheduled_tokens;
+    if (sz > remaining)
+        sz = remaining;
+    if (sz < 1)
+        sz = 1;
+    return sz;
+}
+
+// Positive root C of f(C, H) - f(0, H) = T under f(C, H) = a C (C + H) + b (C + H) + c,
+// i.e. a C^2 + (aH + b) C - T = 0, in the same cancellation-free form.
+double next_chunk_root_two_var(double a, double b, double T, double H, double base)
+{
+    if (a <= 0.0)
+        return b > 0.0 ? T / b : base;
+    const double lin = a * H + b;
+    return 2.0 * T / (lin + sqrt(lin * lin + 4.0 * a * T));
+}
+
 }  // namespace
 
+// Online chunk-size controller: the startup model until enough batches are
+// recorded, then the two-variable model refitted over a sliding window.
+struct cpsa_online {
+    double a, b, c;             // current coefficients
+    bool calibrated;            // two-variable model in use
+    double base;
+    int page_size;
+    int64_t min_chunk, max_model_len, max_num_scheduled_tokens;
+    double smooth_factor;
+    int window, min_points;
+    std::vector<double> x0, x1, x2, t;   // per recorded batch
+};
+
 extern "C" {
+
+cpsa_online *cpp_online_create(double a, double b, double c, int64_t base_chunk_size, int page_size,
+                               int64_t min_chunk, int64_t max_model_len, int64_t max_num_scheduled_tokens,
+                               double smooth_factor, int window, int min_points)
+{
+    if (base_chunk_size <= 0 || page_size <= 0 || min_chunk < 1 || window < 3 || min_points < 3 ||
+        min_points > window)
+        return nullptr;
+    cpsa_online *h = new (std::nothrow) cpsa_online();
+    if (!h)
+        return nullptr;
+    h->a = a;
+    h->b = b;
+    h->c = c;
+    h->calibrated = false;
+    h->base = (double)base_chunk_size;
+    h->page_size = page_size;
+    h->min_chunk = min_chunk;
+    h->max_model_len = max_model_len;
+    h->max_num_scheduled_tokens = max_num_scheduled_tokens;
+    h->smooth_factor = smooth_factor;
+    h->window = window;
+    h->min_points = min_points;
+    return h;
+}
+
+void cpp_online_destroy(cpsa_online *h) { delete h; }
+
+int cpp_online_next_chunk(const cpsa_online *h, int64_t history, int64_t remaining, int64_t *chunk)
+{
+    if (!h || !chunk || history < 0 || remaining < 1)
+        return CPSA_ERR_BAD_SHAPE;
+    const double base = h->base;
+    const double T = h->a * base * base + h->b * base;   // f(base, 0) - f(0, 0), same for both models
+    const double x = h->calibrated ? next_chunk_root_two_var(h->a, h->b, T, (double)history, base)
+                                   : next_chunk_root(h->a, h->b, T, (double)history, base);
+    *chunk = postprocess_chunk(x, history, remaining, base, h->page_size, h->min_chunk, h->max_model_len,
+                               h->max_num_scheduled_tokens, h->smooth_factor);
+    return CPSA_OK;
+}
+
+int cpp_online_record(cpsa_online *h, const int64_t *chunks, const int64_t *histories, int n_chunks,
+                      double time_ms)
+{
+    if (!h || n_chunks < 1 || !chunks || !histories)
+        return CPSA_ERR_BAD_SHAPE;
+    double f0 = 0.0, f1 = 0.0;
+    for (int i = 0; i < n_chunks; ++i) {
+        const double C = (double)chunks[i], H = (double)histories[i];
+        f0 += C * (C + H);
+        f1 += C + H;
+    }
+    h->x0.push_back(f0);
+    h->x1.push_back(f1);
+    h->x2.push_back((double)n_chunks);
+    h->t.push_back(time_ms);
+    const int n = (int)h->t.size();
+    if (n < h->min_points)
+        return CPSA_OK;
+    const int m = n < h->window ? n : h->window;
+    const int o = n - m;
+    double coef[3];
+    if (least_squares3(h->x0.data() + o, h->x1.data() + o, h->x2.data() + o, h->t.data() + o, m, coef) == CPSA_OK) {
+        h->a = coef[0];
+        h->b = coef[1];
+        h->c = coef[2];
+        h->calibrated = true;
+    }
+    return CPSA_OK;
+}
+
+int cpp_online_model(const cpsa_online *h, double *coef, int *n_samples, int *calibrated)
+{
+    if (!h || !coef)
+        return CPSA_ERR_NULL_ARG;
+    coef[0] = h->a;
+    coef[1] = h->b;
+    coef[2] = h->c;
+    if (n_samples)
+        *n_samples = (int)h->t.size();
+    if (calibrated)
+        *calibrated = h->calibrated ? 1 : 0;
+    return CPSA_OK;
+}
 
 int cpp_plan_chunk_sizes(double a, double b, double c, int64_t prompt_len, int64_t base_chunk_size, int page_size,
                          int64_t min_chunk, int64_t max_model_len, int64_t max_num_scheduled_tokens,
@@ -85,19 +216,8 @@ int cpp_plan_chunk_sizes(double a, double b, double c, int64_t prompt_len, int64
     int64_t L = 0, n = 0;
     while (L < prompt_len) {
         const double x = next_chunk_root(a, b, T, (double)L, base);
-        const double xs = smooth_factor * x + (1.0 - smooth_factor) * base;
-        int64_t units = (int64_t)floor(xs / (double)page_size * (1.0 + 1e-9));
-        int64_t sz = units * page_size;
-        if (sz < min_chunk)
-            sz = min_chunk;
-        if (max_model_len > 0 && sz > max_model_len - L)
-            sz = max_model_len - L;
-        if (max_num_scheduled_tokens > 0 && sz > max_num_scheduled_tokens)
-            sz = max_num_scheduled_tokens;
-        if (sz > prompt_len - L)
-            sz = prompt_len - L;
-        if (sz < 1)
-            sz = 1;
+        const int64_t sz = postprocess_chunk(x, L, prompt_len - L, base, page_size, min_chunk, max_model_len,
+                                             max_num_scheduled_tokens, smooth_factor);
         if (n < max_chunks)
             chunks[n] = sz;
         ++n;

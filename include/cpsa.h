@@ -207,6 +207,13 @@ int cpp_split_microbatch(const int32_t *query_lens, int num_reqs, float balance_
 int cpp_read_device_error(uint32_t *dev_err, uint32_t *host_flags, int clear, void *stream);
 
 /*
+ * Copy the device error word to *host_flags without resetting it (synchronises
+ * `stream`): cpp_read_device_error with clear = 0, under the name the contract
+ * of this boundary gives the read.
+ */
+int cpp_get_device_error(const uint32_t *dev_err, uint32_t *host_flags, void *stream);
+
+/*
  * Host-side chunk planner ([CPP] "runtime phase: dynamic prediction").
  *
  * Latency model f(l) = a l^2 + b l + c; target T = f(base_chunk_size) - f(0).
@@ -236,6 +243,37 @@ int cpp_plan_chunk_sizes(double a, double b, double c, int64_t prompt_len,
 int cpp_fit_latency_quadratic(const double *l, const double *t, int n, double *coef);
 int cpp_fit_latency_two_var(const double *x0, const double *x1, const double *x2,
                             const double *t, int n, double *coef);
+
+/*
+ * Online chunk-size controller ([CPP] "online calibration"): the planner above,
+ * but fed back with the measured time of every batch it sized.
+ *
+ * Until min_points batches are recorded it sizes chunks with the startup model
+ * (a, b, c of f(l), exactly as cpp_plan_chunk_sizes). Each recorded batch adds
+ * the features [sum C (C + H), sum (C + H), N] of its N chunks (size C, history
+ * H) and its time; from min_points batches on, (a, b, c) of the two-variable
+ * model f(C, H) = a C (C + H) + b (C + H) + c are refitted by least squares over
+ * the last `window` batches (the page gives 5 to 30 points), and the next chunk
+ * at history H solves f(C, H) - f(0, H) = T, i.e. a C^2 + (aH + b) C - T = 0,
+ * with T = f(base, 0) - f(0, 0) = a base^2 + b base from the current model;
+ * smoothing, page alignment, minimum and caps as in cpp_plan_chunk_sizes, and
+ * at most `remaining` tokens. A singular refit keeps the previous model.
+ *
+ * The handle is host memory owned by the library: create it once, destroy it
+ * with cpp_online_destroy. Not thread-safe; every call is host-only.
+ * cpp_online_create returns NULL on invalid arguments (base, page_size or
+ * min_chunk < 1, window < 3, min_points < 3 or > window).
+ */
+typedef struct cpsa_online cpsa_online;
+cpsa_online *cpp_online_create(double a, double b, double c, int64_t base_chunk_size, int page_size,
+                               int64_t min_chunk, int64_t max_model_len, int64_t max_num_scheduled_tokens,
+                               double smooth_factor, int window, int min_points);
+void cpp_online_destroy(cpsa_online *handle);
+int cpp_online_next_chunk(const cpsa_online *handle, int64_t history, int64_t remaining, int64_t *chunk);
+int cpp_online_record(cpsa_online *handle, const int64_t *chunks, const int64_t *histories, int n_chunks,
+                      double time_ms);
+/* coef[3] = current (a, b, c); *n_samples batches recorded; *calibrated = 1 once refitted */
+int cpp_online_model(const cpsa_online *handle, double *coef, int *n_samples, int *calibrated);
 
 /*
  * Self-test of the attention kernels' two base-2 exponentials on n device floats:

@@ -7,7 +7,8 @@ package imports nothing from the product: the two share no code.
 Parts:
   attention.c  KV write (bit copy by slot) and paged causal attention, fp64, OpenMP
   split.py     simple and balanced micro-batch split points (pure Python integers)
-  planner.py   quadratic latency model, chunk-size solver and post-processing
+  planner.py   quadratic latency model, chunk-size solver and post-processing,
+               online calibration (windowed two-variable refit)
 Parity status of each function (what pins it) is listed in each module's header.
 """
 from __future__ import annotations
@@ -107,4 +108,5 @@ def paged_attention(q, k_cache, v_cache, query_lens, seq_lens, block_table, scal
 
 from .split import simple_split, balanced_split  # noqa: E402,F401
 from .planner import (latency_quadratic, target_latency, solve_chunk, postprocess, plan_chunks,  # noqa: E402,F401
-                      fit_quadratic, fit_two_var)
+                      fit_quadratic, fit_two_var,
+                      solve_chunk_two_var, OnlineCalibrator)

@@ -23,8 +23,22 @@ Readings where the page is silent or numerically fragile:
     root that is a page multiple in exact arithmetic is not lost to rounding;
   * the last chunk of a prompt is whatever remains.
 
+Online calibration (same page, "online calibration"): after every batch the
+features [sum C(C+H), sum (C+H), N] and the measured time are recorded; once
+enough batches are in (the page: 5 to 30 points) the two-variable model is
+refitted by least squares, here over a sliding window of the last `window`
+batches. Readings:
+  * with the two-variable model the next chunk C at history H solves
+    f(C, H) - f(0, H) = T, i.e. a*C^2 + (a*H + b)*C - T = 0 (the counterpart of
+    f(L + x) - f(L) = T; f(0, H) = b*H + c is what a batch costs at that history
+    before any new token);
+  * T = f(base, 0) - f(0, 0) = a*base^2 + b*base is recomputed from the current
+    model, the page's definition of the target applied to the calibrated model;
+  * until the first refit the startup model and its solver are used.
+
 Pinned by closed forms: x(L=0) = base, f(L+x) - f(L) = T before rounding, the
-rounding/cap rules, and least-squares fits that recover exact coefficients.
+rounding/cap rules, least-squares fits that recover exact coefficients, the
+calibrated root at H = 0 equal to base, and a window that forgets older batches.
 The fits are numpy.linalg.lstsq (a library routine).
 """
 from __future__ import annotations
@@ -104,3 +118,51 @@ def fit_two_var(chunks, histories, times):
     t = np.asarray(times, dtype=np.float64)
     coef, *_ = np.linalg.lstsq(X, t, rcond=None)
     return coef, t - X @ coef
+
+
+def solve_chunk_two_var(H, a, b, T, base_chunk_size):
+    """Unrounded root C of a*C^2 + (a*H + b)*C - T = 0 (f(C, H) - f(0, H) = T)."""
+    if a <= 0.0:
+        if b <= 0.0:
+            return float(base_chunk_size)
+        return T / b
+    lin = a * H + b
+    return 2.0 * T / (lin + math.sqrt(lin * lin + 4.0 * a * T))
+
+
+class OnlineCalibrator:
+    """The online chunk-size controller, step by step as the page describes it."""
+
+    def __init__(self, a, b, c, base_chunk_size, page_size, min_chunk=64, max_model_len=None,
+                 max_num_scheduled_tokens=None, smooth_factor=1.0, window=30, min_points=5):
+        self.coef = [float(a), float(b), float(c)]
+        self.calibrated = False
+        self.base, self.page = base_chunk_size, page_size
+        self.min_chunk, self.max_model_len = min_chunk, max_model_len
+        self.max_sched, self.smooth = max_num_scheduled_tokens, smooth_factor
+        self.window, self.min_points = window, min_points
+        self.rows, self.times = [], []
+
+    def next_chunk(self, history, remaining):
+        a, b, c = self.coef
+        T = a * self.base * self.base + b * self.base
+        if self.calibrated:
+            x = solve_chunk_two_var(history, a, b, T, self.base)
+        else:
+            x = solve_chunk(history, a, b, T, self.base)
+        n = postprocess(x, history, self.base, self.page, self.smooth, self.min_chunk,
+                        self.max_model_len, self.max_sched)
+        return max(1, min(n, remaining))
+
+    def record(self, chunks, histories, time_ms):
+        cs = np.atleast_1d(np.asarray(chunks, dtype=np.float64))
+        hs = np.atleast_1d(np.asarray(histories, dtype=np.float64))
+        self.rows.append([float(np.sum(cs * (cs + hs))), float(np.sum(cs + hs)), float(len(cs))])
+        self.times.append(float(time_ms))
+        if len(self.times) >= self.min_points:
+            X = np.asarray(self.rows[-self.window:])
+            t = np.asarray(self.times[-self.window:])
+            if np.linalg.matrix_rank(X) == 3:
+                coef, *_ = np.linalg.lstsq(X, t, rcond=None)
+                self.coef = [float(v) for v in coef]
+                self.calibrated = True

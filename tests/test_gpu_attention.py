@@ -129,3 +129,18 @@ def test_host_argument_errors(cuda_lib):
     with pytest.raises(cuda_lib.CpsaError):    # workspace too small
         cuda_lib.cpp_chunked_prefill_attn(q, kc, kc.clone(), ql, ql.clone(), bt, q.clone(), tiny, e)
     assert cuda_lib.cpp_read_device_error(e) == 0
+
+
+def test_get_device_error_reads_without_clearing(cuda_lib):
+    """cpp_get_device_error returns the word and leaves it; cpp_read_device_error clears it."""
+    import torch
+    k = torch.zeros((2, 2, 64), dtype=torch.bfloat16, device="cuda")
+    kc = torch.zeros((1, 2, 16, 64), dtype=torch.bfloat16, device="cuda")
+    vc = torch.zeros_like(kc)
+    slots = torch.tensor([3, 16], dtype=torch.int64, device="cuda")   # 16 = past the one 16-slot page
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    cuda_lib.cpp_kv_cache_write(k, k, slots, kc, vc, err)
+    assert cuda_lib.cpp_get_device_error(err) == cuda_lib.DEV_SLOT_OUT_OF_RANGE
+    assert cuda_lib.cpp_get_device_error(err) == cuda_lib.DEV_SLOT_OUT_OF_RANGE
+    assert cuda_lib.cpp_read_device_error(err, clear=True) == cuda_lib.DEV_SLOT_OUT_OF_RANGE
+    assert cuda_lib.cpp_get_device_error(err) == 0

@@ -120,3 +120,73 @@ def test_fits_recover_exact_coefficients():
     t = [sum(1e-7 * c * (c + h) + 1e-3 * (c + h) + 0.25 for c, h in zip(cs, hs)) for cs, hs in zip(C, H)]
     coef2, _ = oracle.fit_two_var(C, H, t)
     np.testing.assert_allclose(coef2, [1e-7, 1e-3, 0.25], rtol=1e-7)
+
+
+# ------------------------------------------------------------ online calibration
+def f_two_var(C, H, a, b, c):
+    return a * C * (C + H) + b * (C + H) + c
+
+
+def test_calibrated_root_at_zero_history_is_base():
+    a, b = 3e-7, 2e-3
+    base = 4096
+    T = a * base * base + b * base
+    assert abs(oracle.solve_chunk_two_var(0, a, b, T, base) - base) < 1e-9 * base
+
+
+def test_calibrated_root_equalises_chunk_time():
+    """f(C, H) - f(0, H) = T at the unrounded root, for many (a, b, H)."""
+    rng = np.random.default_rng(11)
+    for _ in range(200):
+        a, b = rng.uniform(1e-9, 1e-6), rng.uniform(1e-5, 1e-2)
+        H = float(rng.integers(0, 200000))
+        T = a * 4096 ** 2 + b * 4096
+        C = oracle.solve_chunk_two_var(H, a, b, T, 4096)
+        lhs = f_two_var(C, H, a, b, 0.3) - f_two_var(0.0, H, a, b, 0.3)
+        assert abs(lhs - T) <= 1e-9 * T
+        assert 0 < C <= 4096 + 1e-6     # history only makes chunks smaller
+    assert oracle.solve_chunk_two_var(5000, 0.0, 2e-3, 8.0, 4096) == pytest.approx(4000.0)
+    assert oracle.solve_chunk_two_var(5000, 0.0, 0.0, 8.0, 4096) == 4096.0
+
+
+def test_online_calibration_recovers_the_model_and_forgets_old_batches():
+    true_a, b0, c0 = (2e-7, 1.5e-3, 0.4)
+    cal = oracle.OnlineCalibrator(1e-7, 1e-3, 0.1, 4096, 128, window=6, min_points=5)
+    L = 0
+    for i in range(4):                          # startup model until the 5th batch
+        x = cal.next_chunk(L, 32768 - L)
+        cal.record([x], [L], f_two_var(x, L, true_a, b0, c0))
+        L += x
+        assert not cal.calibrated and cal.coef == [1e-7, 1e-3, 0.1]
+    x = cal.next_chunk(L, 32768 - L)
+    cal.record([x], [L], f_two_var(x, L, true_a, b0, c0))
+    assert cal.calibrated
+    np.testing.assert_allclose(cal.coef, [true_a, b0, c0], rtol=1e-6)
+    # the machine slows down: after `window` batches of the new model only it is recovered exactly
+    new = (3e-7, 2e-3, 0.6)
+    for i in range(6):
+        C, H = 256 + 128 * i, 1000 * i
+        cal.record([C, 64], [H, 0], f_two_var(C, H, *new) + f_two_var(64, 0, *new))   # c once per chunk
+    np.testing.assert_allclose(cal.coef, list(new), rtol=1e-6)
+
+
+def test_online_controller_matches_oracle():
+    """The library's controller (host C++) against the oracle's, on a noisy latency
+    model: identical chunk sizes, coefficients to 1e-9."""
+    import chunked_prefill_paged_slot_gb300 as cpsa
+    rng = np.random.default_rng(5)
+    for window, smooth in ((30, 1.0), (8, 0.7)):
+        ours = cpsa.OnlineChunker(2e-7, 1e-3, 0.2, 4096, 128, window=window, smooth_factor=smooth)
+        ref = oracle.OnlineCalibrator(2e-7, 1e-3, 0.2, 4096, 128, window=window, smooth_factor=smooth)
+        L, prompt = 0, 65536
+        while L < prompt:
+            x1, x2 = ours.next_chunk(L, prompt - L), ref.next_chunk(L, prompt - L)
+            assert x1 == x2, (L, x1, x2)
+            t = f_two_var(x1, L, 3e-7, 2.2e-3, 0.35) * (1.0 + 0.03 * rng.standard_normal())
+            ours.record([x1], [L], t)
+            ref.record([x1], [L], t)
+            L += x1
+        coef, n, cal = ours.model()
+        assert cal and ref.calibrated and n == len(ref.times)
+        np.testing.assert_allclose(coef, ref.coef, rtol=1e-9)
+        ours.close()
