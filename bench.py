@@ -360,6 +360,75 @@ def kv_write_bandwidth(dev, reps=5):
     return res
 
 
+def serving_loop(dev, chunk_caps=(), tile_align=0, budget=2048, n_req=32, decode_tokens=32, seed=11):
+    """Closed loop: the library's token-budget batch builder sizes every step
+    (decode rows first, then started prompts, then new ones) and allocates pages;
+    each step runs the KV write and the attention kernels on it. Llama-3-8B
+    shapes (32/8 heads, d128), page 16, prompts U[512, 4096], `decode_tokens`
+    decode rows per request. Device time per step from CUDA events."""
+    import torch
+    import chunked_prefill_paged_slot_gb300 as cpsa
+    rng = np.random.Generator(np.random.PCG64(seed))
+    prompts = rng.integers(512, 4096, size=n_req, endpoint=True)
+    P = 16
+    pages = int(sum((int(L) + decode_tokens + P - 1) // P for L in prompts)) + 64
+    sched = cpsa.BatchScheduler(budget, P, pages, page_order=rng.permutation(pages).astype(np.int32),
+                                chunk_caps=chunk_caps, tile_align=tile_align, max_reqs=256,
+                                max_blocks=(4096 + decode_tokens) // P + 2)
+    for i, L in enumerate(prompts):
+        sched.add_request(i, int(L), decode_tokens)
+    g = torch.Generator(device=dev)
+    g.manual_seed(seed)
+    qp = torch.randn((budget, HQ, D), generator=g, device=dev).to(torch.bfloat16)
+    kp = torch.randn((budget, HKV, D), generator=g, device=dev).to(torch.bfloat16)
+    vp = torch.randn((budget, HKV, D), generator=g, device=dev).to(torch.bfloat16)
+    kc = torch.zeros((pages, HKV, P, D), dtype=torch.bfloat16, device=dev)
+    vc = torch.zeros_like(kc)
+    out = torch.empty((budget, HQ, D), dtype=torch.bfloat16, device=dev)
+    err = torch.zeros(1, dtype=torch.int32, device=dev)
+    ws = torch.empty(cpsa.cpp_attn_workspace_bytes(256, budget, HQ, HKV, D, 8), dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    evs, prefill_tok, decode_tok, flops, steps = [], 0, 0, 0.0, 0
+    t0 = time.perf_counter()
+    while True:
+        waiting, running, _, _ = sched.stats()
+        if waiting == 0 and running == 0:
+            break
+        b = sched.step()
+        B, T = len(b["req_ids"]), len(b["slot_mapping"])
+        if B == 0:
+            raise RuntimeError("serving loop made no progress")
+        ql, sl = b["query_lens"], b["seq_lens"]
+        meta = [torch.from_numpy(x).to(dev, non_blocking=True) for x in (ql, sl, b["block_table"], b["slot_mapping"])]
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        cpsa.cpp_kv_cache_write(kp[:T], vp[:T], meta[3], kc, vc, err, stream=stream)
+        cpsa.cpp_chunked_prefill_attn(qp[:T], kc, vc, meta[0], meta[1], meta[2], out[:T], ws, err,
+                                      max_kv_splits=8, stream=stream)
+        e1.record(stream)
+        evs.append((e0, e1))
+        dec = ql == 1
+        decode_tok += int(dec.sum())
+        prefill_tok += int(ql[~dec].sum())
+        for q_r, s_r in zip(ql.tolist(), sl.tolist()):
+            h_r = s_r - q_r
+            flops += 4.0 * D * HQ * (q_r * h_r + q_r * (q_r + 1) // 2)
+        sched.commit()
+        steps += 1
+    torch.cuda.synchronize()
+    wall = time.perf_counter() - t0
+    ms = [a.elapsed_time(b_) for a, b_ in evs]
+    flags = cpsa.cpp_read_device_error(err)
+    sched.close()
+    del kc, vc, qp, kp, vp, ws
+    torch.cuda.empty_cache()
+    return {"steps": steps, "prompt_tokens": prefill_tok, "decode_tokens": decode_tok,
+            "device_ms": round(float(sum(ms)), 3), "mean_step_ms": round(float(np.mean(ms)), 4),
+            "max_step_ms": round(float(np.max(ms)), 4), "wall_s": round(wall, 3),
+            "tokens_per_s_device": round((prefill_tok + decode_tok) / (sum(ms) * 1e-3), 1),
+            "attention_tflops_device": round(flops / (sum(ms) * 1e-3) / 1e12, 2), "device_flags": flags}
+
+
 def step_roofline(ms_per_step, peak_tf, peak_gbs):
     """t_roof of the headline step: per chunk max(F / peak_bf16, bytes_attn / BW) plus the KV
     write's bytes / BW, bytes_attn = K and V of the chunk's keys once per kv head + q read and
@@ -496,6 +565,13 @@ def suite(dev):
     out["tile_alignment_h8192"] = {str(x): round(ct.time(8192, x, reps=5), 4) for x in (511, 512, 513)}
     del ct
     torch.cuda.empty_cache()
+    # --- closed-loop serving: batch builder + kernels, fixed chunks vs the progressive strategy
+    out["serving_loop"] = {
+        "workload": "32 requests, prompts U[512, 4096], 32 decode rows each, token budget 2048, page 16, "
+                    "32/8 heads d128; every step sized by the library's batch builder",
+        "budget_only": serving_loop(dev),
+        "progressive_2048_1024_512": serving_loop(dev, chunk_caps=(2048, 1024, 512)),
+        "budget_tile_128": serving_loop(dev, tile_align=128)}
     # --- micro-batch workload: one stream vs the balanced split on two streams
     spec = W.spec_microbatch()
     d = W.device_batch(spec, device=dev)

@@ -85,6 +85,18 @@ def load():
     lib.cpp_online_record.argtypes = [_c_p, _c_p, _c_p, _c_int, _c_d]
     lib.cpp_online_model.restype = _c_int
     lib.cpp_online_model.argtypes = [_c_p, _c_p, _c_p, _c_p]
+    lib.cpp_sched_create.restype = _c_p
+    lib.cpp_sched_create.argtypes = [_c_i64, _c_int, _c_i64, _c_p, _c_p, _c_int, _c_int]
+    lib.cpp_sched_destroy.restype = None
+    lib.cpp_sched_destroy.argtypes = [_c_p]
+    lib.cpp_sched_add_request.restype = _c_int
+    lib.cpp_sched_add_request.argtypes = [_c_p, _c_i64, _c_i64, _c_i64]
+    lib.cpp_sched_step.restype = _c_int
+    lib.cpp_sched_step.argtypes = [_c_p, _c_int, _c_i64, _c_int, _c_p, _c_p, _c_p, _c_p, _c_p, _c_p, _c_p]
+    lib.cpp_sched_commit.restype = _c_int
+    lib.cpp_sched_commit.argtypes = [_c_p]
+    lib.cpp_sched_stats.restype = _c_int
+    lib.cpp_sched_stats.argtypes = [_c_p, _c_p, _c_p, _c_p, _c_p]
     lib.cpp_selftest_exp2.restype = _c_int
     lib.cpp_selftest_exp2.argtypes = [_c_p, _c_p, _c_p, _c_i64, _c_p]
     lib.cpp_status_string.restype = ctypes.c_char_p
@@ -292,6 +304,62 @@ class OnlineChunker:
     def close(self):
         if getattr(self, "_h", None):
             self._lib.cpp_online_destroy(self._h)
+            self._h = None
+
+    def __del__(self):
+        self.close()
+
+
+class BatchScheduler:
+    """Handle of the library's token-budget batch builder (cpp_sched_* in cpsa.h).
+    step() returns the batch's host arrays (numpy); commit() applies it."""
+
+    def __init__(self, token_budget, page_size, num_pages, page_order=None, chunk_caps=(), tile_align=0,
+                 max_reqs=4096, max_blocks=4096):
+        import numpy as np
+        self._np = np
+        self._lib = load()
+        order = None
+        if page_order is not None:
+            self._order = np.ascontiguousarray(np.asarray(page_order, dtype=np.int32))
+            order = self._order.ctypes.data_as(_c_p)
+        caps = (ctypes.c_int64 * max(1, len(chunk_caps)))(*[int(c) for c in chunk_caps])
+        self._h = self._lib.cpp_sched_create(token_budget, page_size, num_pages, order, caps, len(chunk_caps),
+                                             tile_align)
+        if not self._h:
+            raise CpsaError("cpp_sched_create: invalid arguments")
+        self.max_reqs, self.max_blocks, self.max_tokens = max_reqs, max_blocks, token_budget
+
+    def add_request(self, rid, prompt_len, max_new_tokens):
+        _check(self._lib.cpp_sched_add_request(self._h, rid, prompt_len, max_new_tokens), "cpp_sched_add_request")
+
+    def step(self):
+        np = self._np
+        ids = np.zeros(self.max_reqs, np.int64)
+        ql = np.zeros(self.max_reqs, np.int32)
+        sl = np.zeros(self.max_reqs, np.int32)
+        bt = np.zeros((self.max_reqs, self.max_blocks), np.int32)
+        sm = np.zeros(max(1, self.max_tokens), np.int64)
+        nr, nt = ctypes.c_int(0), ctypes.c_int64(0)
+        p = lambda a: a.ctypes.data_as(_c_p)
+        _check(self._lib.cpp_sched_step(self._h, self.max_reqs, self.max_tokens, self.max_blocks, p(ids), p(ql),
+                                        p(sl), p(bt), p(sm), ctypes.byref(nr), ctypes.byref(nt)), "cpp_sched_step")
+        B, T = nr.value, nt.value
+        return {"req_ids": ids[:B].copy(), "query_lens": ql[:B].copy(), "seq_lens": sl[:B].copy(),
+                "block_table": bt[:B].copy(), "slot_mapping": sm[:T].copy()}
+
+    def commit(self):
+        _check(self._lib.cpp_sched_commit(self._h), "cpp_sched_commit")
+
+    def stats(self):
+        """(waiting, running, finished, free pages)."""
+        v = [ctypes.c_int64(0) for _ in range(4)]
+        _check(self._lib.cpp_sched_stats(self._h, *[ctypes.byref(x) for x in v]), "cpp_sched_stats")
+        return tuple(x.value for x in v)
+
+    def close(self):
+        if getattr(self, "_h", None):
+            self._lib.cpp_sched_destroy(self._h)
             self._h = None
 
     def __del__(self):

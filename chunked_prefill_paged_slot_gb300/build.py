@@ -16,7 +16,8 @@ ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 COMMON = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC", "-Xcompiler", "-O3",
           "--expt-relaxed-constexpr", "-I", os.path.join(HERE, "..", "include")]
 
-SOURCES = ["abi.cu", "plan.cu", "prefill_tc.cu", "decode.cu", "small_kernels.cu", "noalloc.cu", "planner.cpp"]
+SOURCES = ["abi.cu", "plan.cu", "prefill_tc.cu", "decode.cu", "small_kernels.cu", "noalloc.cu", "planner.cpp",
+           "scheduler.cpp"]
 
 
 def _deps():

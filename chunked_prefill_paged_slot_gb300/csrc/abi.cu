@@ -192,6 +192,9 @@ int cpp_chunked_prefill_attn_events(const void *q, const void *k_cache, const vo
         if (ev[i])
             cudaEventRecord(ev[i], st);
     };
+    // programmatic dependent launch between the kernels, except when events are
+    // recorded between them (each kernel then runs in plain stream order)
+    const bool early = events == nullptr;
     int st = check_attn_shape(num_reqs, num_tokens, num_q_heads, num_kv_heads, head_dim, max_kv_splits);
     if (st != CPSA_OK)
         return st;
@@ -255,7 +258,7 @@ int cpp_chunked_prefill_attn_events(const void *q, const void *k_cache, const vo
     pp.max_citems = L.max_citems;
     pp.dev_err = dev_err;
     mark(0, s);
-    if (launch_plan(pp, s) != cudaSuccess)
+    if (launch_plan(pp, s, early) != cudaSuccess)
         return CPSA_ERR_CUDA;
     mark(1, s);
 
@@ -306,7 +309,7 @@ int cpp_chunked_prefill_attn_events(const void *q, const void *k_cache, const vo
     const bool single_prefill = num_reqs == 1 && num_tokens >= 2;
     const bool single_decode = num_reqs == 1 && num_tokens == 1;
     const int grid_c = single_decode ? 0 : pp.chunk_grid;   // one stream-K run per CTA
-    if (grid_c > 0 && launch_chunk_attn(cp, tq, tk, tv, head_dim, nq, grid_c, s) != cudaSuccess)
+    if (grid_c > 0 && launch_chunk_attn(cp, tq, tk, tv, head_dim, nq, grid_c, s, early) != cudaSuccess)
         return CPSA_ERR_CUDA;
     mark(2, s);
 
@@ -317,14 +320,14 @@ int cpp_chunked_prefill_attn_events(const void *q, const void *k_cache, const vo
     dp.k_cache_ptr = k_cache;
     dp.v_cache_ptr = v_cache;
     int grid_d = single_prefill ? 0 : (int)(L.max_ditems < sms ? L.max_ditems : sms);
-    if (grid_d > 0 && launch_decode_attn(dp, tkd, tvd, head_dim, grid_d, s) != cudaSuccess)
+    if (grid_d > 0 && launch_decode_attn(dp, tkd, tvd, head_dim, grid_d, s, early) != cudaSuccess)
         return CPSA_ERR_CUDA;
     mark(3, s);
 
     if (cap > 0) {
         CombineParams cb{counts, citems, part_o, part_ml, out, num_q_heads};
         const int grid_m = 4 * sms;
-        if (grid_m > 0 && launch_combine(cb, head_dim, grid_m, s) != cudaSuccess)
+        if (grid_m > 0 && launch_combine(cb, head_dim, grid_m, s, early) != cudaSuccess)
             return CPSA_ERR_CUDA;
     }
     mark(4, s);

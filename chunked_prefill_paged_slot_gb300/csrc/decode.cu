@@ -384,26 +384,26 @@ decode_attn_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap tm_
 
 template <int D, bool HI>
 cudaError_t launch_decode_t(const DecodeParams &p, const CUtensorMap &tk, const CUtensorMap &tv, int grid,
-                            cudaStream_t s)
+                            cudaStream_t s, bool early)
 {
     using C = DecCfg<D, HI>;
     auto k = decode_attn_kernel<D, HI>;
     cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
     if (e != cudaSuccess)
         return e;
-    return launch_pdl(k, dim3(grid), dim3(C::kThreads), C::kSmemBytes, s, p, tk, tv);
+    return launch_pdl(early, k, dim3(grid), dim3(C::kThreads), C::kSmemBytes, s, p, tk, tv);
 }
 
 }  // namespace
 
 cudaError_t launch_decode_attn(const DecodeParams &p, const CUtensorMap &tk, const CUtensorMap &tv, int head_dim,
-                               int grid, cudaStream_t s)
+                               int grid, cudaStream_t s, bool early)
 {
     if (p.group > 8)
-        return head_dim == 128 ? launch_decode_t<128, true>(p, tk, tv, grid, s)
-                               : launch_decode_t<64, true>(p, tk, tv, grid, s);
-    return head_dim == 128 ? launch_decode_t<128, false>(p, tk, tv, grid, s)
-                           : launch_decode_t<64, false>(p, tk, tv, grid, s);
+        return head_dim == 128 ? launch_decode_t<128, true>(p, tk, tv, grid, s, early)
+                               : launch_decode_t<64, true>(p, tk, tv, grid, s, early);
+    return head_dim == 128 ? launch_decode_t<128, false>(p, tk, tv, grid, s, early)
+                           : launch_decode_t<64, false>(p, tk, tv, grid, s, early);
 }
 
 }  // namespace cpsa

@@ -48,11 +48,12 @@ struct CombineParams {
     int num_q_heads;
 };
 
+// early: launch with programmatic dependent launch (see launch_pdl)
 cudaError_t launch_chunk_attn(const ChunkParams &p, const CUtensorMap &tq, const CUtensorMap &tk,
-                              const CUtensorMap &tv, int head_dim, int nq, int grid, cudaStream_t s);
+                              const CUtensorMap &tv, int head_dim, int nq, int grid, cudaStream_t s, bool early);
 cudaError_t launch_decode_attn(const DecodeParams &p, const CUtensorMap &tk, const CUtensorMap &tv, int head_dim,
-                               int grid, cudaStream_t s);
-cudaError_t launch_combine(const CombineParams &p, int head_dim, int grid, cudaStream_t s);
+                               int grid, cudaStream_t s, bool early);
+cudaError_t launch_combine(const CombineParams &p, int head_dim, int grid, cudaStream_t s, bool early);
 
 cudaError_t launch_kv_cache_write(const void *k, const void *v, const int64_t *slot_mapping,
                                   int64_t num_tokens, int num_kv_heads, int head_dim,

@@ -460,11 +460,11 @@ __global__ void __launch_bounds__(32, 1) plan_small_kernel(PlanParams p)
 
 }  // namespace
 
-cudaError_t launch_plan(const PlanParams &p, cudaStream_t s)
+cudaError_t launch_plan(const PlanParams &p, cudaStream_t s, bool early)
 {
     if (p.num_reqs <= 32)
-        return launch_pdl(plan_small_kernel, dim3(1), dim3(32), 0, s, p);
-    return launch_pdl(plan_kernel, dim3(1), dim3(kPlanThreads), 0, s, p);
+        return launch_pdl(early, plan_small_kernel, dim3(1), dim3(32), 0, s, p);
+    return launch_pdl(early, plan_kernel, dim3(1), dim3(kPlanThreads), 0, s, p);
 }
 
 }  // namespace cpsa

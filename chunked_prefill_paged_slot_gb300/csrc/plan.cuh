@@ -130,6 +130,6 @@ struct PlanParams {
     uint32_t *dev_err;
 };
 
-cudaError_t launch_plan(const PlanParams &p, cudaStream_t s);
+cudaError_t launch_plan(const PlanParams &p, cudaStream_t s, bool early = true);
 
 }  // namespace cpsa

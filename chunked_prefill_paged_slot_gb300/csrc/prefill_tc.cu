@@ -498,24 +498,24 @@ chunk_attn_kernel(const ChunkParams p, const __grid_constant__ CUtensorMap tm_q,
 
 template <int D, int NQ>
 cudaError_t launch_chunk_t(const ChunkParams &p, const CUtensorMap &tq, const CUtensorMap &tk,
-                           const CUtensorMap &tv, int grid, cudaStream_t s)
+                           const CUtensorMap &tv, int grid, cudaStream_t s, bool early)
 {
     using C = ChunkCfg<D, NQ>;
     auto k = chunk_attn_kernel<D, NQ>;
     cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
     if (e != cudaSuccess)
         return e;
-    return launch_pdl(k, dim3(grid), dim3(C::kThreads), C::kSmemBytes, s, p, tq, tk, tv);
+    return launch_pdl(early, k, dim3(grid), dim3(C::kThreads), C::kSmemBytes, s, p, tq, tk, tv);
 }
 
 }  // namespace
 
 cudaError_t launch_chunk_attn(const ChunkParams &p, const CUtensorMap &tq, const CUtensorMap &tk,
-                              const CUtensorMap &tv, int head_dim, int nq, int grid, cudaStream_t s)
+                              const CUtensorMap &tv, int head_dim, int nq, int grid, cudaStream_t s, bool early)
 {
     if (head_dim == 128)
-        return nq == 2 ? launch_chunk_t<128, 2>(p, tq, tk, tv, grid, s) : launch_chunk_t<128, 1>(p, tq, tk, tv, grid, s);
-    return nq == 2 ? launch_chunk_t<64, 2>(p, tq, tk, tv, grid, s) : launch_chunk_t<64, 1>(p, tq, tk, tv, grid, s);
+        return nq == 2 ? launch_chunk_t<128, 2>(p, tq, tk, tv, grid, s, early) : launch_chunk_t<128, 1>(p, tq, tk, tv, grid, s, early);
+    return nq == 2 ? launch_chunk_t<64, 2>(p, tq, tk, tv, grid, s, early) : launch_chunk_t<64, 1>(p, tq, tk, tv, grid, s, early);
 }
 
 }  // namespace cpsa

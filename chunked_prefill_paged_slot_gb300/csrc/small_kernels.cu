@@ -314,25 +314,25 @@ cudaError_t launch_kv_cache_write(const void *k, const void *v, const int64_t *s
     const int64_t cap = (int64_t)num_sms * 8;
     if (blocks > cap) blocks = cap;
     if (head_dim == 128)
-        return launch_pdl(kv_write_kernel<16>, dim3((unsigned)blocks), dim3(256), 0, s, (const uint4 *)k,
+        return launch_pdl(true, kv_write_kernel<16>, dim3((unsigned)blocks), dim3(256), 0, s, (const uint4 *)k,
                           (const uint4 *)v, slot_mapping, num_tokens, num_kv_heads, page_size, num_pages,
                           (uint4 *)k_cache, (uint4 *)v_cache, dev_err);
-    return launch_pdl(kv_write_kernel<8>, dim3((unsigned)blocks), dim3(256), 0, s, (const uint4 *)k,
+    return launch_pdl(true, kv_write_kernel<8>, dim3((unsigned)blocks), dim3(256), 0, s, (const uint4 *)k,
                       (const uint4 *)v, slot_mapping, num_tokens, num_kv_heads, page_size, num_pages,
                       (uint4 *)k_cache, (uint4 *)v_cache, dev_err);
 }
 
-cudaError_t launch_combine(const CombineParams &p, int head_dim, int grid, cudaStream_t s)
+cudaError_t launch_combine(const CombineParams &p, int head_dim, int grid, cudaStream_t s, bool early)
 {
     if (head_dim == 128)
-        return launch_pdl(combine_kernel<128>, dim3(grid), dim3(kCombineThreads), 0, s, p);
-    return launch_pdl(combine_kernel<64>, dim3(grid), dim3(kCombineThreads), 0, s, p);
+        return launch_pdl(early, combine_kernel<128>, dim3(grid), dim3(kCombineThreads), 0, s, p);
+    return launch_pdl(early, combine_kernel<64>, dim3(grid), dim3(kCombineThreads), 0, s, p);
 }
 
 cudaError_t launch_split_microbatch(const int32_t *query_lens, int num_reqs, float balance_threshold,
                                     int32_t length_threshold, int32_t *out3, cudaStream_t s)
 {
-    return launch_pdl(split_kernel, dim3(1), dim3(kSplitThreads), 0, s, query_lens, num_reqs, balance_threshold,
+    return launch_pdl(true, split_kernel, dim3(1), dim3(kSplitThreads), 0, s, query_lens, num_reqs, balance_threshold,
                       length_threshold, out3);
 }
 

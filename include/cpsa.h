@@ -276,6 +276,47 @@ int cpp_online_record(cpsa_online *handle, const int64_t *chunks, const int64_t 
 int cpp_online_model(const cpsa_online *handle, double *coef, int *n_samples, int *calibrated);
 
 /*
+ * Token-budget batch builder with page allocation ([CP] section 3: the
+ * scheduling cycle; section 3.2.2: chunk-size strategies). Host only.
+ *
+ * Each step builds one batch under token_budget tokens: decode rows first (one
+ * token each, admission order), then prompts already started, each taking
+ * min(remaining prompt, budget left) tokens, then waiting requests in arrival
+ * order while budget is left. A prefill chunk is also capped by
+ * chunk_caps[min(i, n_caps - 1)] for the prompt's i-th chunk (n_caps = 0: no
+ * cap; {2048, 1024, 512} is the progressive strategy) and, when it is not the
+ * prompt's last, rounded down to a multiple of tile_align (0: none).
+ * Pages come from a free list (page_order, or 0 .. num_pages - 1 when NULL),
+ * taken from the front as a request's sequence grows and returned to the back
+ * when it finishes (prompt prefilled and max_new_tokens decode rows run). A
+ * decode row or started prompt whose tokens do not fit in the free pages is
+ * skipped for the step; admission stops at the first waiting request that does
+ * not fit. A step that schedules nothing while requests remain means the pool
+ * is too small: the caller must stop.
+ *
+ * cpp_sched_step writes the batch for cpp_kv_cache_write and
+ * cpp_chunked_prefill_attn into HOST arrays: req_ids[B], query_lens[B],
+ * seq_lens[B] (history + this step's tokens), block_table[B][max_blocks]
+ * (-1 padded), slot_mapping[T] (positions seq_len - query_len .. seq_len - 1 of
+ * each request, batch order). It fails with CPSA_ERR_BAD_SHAPE, changing
+ * nothing, when max_reqs, max_tokens or max_blocks is too small, or when the
+ * previous step was not committed. cpp_sched_commit applies the last step's
+ * progress (call it once the step's kernels are enqueued). The handle is host
+ * memory owned by the library; not thread-safe.
+ */
+typedef struct cpsa_sched cpsa_sched;
+cpsa_sched *cpp_sched_create(int64_t token_budget, int page_size, int64_t num_pages, const int32_t *page_order,
+                             const int64_t *chunk_caps, int n_caps, int tile_align);
+void cpp_sched_destroy(cpsa_sched *handle);
+int cpp_sched_add_request(cpsa_sched *handle, int64_t id, int64_t prompt_len, int64_t max_new_tokens);
+int cpp_sched_step(cpsa_sched *handle, int max_reqs, int64_t max_tokens, int max_blocks, int64_t *req_ids,
+                   int32_t *query_lens, int32_t *seq_lens, int32_t *block_table, int64_t *slot_mapping,
+                   int *n_reqs, int64_t *n_tokens);
+int cpp_sched_commit(cpsa_sched *handle);
+int cpp_sched_stats(const cpsa_sched *handle, int64_t *waiting, int64_t *running, int64_t *finished,
+                    int64_t *free_pages);
+
+/*
  * Self-test of the attention kernels' two base-2 exponentials on n device floats:
  * out_poly[i] = the FMA-pipe polynomial path (x clamped to [-125, 127]; range
  * reduction to f in [-1/2, 1/2] plus a degree-3 minimax polynomial, relative

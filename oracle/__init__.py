@@ -9,6 +9,7 @@ Parts:
   split.py     simple and balanced micro-batch split points (pure Python integers)
   planner.py   quadratic latency model, chunk-size solver and post-processing,
                online calibration (windowed two-variable refit)
+  scheduler.py token-budget batch builder with page allocation
 Parity status of each function (what pins it) is listed in each module's header.
 """
 from __future__ import annotations
@@ -110,3 +111,4 @@ from .split import simple_split, balanced_split  # noqa: E402,F401
 from .planner import (latency_quadratic, target_latency, solve_chunk, postprocess, plan_chunks,  # noqa: E402,F401
                       fit_quadratic, fit_two_var,
                       solve_chunk_two_var, OnlineCalibrator)
+from .scheduler import Scheduler  # noqa: E402,F401

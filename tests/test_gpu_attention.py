@@ -9,7 +9,7 @@ import pytest
 
 import oracle
 import workloads as W
-from helpers import compare, oracle_caches, run_gpu_batch
+from helpers import bf16_tensor_to_f64, compare, oracle_caches, run_gpu_batch, to_dev, to_dev_bf16
 
 pytestmark = pytest.mark.gpu
 
@@ -144,3 +144,30 @@ def test_get_device_error_reads_without_clearing(cuda_lib):
     assert cuda_lib.cpp_get_device_error(err) == cuda_lib.DEV_SLOT_OUT_OF_RANGE
     assert cuda_lib.cpp_read_device_error(err, clear=True) == cuda_lib.DEV_SLOT_OUT_OF_RANGE
     assert cuda_lib.cpp_get_device_error(err) == 0
+
+
+def test_events_entry_point_on_a_mixed_batch(cuda_lib):
+    """cpp_chunked_prefill_attn_events (plain stream order, events between the kernels)
+    on decode rows plus prefills with split units: same result as the oracle."""
+    import torch
+    spec = W.BatchSpec(hist=[5000, 0, 300, 7000, 64], qlen=[1, 400, 1, 257, 1], num_q_heads=32, num_kv_heads=8,
+                       head_dim=128, page_size=16, seed=611)
+    b = W.make_batch(spec)
+
+    kc = to_dev(W.empty_cache(b).view(np.int16)).view(torch.bfloat16)
+    vc = kc.clone()
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    cuda_lib.cpp_kv_cache_write(to_dev_bf16(b.hist_k), to_dev_bf16(b.hist_v), to_dev(b.hist_slot_mapping), kc, vc, err)
+    cuda_lib.cpp_kv_cache_write(to_dev_bf16(b.k), to_dev_bf16(b.v), to_dev(b.slot_mapping), kc, vc, err)
+    B, T = len(spec.qlen), b.num_tokens
+    ws = torch.empty(cuda_lib.cpp_attn_workspace_bytes(B, T, 32, 8, 128, 8), dtype=torch.uint8, device="cuda")
+    out = torch.full((T, 32, 128), float("nan"), dtype=torch.bfloat16, device="cuda")
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(5)]
+    cuda_lib.cpp_chunked_prefill_attn_events(to_dev_bf16(b.q), kc, vc, to_dev(b.query_lens), to_dev(b.seq_lens),
+                                             to_dev(b.block_table), out, ws, err, ev, max_kv_splits=8)
+    torch.cuda.synchronize()
+    assert cuda_lib.cpp_read_device_error(err) == 0
+    assert all(ev[i].elapsed_time(ev[i + 1]) >= 0 for i in range(4))
+    okc, okv = oracle_caches(b)
+    ref = oracle.paged_attention(b.q, okc, okv, b.query_lens, b.seq_lens, b.block_table)
+    compare(bf16_tensor_to_f64(out), ref, what="events entry point")
