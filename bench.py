@@ -4,7 +4,10 @@
 Step = one pass of the whole path over the headline workload: a Llama-3-8B-shaped
 attention layer (32 q / 8 kv heads, head_dim 128, bf16, page 128) prefilling one
 32768-token sequence in 64 chunks of 512; per chunk the micro-batch split, the
-slot_mapping KV write and the causal attention over the paged cache.
+slot_mapping KV write and the causal attention over the paged cache. The KV
+write runs fused into the attention call (cpp_chunked_prefill_attn_write_kv);
+`--two-call` times the separate write and attention calls instead, and the
+line's `two_call_step` reports that variant on the same inputs.
 
 Prints one JSON line (rank 0). `value` is attention TFLOP/s of the whole step
 (algorithmic FLOPs: 4*d*Hq*sum_i (h + i + 1), unmasked pairs only) with inputs
@@ -165,10 +168,11 @@ def draw_inputs(dev, seed=2):
 class ChunkedPrefill:
     """Device buffers of the headline workload and its step."""
 
-    def __init__(self, dev, seed=2, max_kv_splits=8):
+    def __init__(self, dev, seed=2, max_kv_splits=8, fused=True):
         import torch
         import chunked_prefill_paged_slot_gb300 as cpsa
         self.torch, self.cpsa, self.dev = torch, cpsa, dev
+        self.fused = fused
         n_pages = SEQ // PAGE
         bf = torch.bfloat16
         self.q, self.k, self.v, self.slots, self.bt = draw_inputs(dev, seed)
@@ -188,6 +192,13 @@ class ChunkedPrefill:
     def chunk(self, i, q, k, v, slots, out, stream, marks=None):
         cpsa = self.cpsa
         cpsa.cpp_split_microbatch(self.qlens[i], self.split_out, 0.1, 256, stream=stream)
+        if self.fused:
+            cpsa.cpp_chunked_prefill_attn_write_kv(q, k, v, slots, self.k_cache, self.v_cache, self.qlens[i],
+                                                   self.slens[i], self.bt, out, self.ws, self.err,
+                                                   max_kv_splits=self.max_kv_splits, stream=stream,
+                                                   events=None if marks is None else
+                                                   [None, marks[0], marks[1], None, None])
+            return
         cpsa.cpp_kv_cache_write(k, v, slots, self.k_cache, self.v_cache, self.err, stream=stream)
         if marks is None:
             cpsa.cpp_chunked_prefill_attn(q, self.k_cache, self.v_cache, self.qlens[i], self.slens[i], self.bt, out,
@@ -613,6 +624,10 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-secondary", action="store_true")
     ap.add_argument("--no-suite", action="store_true")
+    ap.add_argument("--no-compare", action="store_true",
+                    help="skip timing the other variant of the step (for profiling runs)")
+    ap.add_argument("--two-call", action="store_true",
+                    help="time the KV write and the attention as two calls (default: the fused call)")
     ap.add_argument("--profile-decode", action="store_true",
                     help="only the mixed decode step with 128 decode rows (about 2.5 GB of cache), "
                          "a small case for ncu captures of the decode kernel")
@@ -640,7 +655,7 @@ def main():
     import chunked_prefill_paged_slot_gb300 as cpsa
     cpsa.load()
 
-    wl = ChunkedPrefill(dev)
+    wl = ChunkedPrefill(dev, fused=not args.two_call)
     stream = torch.cuda.current_stream(dev)
     flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)   # > L2 (129 MB)
     for _ in range(max(3, args.warmup)):
@@ -723,15 +738,37 @@ def main():
                 "per_launch_flops": per_launch_flops, "per_launch_ms": round(per_launch_ms, 4),
                 "last_chunk_ms": round(float(km[:, -1].mean()), 4),
                 "last_chunk_tflops": round(chunk_flops((N_CHUNKS - 1) * CHUNK, CHUNK) / (km[:, -1].mean() * 1e-3) / 1e12, 2)}
-    # per chunk: split, KV write, plan, chunk attention, combine (a single prefill
-    # request launches no decode kernel)
-    launches = args.steps * N_CHUNKS * 5
+    # per chunk: split, [KV write,] plan, chunk attention, combine (a single
+    # prefill request launches no decode kernel)
+    launches = args.steps * N_CHUNKS * (4 if wl.fused else 5)
+
+    # the other variant of the step (two calls, or the fused call) on the same inputs
+    other = {}
+    if rank == 0 and not args.no_compare:
+        wl.fused = not wl.fused
+        for _ in range(3):
+            wl.step(stream)
+        torch.cuda.synchronize()
+        oms = []
+        o0, o1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        for _ in range(10):
+            flush.zero_()
+            o0.record(stream)
+            wl.step(stream)
+            o1.record(stream)
+            torch.cuda.synchronize()
+            oms.append(o0.elapsed_time(o1))
+        o_ms = float(np.mean(oms))
+        other = {"ms_per_step": round(o_ms, 4), "value": round(STEP_FLOPS / (o_ms * 1e-3) / 1e12, 3),
+                 "device_flags": cpsa.cpp_read_device_error(wl.err)}
+        wl.fused = not wl.fused
 
     line = {"metric": METRIC, "value": round(value, 3), "unit": "TFLOP/s", "n_gpus": world,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_per_step, 4),
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
             "data": "synthetic (seeded N(0,1) bf16 q/k/v, permuted page pool)",
             "config": {"workload": WORKLOAD, "global_batch": world, "seq_len": SEQ, "chunk": CHUNK,
+                       "kv_write": "fused into the attention call" if wl.fused else "separate call",
                        "parallelism": "replicas" if world > 1 else "single-gpu",
                        "l2": "flushed between steps (256 MB write)", "max_kv_splits": wl.max_kv_splits,
                        "step_flops": STEP_FLOPS},
@@ -742,6 +779,8 @@ def main():
             "step_roofline": step_roofline(ms_per_step, peak_tf, peak_bw),
             "wall_s": round(wall, 3), "host_enqueue_ms_per_step": round(1e3 * float(np.mean(enqueue_s)), 3),
             "device_flags": flags}
+    if other:
+        line["fused_step" if not wl.fused else "two_call_step"] = other
     if not args.no_secondary and rank == 0:
         del wl
         torch.cuda.empty_cache()

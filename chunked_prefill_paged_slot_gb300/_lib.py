@@ -58,6 +58,12 @@ def load():
                                              _c_p, _c_p]
     lib.cpp_chunked_prefill_attn_events.restype = _c_int
     lib.cpp_chunked_prefill_attn_events.argtypes = lib.cpp_chunked_prefill_attn.argtypes + [_c_p]
+    lib.cpp_chunked_prefill_attn_write_kv.restype = _c_int
+    lib.cpp_chunked_prefill_attn_write_kv.argtypes = [_c_p, _c_p, _c_p, _c_p, _c_p, _c_p, _c_p, _c_p, _c_p, _c_int,
+                                                      _c_i64, _c_int, _c_int, _c_int, _c_int, _c_int, _c_i64, _c_f,
+                                                      _c_int, _c_p, _c_p, _c_size, _c_p, _c_p]
+    lib.cpp_chunked_prefill_attn_write_kv_events.restype = _c_int
+    lib.cpp_chunked_prefill_attn_write_kv_events.argtypes = lib.cpp_chunked_prefill_attn_write_kv.argtypes + [_c_p]
     lib.cpp_chunked_prefill_attn_noalloc.restype = _c_int
     lib.cpp_chunked_prefill_attn_noalloc.argtypes = [_c_p, _c_p, _c_p, _c_p, _c_p, _c_p, _c_int, _c_i64, _c_int,
                                                      _c_int, _c_int, _c_int, _c_int, _c_i64, _c_f, _c_int, _c_p,
@@ -195,6 +201,39 @@ def cpp_chunked_prefill_attn_events(q, k_cache, v_cache, query_lens, seq_lens, b
         _dev(out, torch.bfloat16, "out"), _dev(workspace, torch.uint8, "workspace"), workspace.numel(),
         _dev(dev_err, torch.int32, "dev_err"), _stream_ptr(stream), evs)
     _check(st, "cpp_chunked_prefill_attn_events")
+
+
+def cpp_chunked_prefill_attn_write_kv(q, k, v, slot_mapping, k_cache, v_cache, query_lens, seq_lens, block_table,
+                                      out, workspace, dev_err, scale=0.0, max_kv_splits=8, stream=None,
+                                      events=None):
+    """KV write fused into the attention: k, v [T, Hkv, d] bf16 and slot_mapping [T] int64 as for
+    cpp_kv_cache_write (the caches are written), the rest as for cpp_chunked_prefill_attn.
+    events: None, or 5 torch.cuda.Event marks (None allowed) as for cpp_chunked_prefill_attn_events."""
+    T, Hq, d = q.shape
+    pages, Hkv, P, d2 = k_cache.shape
+    B = query_lens.shape[0]
+    if out.shape != q.shape or v_cache.shape != k_cache.shape or d2 != d or seq_lens.shape != (B,) \
+            or block_table.dim() != 2 or block_table.shape[0] != B or k.shape != (T, Hkv, d) \
+            or v.shape != k.shape or slot_mapping.shape != (T,):
+        raise CpsaError("cpp_chunked_prefill_attn_write_kv: inconsistent shapes")
+    args = (_dev(q, torch.bfloat16, "q"), _dev(k, torch.bfloat16, "k"), _dev(v, torch.bfloat16, "v"),
+            _dev(slot_mapping, torch.int64, "slot_mapping"), _dev(k_cache, torch.bfloat16, "k_cache"),
+            _dev(v_cache, torch.bfloat16, "v_cache"), _dev(query_lens, torch.int32, "query_lens"),
+            _dev(seq_lens, torch.int32, "seq_lens"), _dev(block_table, torch.int32, "block_table"),
+            B, T, block_table.shape[1], Hq, Hkv, d, P, pages, float(scale), int(max_kv_splits),
+            _dev(out, torch.bfloat16, "out"), _dev(workspace, torch.uint8, "workspace"), workspace.numel(),
+            _dev(dev_err, torch.int32, "dev_err"), _stream_ptr(stream))
+    if events is None:
+        st = load().cpp_chunked_prefill_attn_write_kv(*args)
+    else:
+        if len(events) != 5:
+            raise CpsaError("cpp_chunked_prefill_attn_write_kv: events must hold 5 entries")
+        for e in events:
+            if e is not None and not e.cuda_event:
+                e.record(stream)          # torch creates its events lazily, on first record
+        evs = (_c_p * 5)(*[_c_p(e.cuda_event) if e is not None else _c_p(0) for e in events])
+        st = load().cpp_chunked_prefill_attn_write_kv_events(*args, evs)
+    _check(st, "cpp_chunked_prefill_attn_write_kv")
 
 
 def cpp_chunked_prefill_attn_noalloc(q, k_cache, v_cache, query_lens, seq_lens, block_table, out, dev_err,

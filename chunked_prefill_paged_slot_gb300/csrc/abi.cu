@@ -88,6 +88,12 @@ bool make_map4_halves(CUtensorMap *m, const void *base, int page_size, uint64_t 
 
 int nq_for_group(int group) { return (group % 2 == 0) ? 2 : 1; }
 
+int attn_impl(const void *q, const void *k_new, const void *v_new, const int64_t *slot_mapping, void *k_cache,
+              void *v_cache, const int32_t *query_lens, const int32_t *seq_lens, const int32_t *block_table,
+              int num_reqs, int64_t num_tokens, int max_blocks_per_req, int num_q_heads, int num_kv_heads,
+              int head_dim, int page_size, int64_t num_pages, float scale, int max_kv_splits, void *out,
+              void *workspace, size_t workspace_bytes, uint32_t *dev_err, void *stream, void *const *events);
+
 int check_attn_shape(int num_reqs, int64_t num_tokens, int num_q_heads, int num_kv_heads, int head_dim,
                      int max_kv_splits)
 {
@@ -184,6 +190,59 @@ int cpp_chunked_prefill_attn_events(const void *q, const void *k_cache, const vo
                                     int max_kv_splits, void *out, void *workspace, size_t workspace_bytes,
                                     uint32_t *dev_err, void *stream, void *const *events)
 {
+    return attn_impl(q, nullptr, nullptr, nullptr, const_cast<void *>(k_cache), const_cast<void *>(v_cache),
+                     query_lens, seq_lens, block_table, num_reqs, num_tokens, max_blocks_per_req, num_q_heads,
+                     num_kv_heads, head_dim, page_size, num_pages, scale, max_kv_splits, out, workspace,
+                     workspace_bytes, dev_err, stream, events);
+}
+
+int cpp_chunked_prefill_attn_write_kv(const void *q, const void *k, const void *v, const int64_t *slot_mapping,
+                                      void *k_cache, void *v_cache, const int32_t *query_lens,
+                                      const int32_t *seq_lens, const int32_t *block_table, int num_reqs,
+                                      int64_t num_tokens, int max_blocks_per_req, int num_q_heads, int num_kv_heads,
+                                      int head_dim, int page_size, int64_t num_pages, float scale, int max_kv_splits,
+                                      void *out, void *workspace, size_t workspace_bytes, uint32_t *dev_err,
+                                      void *stream)
+{
+    return cpp_chunked_prefill_attn_write_kv_events(q, k, v, slot_mapping, k_cache, v_cache, query_lens, seq_lens,
+                                                    block_table, num_reqs, num_tokens, max_blocks_per_req,
+                                                    num_q_heads, num_kv_heads, head_dim, page_size, num_pages, scale,
+                                                    max_kv_splits, out, workspace, workspace_bytes, dev_err, stream,
+                                                    nullptr);
+}
+
+int cpp_chunked_prefill_attn_write_kv_events(const void *q, const void *k, const void *v,
+                                             const int64_t *slot_mapping, void *k_cache, void *v_cache,
+                                             const int32_t *query_lens, const int32_t *seq_lens,
+                                             const int32_t *block_table, int num_reqs, int64_t num_tokens,
+                                             int max_blocks_per_req, int num_q_heads, int num_kv_heads,
+                                             int head_dim, int page_size, int64_t num_pages, float scale,
+                                             int max_kv_splits, void *out, void *workspace,
+                                             size_t workspace_bytes, uint32_t *dev_err, void *stream,
+                                             void *const *events)
+{
+    if (num_tokens > 0 && (!k || !v || !slot_mapping))
+        return CPSA_ERR_NULL_ARG;
+    if ((k && !aligned16(k)) || (v && !aligned16(v)))
+        return CPSA_ERR_MISALIGNED;
+    return attn_impl(q, k, v, slot_mapping, k_cache, v_cache, query_lens, seq_lens, block_table, num_reqs,
+                     num_tokens, max_blocks_per_req, num_q_heads, num_kv_heads, head_dim, page_size, num_pages,
+                     scale, max_kv_splits, out, workspace, workspace_bytes, dev_err, stream, events);
+}
+
+}  // extern "C"
+
+namespace {
+
+// The attention call; k_new != nullptr fuses the KV write (k_new, v_new,
+// slot_mapping non-null then).
+int attn_impl(const void *q, const void *k_new, const void *v_new, const int64_t *slot_mapping, void *k_cache,
+              void *v_cache, const int32_t *query_lens, const int32_t *seq_lens, const int32_t *block_table,
+              int num_reqs, int64_t num_tokens, int max_blocks_per_req, int num_q_heads, int num_kv_heads,
+              int head_dim, int page_size, int64_t num_pages, float scale, int max_kv_splits, void *out,
+              void *workspace, size_t workspace_bytes, uint32_t *dev_err, void *stream, void *const *events)
+{
+    const bool fused = k_new != nullptr;
     cudaEvent_t ev[5] = {nullptr, nullptr, nullptr, nullptr, nullptr};
     if (events)
         for (int i = 0; i < 5; ++i)
@@ -246,6 +305,7 @@ int cpp_chunked_prefill_attn_events(const void *q, const void *k_cache, const vo
     pp.nq = nq;
     pp.max_splits = max_kv_splits;
     pp.chunk_grid = sms < kMaxChunkGrid ? sms : kMaxChunkGrid;
+    pp.fused = fused ? 1 : 0;
     pp.prow_capacity = cap;
     pp.counts = counts;
     pp.cu_q = cu_q;
@@ -280,6 +340,12 @@ int cpp_chunked_prefill_attn_events(const void *q, const void *k_cache, const vo
     ac.part_o = part_o;
     ac.part_ml = part_ml;
     ac.dev_err = dev_err;
+    ac.fused = fused ? 1 : 0;
+    ac.k_new = k_new;
+    ac.v_new = v_new;
+    ac.slot_mapping = slot_mapping;
+    ac.k_cache_w = k_cache;
+    ac.v_cache_w = v_cache;
 
     const uint64_t D = (uint64_t)head_dim;
     const uint64_t rows_kv = (uint64_t)num_pages * (uint64_t)num_kv_heads;
@@ -288,6 +354,13 @@ int cpp_chunked_prefill_attn_events(const void *q, const void *k_cache, const vo
     if (!make_map(&tq, q, D, (uint64_t)num_q_heads, (uint64_t)num_tokens, D * 2, D * 2 * num_q_heads, 64, 1, 128) ||
         !make_map(&tk, k_cache, D, (uint64_t)page_size, rows_kv, D * 2, D * 2 * page_size, 64, pb_chunk, 1) ||
         !make_map(&tv, v_cache, D, (uint64_t)page_size, rows_kv, D * 2, D * 2 * page_size, 64, pb_chunk, 1))
+        return CPSA_ERR_CUDA;
+    // the new K/V rows, [T][Hkv][D]: 128-token boxes of one kv head (fused KV write)
+    CUtensorMap tkn = tk, tvn = tv;
+    if (fused && (!make_map(&tkn, k_new, D, (uint64_t)num_kv_heads, (uint64_t)num_tokens, D * 2,
+                            D * 2 * num_kv_heads, 64, 1, 128) ||
+                  !make_map(&tvn, v_new, D, (uint64_t)num_kv_heads, (uint64_t)num_tokens, D * 2,
+                            D * 2 * num_kv_heads, 64, 1, 128)))
         return CPSA_ERR_CUDA;
     // decode: one box per page-head block (at most 64 rows) covering all of head_dim
     const uint32_t pb_dec = page_size < kDecodeChunk ? page_size : kDecodeChunk;
@@ -309,7 +382,7 @@ int cpp_chunked_prefill_attn_events(const void *q, const void *k_cache, const vo
     const bool single_prefill = num_reqs == 1 && num_tokens >= 2;
     const bool single_decode = num_reqs == 1 && num_tokens == 1;
     const int grid_c = single_decode ? 0 : pp.chunk_grid;   // one stream-K run per CTA
-    if (grid_c > 0 && launch_chunk_attn(cp, tq, tk, tv, head_dim, nq, grid_c, s, early) != cudaSuccess)
+    if (grid_c > 0 && launch_chunk_attn(cp, tq, tk, tv, tkn, tvn, head_dim, nq, grid_c, s, early) != cudaSuccess)
         return CPSA_ERR_CUDA;
     mark(2, s);
 
@@ -333,6 +406,10 @@ int cpp_chunked_prefill_attn_events(const void *q, const void *k_cache, const vo
     mark(4, s);
     return CPSA_OK;
 }
+
+}  // namespace
+
+extern "C" {
 
 int cpp_split_microbatch(const int32_t *query_lens, int num_reqs, float balance_threshold, int32_t length_threshold,
                          int32_t *out3, void *stream)

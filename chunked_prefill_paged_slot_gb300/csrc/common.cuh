@@ -101,6 +101,31 @@ __device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, volati
     }
 }
 
+// mbar_wait for warps off the critical path: sleeps between polls so that the
+// waiting warp leaves the issue slots of its SM sub-partition to the warps that
+// share it. Same limits and result as mbar_wait.
+__device__ __forceinline__ bool mbar_wait_sleep(uint64_t *bar, uint32_t parity, volatile int *abort,
+                                                uint32_t sleep_ns = 256)
+{
+    uint64_t t0 = 0;
+    for (uint32_t it = 0;; ++it) {
+        if (mbar_try_wait(bar, parity))
+            return true;
+        __nanosleep(sleep_ns);
+        if ((it & 7u) == 7u) {
+            if (*abort)
+                return false;
+            const uint64_t now = global_timer_ns();
+            if (t0 == 0) {
+                t0 = now;
+            } else if (now - t0 > kWaitLimitNs) {
+                *abort = 1;
+                return false;
+            }
+        }
+    }
+}
+
 // ---------------------------------------------------------------------------
 // TMA: tiled tensor loads into shared memory, completion on an mbarrier
 // ---------------------------------------------------------------------------
@@ -126,6 +151,28 @@ __device__ __forceinline__ void tma_load_4d(void *smem_dst, const CUtensorMap *m
                  "l"(reinterpret_cast<uint64_t>(map)), "r"(smem_u32(bar)), "r"(c0), "r"(c1), "r"(c2), "r"(c3)
                  : "memory");
 }
+
+// Tiled tensor store of a box from shared memory (same swizzle as the map's
+// loads) to global memory, tracked by this thread's bulk async-groups.
+__device__ __forceinline__ void tma_store_3d(const CUtensorMap *map, const void *smem_src, int c0, int c1, int c2)
+{
+    asm volatile("cp.async.bulk.tensor.3d.global.shared::cta.bulk_group [%0, {%2, %3, %4}], [%1];" ::"l"(
+                     reinterpret_cast<uint64_t>(map)),
+                 "r"(smem_u32(smem_src)), "r"(c0), "r"(c1), "r"(c2)
+                 : "memory");
+}
+
+__device__ __forceinline__ void bulk_commit_group() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
+
+// Wait until the shared-memory sources of this thread's committed bulk stores
+// have been read (the buffers may then be reused).
+__device__ __forceinline__ void bulk_wait_group_read0()
+{
+    asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
+}
+
+// Wait until this thread's committed bulk stores have completed.
+__device__ __forceinline__ void bulk_wait_group0() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
 
 // Untiled bulk copy of `bytes` (multiple of 16, both addresses 16-byte aligned)
 // from global to shared memory, completion counted on the mbarrier.

@@ -22,6 +22,10 @@
 //              once its group's four warps are done with it.
 // At the end of an item the four warps merge (max, sum, O) through shared
 // memory and write the bf16 row, or an fp32 partial when the row is split.
+// With the KV write fused, the row's own key (the last of its context) is not
+// in the cache yet: the producer lands the stage holding it, overwrites that row
+// in shared memory with the new K and V rows, stores the same bytes to the
+// cache slot slot_mapping names, and only then releases the stage.
 #include "common.cuh"
 #include "kernels.cuh"
 #include "plan.cuh"
@@ -54,6 +58,7 @@ struct DecCfg {
 
 struct DecBars {
     uint64_t full[10], empty[10];
+    uint64_t patch;   // fused KV write: copies of the stage that gets the new row
     int abort;
 };
 
@@ -116,6 +121,7 @@ decode_attn_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap tm_
             mbar_init(&bars->full[s], 1);
             mbar_init(&bars->empty[s], 4);
         }
+        mbar_init(&bars->patch, 1);
         bars->abort = 0;
         fence_barrier_init();
     }
@@ -134,12 +140,15 @@ decode_attn_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap tm_
         }
         const int PB = p.page_size < kKC ? p.page_size : kKC;
         const int NB = kKC / PB;
+        const int lg = 31 - __clz(PB);
         const uint32_t box_bytes = (uint32_t)PB * C::kRowBytes;
-        uint32_t g = 0;
+        uint32_t g = 0, patch_uses = 0;
         bool stop = false;
         for (int it = blockIdx.x; it < n_items && !stop && !*abort; it += gridDim.x) {
             const DecodeItem w = p.ditems[it];
             const int32_t *bt_row = p.block_table + (int64_t)w.r * p.max_blocks;
+            // the row's own key, when this item's range ends with it and the KV write is fused
+            const int knew = (p.fused && w.key1 == p.seq_lens[w.r]) ? w.key1 - 1 : -1;
             // page numbers of the next kLookahead stages stay in flight in registers
             // (lane j < NB holds box j of a stage), so the block_table latency is
             // paid once per item rather than once per stage
@@ -172,8 +181,10 @@ decode_attn_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap tm_
                 const uint32_t bytes = (uint32_t)__popc(vmask) * box_bytes * 2;
                 uint8_t *kdst = smem + stage * C::kStageBytes;
                 uint8_t *vdst = kdst + C::kTileBytes;
+                const bool patch = knew >= c0 && knew < c0 + kKC;
+                uint64_t *bar = patch ? &bars->patch : &bars->full[stage];
                 if (lane == 0)
-                    mbar_arrive_expect_tx(&bars->full[stage], bytes);
+                    mbar_arrive_expect_tx(bar, bytes);
                 for (int j = 0; j < NB; ++j) {
                     const int pj = __shfl_sync(0xffffffffu, page, j);
                     const int oj = __shfl_sync(0xffffffffu, off, j);
@@ -181,13 +192,45 @@ decode_attn_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap tm_
                         // rows [oj, oj + PB) of page-head block (pj, kvh), both halves in one box
                         const int z = pj * p.num_kv_heads + w.kvh;
                         if (C::kHalves == 2) {
-                            tma_load_4d(kdst + j * box_bytes, &tm_k, &bars->full[stage], 0, oj, 0, z);
-                            tma_load_4d(vdst + j * box_bytes, &tm_v, &bars->full[stage], 0, oj, 0, z);
+                            tma_load_4d(kdst + j * box_bytes, &tm_k, bar, 0, oj, 0, z);
+                            tma_load_4d(vdst + j * box_bytes, &tm_v, bar, 0, oj, 0, z);
                         } else {
-                            tma_load_3d(kdst + j * box_bytes, &tm_k, &bars->full[stage], 0, oj, z);
-                            tma_load_3d(vdst + j * box_bytes, &tm_v, &bars->full[stage], 0, oj, z);
+                            tma_load_3d(kdst + j * box_bytes, &tm_k, bar, 0, oj, z);
+                            tma_load_3d(vdst + j * box_bytes, &tm_v, bar, 0, oj, z);
                         }
                     }
+                }
+                if (patch) {
+                    if (!mbar_wait(&bars->patch, patch_uses & 1u, abort)) {
+                        stop = true;
+                        break;
+                    }
+                    ++patch_uses;
+                    // lanes 0..D/8-1: 16-byte chunks of the K row; lanes 16..16+D/8-1: of the V row
+                    const int which = lane >> 4, ch = lane & 15;
+                    if (ch < D / 8) {
+                        const int rr = knew - c0;
+                        const int64_t src = ((int64_t)w.t * p.num_kv_heads + w.kvh) * (D / 8) + ch;
+                        const uint4 val = __ldg(reinterpret_cast<const uint4 *>(which ? p.v_new : p.k_new) + src);
+                        uint8_t *tile = which ? vdst : kdst;
+                        *reinterpret_cast<uint4 *>(tile + half_row_off<D>(rr, ch >> 3, lg) +
+                                                   (((ch & 7) ^ (rr & 7)) << 4)) = val;
+                        const int64_t slot = __ldg(p.slot_mapping + w.t);
+                        if (slot >= 0) {
+                            if (slot < p.num_pages * (int64_t)p.page_size) {
+                                const int lg_p = __ffs(p.page_size) - 1;   // page_size is a power of two
+                                const int64_t pg = slot >> lg_p, po = slot & (p.page_size - 1);
+                                reinterpret_cast<uint4 *>(which ? p.v_cache_w : p.k_cache_w)
+                                    [((pg * p.num_kv_heads + w.kvh) * p.page_size + po) * (D / 8) + ch] = val;
+                            } else if (lane == 0) {
+                                set_dev_error(p.dev_err, CPSA_DEV_SLOT_OUT_OF_RANGE);
+                            }
+                        }
+                    }
+                    fence_proxy_async_smem();   // the patch before later copies into this stage
+                    __syncwarp();
+                    if (lane == 0)
+                        mbar_arrive(&bars->full[stage]);
                 }
             }
         }

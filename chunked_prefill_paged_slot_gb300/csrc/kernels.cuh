@@ -25,6 +25,13 @@ struct AttnCommon {
     float *part_o;             // fp32 [rows][D] partial outputs of split rows
     float *part_ml;            // fp32 [rows][2]  (max in log2 units, row sum)
     uint32_t *dev_err;
+    // KV write fused into the attention (fused != 0): the new tokens' keys and
+    // values are read from k_new / v_new rather than from the cache, and each is
+    // also stored, once, to the cache slot slot_mapping names
+    int fused;
+    const void *k_new, *v_new;         // bf16 [T][Hkv][D]
+    const int64_t *slot_mapping;       // [T]
+    void *k_cache_w, *v_cache_w;       // bf16 [pages][Hkv][P][D], written
 };
 
 struct ChunkParams : AttnCommon {
@@ -49,8 +56,10 @@ struct CombineParams {
 };
 
 // early: launch with programmatic dependent launch (see launch_pdl)
+// tkn / tvn: maps over k_new / v_new (used when p.fused)
 cudaError_t launch_chunk_attn(const ChunkParams &p, const CUtensorMap &tq, const CUtensorMap &tk,
-                              const CUtensorMap &tv, int head_dim, int nq, int grid, cudaStream_t s, bool early);
+                              const CUtensorMap &tv, const CUtensorMap &tkn, const CUtensorMap &tvn, int head_dim,
+                              int nq, int grid, cudaStream_t s, bool early);
 cudaError_t launch_decode_attn(const DecodeParams &p, const CUtensorMap &tk, const CUtensorMap &tv, int head_dim,
                                int grid, cudaStream_t s, bool early);
 cudaError_t launch_combine(const CombineParams &p, int head_dim, int grid, cudaStream_t s, bool early);

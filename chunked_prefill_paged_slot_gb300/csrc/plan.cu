@@ -41,6 +41,13 @@ __device__ Req load_req(const PlanParams &p, int r)
     return q;
 }
 
+// KV tiles of one unit of query tile qt (rows [128 qt, 128 qt + rows)); see the
+// tile grids in plan.cuh.
+__device__ __forceinline__ int unit_tiles(const PlanParams &p, const Req &rq, int qt, int rows)
+{
+    return p.fused ? ceil_div(rq.hist, kTileN) + qt + 1 : ceil_div(rq.hist + qt * kTileM + rows, kTileN);
+}
+
 // KV tiles of all prefill units of one request (0 for decode / invalid / empty).
 __device__ int prefill_tiles(const PlanParams &p, const Req &rq)
 {
@@ -48,10 +55,8 @@ __device__ int prefill_tiles(const PlanParams &p, const Req &rq)
         return 0;
     const int units_per_qtile = p.Hkv * (p.group / p.nq);
     int tiles = 0;
-    for (int i0 = 0; i0 < rq.q; i0 += kTileM) {
-        const int rows = min(kTileM, rq.q - i0);
-        tiles += ceil_div(rq.hist + i0 + rows, kTileN) * units_per_qtile;
-    }
+    for (int qt = 0; qt * kTileM < rq.q; ++qt)
+        tiles += unit_tiles(p, rq, qt, min(kTileM, rq.q - qt * kTileM)) * units_per_qtile;
     return tiles;
 }
 
@@ -125,7 +130,7 @@ __device__ Counts request_work(const PlanParams &p, int r, const Req &rq, int ti
     for (int qt = nqt - 1; qt >= 0; --qt) {
         const int i0 = qt * kTileM;
         const int rows = min(kTileM, rq.q - i0);
-        const int nkv = ceil_div(rq.hist + i0 + rows, kTileN);
+        const int nkv = unit_tiles(p, rq, qt, rows);
         for (int jb = 0; jb < upq; jb += 32) {
             const int j = jb + lane;
             const bool active = j < upq;

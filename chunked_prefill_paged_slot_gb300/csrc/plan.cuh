@@ -24,6 +24,12 @@ namespace cpsa {
 // results the combine kernel merges. Every CTA gets the same amount of work.
 // Decode: a row splits into pieces of kDecodeKeysPerSplit keys (at most
 // max_kv_splits), depending only on its own length.
+// KV tiles of a unit: tile kt holds keys [128 kt, 128 kt + 128). With the KV
+// write fused, the history (keys below h) keeps that grid, its last tile cut at
+// h, and the chunk's own keys form tiles of their own starting at h, so that
+// they come from the new K/V rows: tile ceil(h / 128) + j holds keys
+// [h + 128 j, h + 128 j + 128), and the unit of query tile i has ceil(h / 128) +
+// i + 1 tiles (the same count whenever h is a multiple of 128).
 constexpr int kMinRunTiles = 4;             // shortest run of KV tiles per CTA
 constexpr int kMaxChunkGrid = 256;          // upper bound of the chunk kernel's grid (SMs)
 constexpr int kDecodeChunk = 64;            // keys per decode pipeline stage
@@ -119,6 +125,7 @@ struct PlanParams {
     int Hq, Hkv, group, nq;    // nq: q heads per chunk-kernel CTA (1 or 2)
     int max_splits;
     int chunk_grid;            // CTAs of the chunk kernel (stream-K runs)
+    int fused;                 // KV write fused: the chunk's own keys form tiles of their own
     int64_t prow_capacity;     // partial rows that fit
     int32_t *counts;
     int32_t *cu_q;

@@ -6,13 +6,15 @@
 // attention; metadata from the "Ascend dual-stream parallel" article, section
 // 3.1): for a 128-row tile of one request's new tokens and NQ q heads that share
 // one kv head, softmax(scale * Q K^T) V over the keys 0 .. h_r + i of every row i,
-// the history keys and the chunk's own keys alike read from the cache pages
-// listed in block_table.
+// the history keys read from the cache pages listed in block_table. The chunk's
+// own keys come from the cache too, or, with the KV write fused (the KV write
+// of the dual-stream article's section 3.1 folded into this kernel), straight
+// from the new K/V rows, each tile of them also stored once to its cache slots.
 //
-// CTA layout (320 threads, one CTA per SM, persistent over prefill items):
+// CTA layout (352 threads, one CTA per SM, persistent over prefill items):
 //   warp 8       TMA producer: Q tiles once per item, then K_j, V_j into a ring
 //                of shared-memory slots; block_table lookups; zeroes the value
-//                rows past seq_len in the last tile (they may hold anything).
+//                rows past the tile's last key (they may hold anything).
 //   warp 9       tcgen05 issuer (one elected lane per instruction, the warp
 //                converged): S_n = Q_n K_j^T into TMEM, then O_n += P_n V_j with
 //                P_n read from TMEM; TMEM alloc/dealloc.
@@ -20,6 +22,12 @@
 //                S row from TMEM, causal mask on the diagonal/tail tiles, online
 //                max/sum in fp32 (base-2 exponent, scale folded in), P as bf16
 //                back into TMEM over S; final O / l epilogue.
+//   warp 10      cache writer (fused KV write only): for each tile of new rows
+//                this CTA owns (the diagonal tile of head pair 0), TMA-loads its
+//                K and then its V rows into a staging buffer of its own and
+//                TMA-stores them to the cache pages slot_mapping names, apart
+//                from the attention pipeline (rows whose slots do not form whole
+//                page boxes are stored row by row).
 // Exponentials: in tiles without masked columns kFmaExpPairsPer8 of every 8
 // pairs go to the FMA pipe (exp2_poly_x2), the rest to MUFU ex2, so neither unit
 // sets the pace alone; the row sum and the exponent arguments use packed f32x2 arithmetic.
@@ -49,11 +57,14 @@ struct ChunkCfg {
     static constexpr int kSlots = D == 128 ? 4 : 8;
     static constexpr int kQOff = 0;
     static constexpr int kSlotOff = NQ * kTileBytes;
-    static constexpr int kBarOff = kSlotOff + kSlots * kTileBytes;
+    static constexpr int kStageOff = kSlotOff + kSlots * kTileBytes;   // the cache writer's buffer
+    static constexpr int kBarOff = kStageOff + kTileBytes;
     static constexpr int kSmemBytes = kBarOff + 1024 + 1024;   // barriers + alignment slack
-    static constexpr int kThreads = 320;
+    static_assert(kSmemBytes <= 232448, "beyond the 227 KB of shared memory a CTA may have");
+    static constexpr int kThreads = 352;
     static constexpr int kLoadWarp = 8;
     static constexpr int kMmaWarp = 9;
+    static constexpr int kWriteWarp = 10;
     static constexpr uint32_t kTmemCols = 512;
     __host__ __device__ static constexpr uint32_t s_col(int n) { return (uint32_t)n * 128u; }
     __host__ __device__ static constexpr uint32_t o_col(int n) { return 256u + (uint32_t)n * D; }
@@ -63,15 +74,67 @@ struct ChunkBars {
     uint64_t q_full, q_empty, tail, drain;
     uint64_t s_full[2], p_full[2], o_done[2];
     uint64_t slot_full[8], slot_empty[8];
+    uint64_t stage;        // fused KV write: the writer's buffer is loaded
     uint32_t tmem_base;
     int abort;
     int it_begin, it_end;    // this CTA's run of pieces
 };
 
+// Cache stores of one staged K or V tile of new rows (128 rows, 128-byte
+// swizzled 64-column halves), rows [0, rows) to the slots sl of kv head kvh (lane
+// l holds the slots of rows l, l + 32, l + 64, l + 96). The tile is cut into
+// boxes of PB = min(page_size, 128) rows; a box whose rows are valid tokens with
+// consecutive slots inside one page is stored by TMA through the cache's own
+// tensor map (box_mask bit j, box start slots in s0), the rest row by row from
+// shared memory (lane = row, no shuffles). Negative slots are padding; slots past
+// the cache set the error flag. Lane 0 commits the TMA stores as one bulk group.
+template <int D>
+__device__ __forceinline__ void store_tile_rows(const ChunkParams &p, const CUtensorMap *map, const uint8_t *tile,
+                                                void *cache, int kvh, int rows, const int64_t (&sl)[4],
+                                                uint32_t box_mask, const int64_t *s0, int PB, int lane,
+                                                bool flag_errors)
+{
+    constexpr int CPR = D / 8;        // 16-byte chunks per row
+    const int lg_p = __ffs(p.page_size) - 1;   // page_size is a power of two
+    const int64_t n_slots = p.num_pages * (int64_t)p.page_size;
+    if (lane == 0) {
+        for (int j = 0; j < 128 / PB; ++j) {
+            if (!((box_mask >> j) & 1u))
+                continue;
+            const int off = (int)(s0[j] & (p.page_size - 1));
+            const int z = (int)((s0[j] >> lg_p) * p.num_kv_heads + kvh);
+#pragma unroll
+            for (int c = 0; c < D / 64; ++c)
+                tma_store_3d(map, tile + c * (128 * 128) + j * PB * 128, c * 64, off, z);
+        }
+        bulk_commit_group();
+    }
+    uint4 *dst_base = reinterpret_cast<uint4 *>(cache);
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+        const int row = lane + 32 * q;
+        const int64_t slot = sl[q];
+        if (row >= rows || slot < 0 || ((box_mask >> (row / PB)) & 1u))
+            continue;
+        if (slot >= n_slots) {
+            if (flag_errors)
+                set_dev_error(p.dev_err, CPSA_DEV_SLOT_OUT_OF_RANGE);
+            continue;
+        }
+        uint4 *dst = dst_base + (((slot >> lg_p) * p.num_kv_heads + kvh) * p.page_size +
+                                 (slot & (p.page_size - 1))) * CPR;
+#pragma unroll 4
+        for (int ch = 0; ch < CPR; ++ch)
+            dst[ch] = *reinterpret_cast<const uint4 *>(tile + (ch >> 3) * (128 * 128) + row * 128 +
+                                                       (((ch & 7) ^ (row & 7)) << 4));
+    }
+}
+
 template <int D, int NQ>
-__global__ void __launch_bounds__(320, 1)
+__global__ void __launch_bounds__(352, 1)
 chunk_attn_kernel(const ChunkParams p, const __grid_constant__ CUtensorMap tm_q,
-                  const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v)
+                  const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
+                  const __grid_constant__ CUtensorMap tm_kn, const __grid_constant__ CUtensorMap tm_vn)
 {
     using C = ChunkCfg<D, NQ>;
     extern __shared__ uint8_t smem_raw[];
@@ -92,6 +155,7 @@ chunk_attn_kernel(const ChunkParams p, const __grid_constant__ CUtensorMap tm_q,
             mbar_init(&bars->slot_full[s], 1);
             mbar_init(&bars->slot_empty[s], 1);
         }
+        mbar_init(&bars->stage, 1);
         bars->abort = 0;
         fence_barrier_init();
     }
@@ -99,6 +163,10 @@ chunk_attn_kernel(const ChunkParams p, const __grid_constant__ CUtensorMap tm_q,
         tma_prefetch_desc(&tm_q);
         tma_prefetch_desc(&tm_k);
         tma_prefetch_desc(&tm_v);
+        if (p.fused) {
+            tma_prefetch_desc(&tm_kn);
+            tma_prefetch_desc(&tm_vn);
+        }
     }
     if (warp == C::kMmaWarp) {
         tmem_alloc(&bars->tmem_base, C::kTmemCols);
@@ -131,6 +199,11 @@ chunk_attn_kernel(const ChunkParams p, const __grid_constant__ CUtensorMap tm_q,
             const int h0 = kvh * p.group + hp * NQ;
             const int cu = p.cu_q[w.r];
             const int s_len = p.seq_lens[w.r];
+            const int hist = s_len - p.query_lens[w.r];
+            // tiles [0, nh) come from the cache, over keys [0, hist_end); the rest
+            // (fused KV write) from the new rows
+            const int nh = p.fused ? (hist + 127) / 128 : 0x7fffffff;
+            const int hist_end = p.fused ? hist : s_len;
             if (q_uses > 0 && !mbar_wait(&bars->q_empty, (q_uses - 1) & 1, abort))
                 break;
             if (lane == 0) {
@@ -147,26 +220,30 @@ chunk_attn_kernel(const ChunkParams p, const __grid_constant__ CUtensorMap tm_q,
             auto lookup = [&](int kt) -> int {
                 int pg = -1;
                 const int key = kt * 128 + lane * PB;
-                if (lane < NB && kt < w.kt1 && key < s_len)
+                if (lane < NB && kt < w.kt1 && kt < nh && key < hist_end)
                     pg = __ldg(bt_row + key / p.page_size);
                 return pg;
             };
             int next_page = lookup(w.kt0);
             bool stop = false;
             for (int kt = w.kt0; kt < w.kt1 && !stop; ++kt) {
-                const int key0 = kt * 128;
+                const bool from_new = kt >= nh;
+                const int key0 = from_new ? hist + (kt - nh) * 128 : kt * 128;
+                const int key_end = from_new ? s_len : hist_end;   // keys [key0, key_end) are used
                 const int page = next_page;
                 next_page = lookup(kt + 1);
                 const int off = (key0 + lane * PB) % p.page_size;
                 bool valid = false;
-                if (lane < NB && key0 + lane * PB < s_len) {
+                if (!from_new && lane < NB && key0 + lane * PB < key_end) {
                     valid = page >= 0 && page < p.num_pages;
                     if (!valid)
                         set_dev_error(p.dev_err, CPSA_DEV_PAGE_OUT_OF_RANGE);
                 }
                 const uint32_t vmask = __ballot_sync(0xffffffffu, valid);
-                const uint32_t bytes = (uint32_t)__popc(vmask) * box_bytes * C::kHalves;
-                const bool tail = key0 + 128 > s_len;
+                // a box of new rows is always whole (rows past the last token read as zero)
+                const uint32_t bytes =
+                    from_new ? (uint32_t)C::kTileBytes : (uint32_t)__popc(vmask) * box_bytes * C::kHalves;
+                const bool tail = key0 + 128 > key_end;
                 for (int kv = 0; kv < 2 && !stop; ++kv) {
                     const int slot = slot_it % C::kSlots;
                     if (slot_it >= (uint32_t)C::kSlots &&
@@ -175,28 +252,36 @@ chunk_attn_kernel(const ChunkParams p, const __grid_constant__ CUtensorMap tm_q,
                         break;
                     }
                     uint8_t *dst = smem + C::kSlotOff + slot * C::kTileBytes;
-                    const CUtensorMap *map = kv == 0 ? &tm_k : &tm_v;
                     const bool fix = kv == 1 && tail;
                     uint64_t *bar = fix ? &bars->tail : &bars->slot_full[slot];
                     if (lane == 0)
                         mbar_arrive_expect_tx(bar, bytes);
-                    for (int j = 0; j < NB; ++j) {
-                        int pj = __shfl_sync(0xffffffffu, page, j);
-                        int oj = __shfl_sync(0xffffffffu, off, j);
-                        if (lane == 0 && ((vmask >> j) & 1u))
+                    if (from_new) {
+                        // rows of tokens cu + key0 - hist .. + 127, kv head kvh
+                        const CUtensorMap *map = kv == 0 ? &tm_kn : &tm_vn;
+                        if (lane == 0)
                             for (int c = 0; c < C::kHalves; ++c)
-                                tma_load_3d(dst + c * C::kHalfBytes + j * box_bytes, map, bar, c * 64,
-                                            oj, pj * p.num_kv_heads + kvh);
+                                tma_load_3d(dst + c * C::kHalfBytes, map, bar, c * 64, kvh, cu + key0 - hist);
+                    } else {
+                        const CUtensorMap *map = kv == 0 ? &tm_k : &tm_v;
+                        for (int j = 0; j < NB; ++j) {
+                            int pj = __shfl_sync(0xffffffffu, page, j);
+                            int oj = __shfl_sync(0xffffffffu, off, j);
+                            if (lane == 0 && ((vmask >> j) & 1u))
+                                for (int c = 0; c < C::kHalves; ++c)
+                                    tma_load_3d(dst + c * C::kHalfBytes + j * box_bytes, map, bar, c * 64,
+                                                oj, pj * p.num_kv_heads + kvh);
+                        }
                     }
                     if (fix) {
-                        // value rows >= seq_len must be zero: P is zero there, but the
+                        // value rows >= key_end must be zero: P is zero there, but the
                         // bytes may be NaN and 0 * NaN would poison the row sums.
                         if (!mbar_wait(&bars->tail, tail_uses & 1, abort)) {
                             stop = true;
                             break;
                         }
                         ++tail_uses;
-                        const int first = s_len - key0;   // 1 .. 127
+                        const int first = key_end - key0;   // 1 .. 127
                         const int nchunks = (128 - first) * 8;   // 16-byte chunks per half
                         for (int c = 0; c < C::kHalves; ++c)
                             for (int x = lane; x < nchunks; x += 32) {
@@ -213,6 +298,101 @@ chunk_attn_kernel(const ChunkParams p, const __grid_constant__ CUtensorMap tm_q,
             }
             if (stop)
                 break;
+        }
+    } else if (warp == C::kWriteWarp) {
+        // ------------------------------------------------------------ cache writer
+        // Independent of the attention pipeline: it reads the new rows itself,
+        // one K or V tile at a time, through its own buffer and barrier.
+        if (p.fused) {
+            uint8_t *stage = smem + C::kStageOff;
+            uint32_t stage_uses = 0;
+            bool ok = true;
+            for (int it = it_begin; it < it_end && ok && !*abort; ++it) {
+                const PrefillItem w = p.pitems[it];
+                const int kvh = w.kvh_hp & 0xFFFF, hp = w.kvh_hp >> 16;
+                const int q_len = p.query_lens[w.r];
+                const int hist = p.seq_lens[w.r] - q_len;
+                const int kd = hp == 0 ? (hist + 127) / 128 + w.i0 / 128 : -1;
+                if (kd < w.kt0 || kd >= w.kt1)
+                    continue;
+                const int rows = min(128, q_len - w.i0);
+                const int t0 = p.cu_q[w.r] + w.i0;
+                int64_t sl[4];
+#pragma unroll
+                for (int q = 0; q < 4; ++q) {
+                    const int row = lane + 32 * q;
+                    sl[q] = row < rows ? __ldg(p.slot_mapping + t0 + row) : -1;
+                }
+                // which boxes of PB rows go whole by TMA: valid rows, slots
+                // consecutive from a box start that leaves the box inside its page
+                const int PB = p.page_size < 128 ? p.page_size : 128;
+                const int64_t n_slots = p.num_pages * (int64_t)p.page_size;
+                uint32_t okm[4];
+#pragma unroll
+                for (int q = 0; q < 4; ++q) {
+                    const int row = lane + 32 * q;
+                    const int64_t sv = sl[q];
+                    int64_t prev = __shfl_up_sync(0xffffffffu, sv, 1);
+                    const int64_t wrap = __shfl_sync(0xffffffffu, q > 0 ? sl[q > 0 ? q - 1 : 0] : -2, 31);
+                    if (lane == 0)
+                        prev = wrap;
+                    bool good = row < rows && sv >= 0 && sv < n_slots;
+                    if (row % PB == 0)
+                        good = good && (sv & (p.page_size - 1)) + PB <= p.page_size;
+                    else
+                        good = good && sv == prev + 1;
+                    okm[q] = __ballot_sync(0xffffffffu, good);
+                }
+                uint32_t box_mask = 0;
+                int64_t s0[16];
+#pragma unroll
+                for (int j = 0; j < 16; ++j) {
+                    if (j < 128 / PB) {
+                        const int r0 = j * PB;
+                        const int q0 = r0 >> 5;
+                        bool whole;
+                        if (PB >= 32) {
+                            whole = true;
+                            for (int q = q0; q < ((r0 + PB) >> 5); ++q)
+                                whole = whole && okm[q] == 0xffffffffu;
+                        } else {
+                            const uint32_t m = ((1u << PB) - 1u) << (r0 & 31);
+                            whole = (okm[q0] & m) == m;
+                        }
+                        const int64_t mine = q0 == 0 ? sl[0] : q0 == 1 ? sl[1] : q0 == 2 ? sl[2] : sl[3];
+                        s0[j] = __shfl_sync(0xffffffffu, mine, r0 & 31);
+                        box_mask |= (whole ? 1u : 0u) << j;
+                    }
+                }
+                for (int kv = 0; kv < 2 && ok; ++kv) {
+                    if (lane == 0) {
+                        mbar_arrive_expect_tx(&bars->stage, C::kTileBytes);
+                        for (int c = 0; c < C::kHalves; ++c)
+                            tma_load_3d(stage + c * C::kHalfBytes, kv == 0 ? &tm_kn : &tm_vn, &bars->stage, c * 64,
+                                        kvh, t0);
+                    }
+                    ok = __all_sync(0xffffffffu, mbar_wait_sleep(&bars->stage, stage_uses & 1u, abort));
+                    if (!ok) {
+                        // let the copy in flight land before the CTA can end
+                        if (lane == 0) {
+                            const uint64_t ts = global_timer_ns();
+                            while (!mbar_try_wait(&bars->stage, stage_uses & 1u) &&
+                                   global_timer_ns() - ts < 100000000ull) {
+                            }
+                        }
+                        break;
+                    }
+                    ++stage_uses;
+                    store_tile_rows<D>(p, kv == 0 ? &tm_k : &tm_v, stage, kv == 0 ? p.k_cache_w : p.v_cache_w, kvh,
+                                       rows, sl, box_mask, s0, PB, lane, kv == 0);
+                    if (lane == 0)
+                        bulk_wait_group_read0();   // the TMA stores have read the buffer
+                    fence_proxy_async_smem();      // and so have this warp's row copies, before the next load
+                    __syncwarp();
+                }
+            }
+            if (lane == 0)
+                bulk_wait_group0();   // the cache stores are complete before the CTA ends
         }
     } else if (warp == C::kMmaWarp) {
         // ------------------------------------------------------------ MMA issuer
@@ -344,11 +524,18 @@ chunk_attn_kernel(const ChunkParams p, const __grid_constant__ CUtensorMap tm_q,
             const int hist = s_len - q_len;
             const int i = w.i0 + row;
             const int limit = min(hist + i, s_len - 1);   // last visible key of this row
+            // with the KV write fused, tiles from nh on hold the chunk's own keys
+            // from key hist on, and the cache tiles before them end at hist
+            const int nh = p.fused ? (hist + 127) / 128 : 0x7fffffff;
+            const int limit_hist = p.fused ? hist - 1 : limit;
             const int n = w.kt1 - w.kt0;
             float m_use = -INFINITY, l = 0.f;
             bool ok = true;
             for (int t = 0; t < n; ++t) {
-                const int key0 = (w.kt0 + t) * 128;
+                const int kt = w.kt0 + t;
+                const bool from_new = kt >= nh;
+                const int key0 = from_new ? hist + (kt - nh) * 128 : kt * 128;
+                const int lim = from_new ? limit : limit_hist;
                 if (!(ok = mbar_wait(&bars->s_full[wg], s_uses & 1, abort)))
                     break;
                 ++s_uses;
@@ -360,11 +547,11 @@ chunk_attn_kernel(const ChunkParams p, const __grid_constant__ CUtensorMap tm_q,
                 tmem_wait_ld();
 #define SV(x) __uint_as_float(sr[(x) >> 5][(x) & 31])
                 // causal / tail mask: only tiles that reach past some row's last key
-                const bool masked = __any_sync(0xffffffffu, key0 + 127 > limit);
+                const bool masked = __any_sync(0xffffffffu, key0 + 127 > lim);
                 if (masked) {
 #pragma unroll
                     for (int x = 0; x < 128; ++x)
-                        if (key0 + x > limit) sr[x >> 5][x & 31] = 0xff800000u;   // -inf
+                        if (key0 + x > lim) sr[x >> 5][x & 31] = 0xff800000u;   // -inf
                 }
                 // row max as 4 independent fmax3 chains joined at the end (short latency)
                 float mc[4];
@@ -498,24 +685,28 @@ chunk_attn_kernel(const ChunkParams p, const __grid_constant__ CUtensorMap tm_q,
 
 template <int D, int NQ>
 cudaError_t launch_chunk_t(const ChunkParams &p, const CUtensorMap &tq, const CUtensorMap &tk,
-                           const CUtensorMap &tv, int grid, cudaStream_t s, bool early)
+                           const CUtensorMap &tv, const CUtensorMap &tkn, const CUtensorMap &tvn, int grid,
+                           cudaStream_t s, bool early)
 {
     using C = ChunkCfg<D, NQ>;
     auto k = chunk_attn_kernel<D, NQ>;
     cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
     if (e != cudaSuccess)
         return e;
-    return launch_pdl(early, k, dim3(grid), dim3(C::kThreads), C::kSmemBytes, s, p, tq, tk, tv);
+    return launch_pdl(early, k, dim3(grid), dim3(C::kThreads), C::kSmemBytes, s, p, tq, tk, tv, tkn, tvn);
 }
 
 }  // namespace
 
 cudaError_t launch_chunk_attn(const ChunkParams &p, const CUtensorMap &tq, const CUtensorMap &tk,
-                              const CUtensorMap &tv, int head_dim, int nq, int grid, cudaStream_t s, bool early)
+                              const CUtensorMap &tv, const CUtensorMap &tkn, const CUtensorMap &tvn, int head_dim,
+                              int nq, int grid, cudaStream_t s, bool early)
 {
     if (head_dim == 128)
-        return nq == 2 ? launch_chunk_t<128, 2>(p, tq, tk, tv, grid, s, early) : launch_chunk_t<128, 1>(p, tq, tk, tv, grid, s, early);
-    return nq == 2 ? launch_chunk_t<64, 2>(p, tq, tk, tv, grid, s, early) : launch_chunk_t<64, 1>(p, tq, tk, tv, grid, s, early);
+        return nq == 2 ? launch_chunk_t<128, 2>(p, tq, tk, tv, tkn, tvn, grid, s, early)
+                       : launch_chunk_t<128, 1>(p, tq, tk, tv, tkn, tvn, grid, s, early);
+    return nq == 2 ? launch_chunk_t<64, 2>(p, tq, tk, tv, tkn, tvn, grid, s, early)
+                   : launch_chunk_t<64, 1>(p, tq, tk, tv, tkn, tvn, grid, s, early);
 }
 
 }  // namespace cpsa

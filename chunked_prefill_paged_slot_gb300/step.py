@@ -1,4 +1,5 @@
-"""One attention step of a chunked-prefill batch: KV write, then attention.
+"""One attention step of a chunked-prefill batch: KV write, then attention
+(two kernels' worth of calls, or one call with the write fused into it).
 
 Host orchestration only (workspace ownership, streams, events, pointer
 offsets); every step of the computation runs in libcpsa.so's kernels.
@@ -20,8 +21,10 @@ from . import _lib
 class AttentionStep:
     def __init__(self, num_reqs: int, num_tokens: int, num_q_heads: int, num_kv_heads: int, head_dim: int,
                  max_kv_splits: int = 8, device=None, workspace_bytes: int | None = None,
-                 two_stream: bool = False, balance_threshold: float = 0.1, length_threshold: int = 256):
+                 two_stream: bool = False, balance_threshold: float = 0.1, length_threshold: int = 256,
+                 fused_kv_write: bool = False):
         device = torch.device(device if device is not None else "cuda")
+        self.fused_kv_write = fused_kv_write
         self.dims = (num_q_heads, num_kv_heads, head_dim)
         self.max_kv_splits = max_kv_splits
         if workspace_bytes is None:
@@ -41,6 +44,11 @@ class AttentionStep:
             scale: float = 0.0, stream=None, workspace=None):
         """KV write of the new tokens, then attention, on one stream."""
         ws = self.workspaces[0] if workspace is None else workspace
+        if self.fused_kv_write:
+            _lib.cpp_chunked_prefill_attn_write_kv(q, k, v, slot_mapping, k_cache, v_cache, query_lens, seq_lens,
+                                                   block_table, out, ws, self.dev_err, scale=scale,
+                                                   max_kv_splits=self.max_kv_splits, stream=stream)
+            return
         _lib.cpp_kv_cache_write(k, v, slot_mapping, k_cache, v_cache, self.dev_err, stream=stream)
         _lib.cpp_chunked_prefill_attn(q, k_cache, v_cache, query_lens, seq_lens, block_table, out, ws,
                                       self.dev_err, scale=scale, max_kv_splits=self.max_kv_splits, stream=stream)

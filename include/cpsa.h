@@ -156,6 +156,55 @@ int cpp_chunked_prefill_attn_events(const void *q, const void *k_cache, const vo
                                     void *const *events);
 
 /*
+ * The KV write fused into the attention: cpp_kv_cache_write followed by
+ * cpp_chunked_prefill_attn in one call, with no separate write kernel and no
+ * re-read of the new rows from the cache ([DS] section 3.1 for the write and
+ * the metadata, [CP] section 3.2.1 for the attention, whose chunk attends to
+ * its own keys alongside the cached history).
+ *
+ * k, v: bf16 [num_tokens][num_kv_heads][head_dim], contiguous, 16-byte aligned
+ * (the layout of cpp_kv_cache_write); slot_mapping: int64 [num_tokens]; both
+ * caches are written. Every other argument, the workspace and the device flags
+ * are those of cpp_chunked_prefill_attn.
+ *
+ * Attention reads the history keys (positions < h_r) from the cache through
+ * block_table and the new tokens' keys and values straight from k and v, so
+ * its result equals the two-call sequence whenever token i of request r is
+ * placed at slot block_table[r][(h_r + i) / page_size] * page_size + (h_r + i) %
+ * page_size, the usual case. Each new row is also stored, once and bit for bit,
+ * to k_cache / v_cache at slot_mapping[t] with the rules of cpp_kv_cache_write
+ * (s < 0 skipped, s past the cache flagged with CPSA_DEV_SLOT_OUT_OF_RANGE and
+ * skipped). Rows of requests that fail validation (CPSA_DEV_SEQ_LT_QUERY,
+ * CPSA_DEV_SEQ_GT_TABLE, CPSA_DEV_TOKENS_MISMATCH) are neither attended nor
+ * stored. The stores of a call become visible to later stream-ordered work; no
+ * part of the same call reads them. With every h_r a multiple of 128 the output
+ * is bit-identical to the two-call sequence; otherwise the chunk's keys are
+ * tiled from h_r rather than from a multiple of 128 and the output agrees to
+ * the attention's rounding.
+ */
+int cpp_chunked_prefill_attn_write_kv(const void *q, const void *k, const void *v,
+                                      const int64_t *slot_mapping, void *k_cache, void *v_cache,
+                                      const int32_t *query_lens, const int32_t *seq_lens,
+                                      const int32_t *block_table, int num_reqs, int64_t num_tokens,
+                                      int max_blocks_per_req, int num_q_heads, int num_kv_heads,
+                                      int head_dim, int page_size, int64_t num_pages, float scale,
+                                      int max_kv_splits, void *out, void *workspace,
+                                      size_t workspace_bytes, uint32_t *dev_err, void *stream);
+
+/* cpp_chunked_prefill_attn_write_kv with the 5 timing events of
+ * cpp_chunked_prefill_attn_events (same positions, same plain stream order). */
+int cpp_chunked_prefill_attn_write_kv_events(const void *q, const void *k, const void *v,
+                                             const int64_t *slot_mapping, void *k_cache,
+                                             void *v_cache, const int32_t *query_lens,
+                                             const int32_t *seq_lens, const int32_t *block_table,
+                                             int num_reqs, int64_t num_tokens,
+                                             int max_blocks_per_req, int num_q_heads,
+                                             int num_kv_heads, int head_dim, int page_size,
+                                             int64_t num_pages, float scale, int max_kv_splits,
+                                             void *out, void *workspace, size_t workspace_bytes,
+                                             uint32_t *dev_err, void *stream, void *const *events);
+
+/*
  * cpp_chunked_prefill_attn for callers that cannot allocate device memory.
  * (The pages have no counterpart of this call; it exists for library users.)
  *

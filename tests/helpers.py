@@ -72,3 +72,36 @@ def run_gpu_batch(cpsa, batch, max_kv_splits=8, workspace_bytes=None, scale=0.0,
     torch.cuda.synchronize()
     flags = cpsa.cpp_read_device_error(err)
     return bf16_tensor_to_f64(out), flags, kc, vc
+
+
+def run_gpu_batch_fused(cpsa, batch, max_kv_splits=8, scale=0.0, slot_mapping=None):
+    """History written by cpp_kv_cache_write into NaN-filled caches, then one
+    cpp_chunked_prefill_attn_write_kv call that writes the new tokens and attends.
+    Returns (out float64, flags, k_cache, v_cache)."""
+    import torch
+    s = batch.spec
+    kc = to_dev(W.empty_cache(batch).view(np.int16)).view(torch.bfloat16)
+    vc = kc.clone()
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    if batch.hist_k is not None and batch.hist_k.shape[0]:
+        cpsa.cpp_kv_cache_write(to_dev_bf16(batch.hist_k), to_dev_bf16(batch.hist_v),
+                                to_dev(batch.hist_slot_mapping), kc, vc, err)
+    T = batch.num_tokens
+    B = len(s.qlen)
+    ws = torch.empty(cpsa.cpp_attn_workspace_bytes(B, T, s.num_q_heads, s.num_kv_heads, s.head_dim, max_kv_splits),
+                     dtype=torch.uint8, device="cuda")
+    out = torch.full((T, s.num_q_heads, s.head_dim), float("nan"), dtype=torch.bfloat16, device="cuda")
+    sm = batch.slot_mapping if slot_mapping is None else slot_mapping
+    cpsa.cpp_chunked_prefill_attn_write_kv(to_dev_bf16(batch.q), to_dev_bf16(batch.k), to_dev_bf16(batch.v),
+                                           to_dev(sm), kc, vc, to_dev(batch.query_lens), to_dev(batch.seq_lens),
+                                           to_dev(batch.block_table), out, ws, err, scale=scale,
+                                           max_kv_splits=max_kv_splits)
+    torch.cuda.synchronize()
+    flags = cpsa.cpp_read_device_error(err)
+    return bf16_tensor_to_f64(out), flags, kc, vc
+
+
+def cache_bits(t):
+    """A bf16 device cache as uint16 bits on the host."""
+    import torch
+    return t.contiguous().view(torch.int16).cpu().numpy().view(np.uint16)
