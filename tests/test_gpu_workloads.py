@@ -176,3 +176,84 @@ def test_gpu_chunk_invariance(cuda_lib):
         assert cuda_lib.cpp_read_device_error(err) == 0
         outs.append(out.float().cpu().numpy().astype(np.float64))
     compare(outs[1], outs[0], atol=1e-2, rtol_f=3e-3, what="chunked vs whole")
+
+
+def test_llama_64_chunks_match_one_prefill(cuda_lib):
+    """The headline workload end to end: the 32768-token prompt prefilled in 64
+    fused chunks of 512 agrees with the same prompt prefilled as one causal chunk
+    of 32768 (every row, every head), and both leave the same cache."""
+    import torch
+    SEQ, C, P = 32768, 512, 128
+    q, k, v, slots, bt = W.device_sequence(SEQ, P)
+    n_pages = bt.shape[1]
+    outs, caches = [], []
+    for chunk in (C, SEQ):
+        kc = torch.full((n_pages, 8, P, 128), float("nan"), dtype=torch.bfloat16, device="cuda")
+        vc = kc.clone()
+        err = torch.zeros(1, dtype=torch.int32, device="cuda")
+        out = torch.empty_like(q)
+        ws = torch.empty(cuda_lib.cpp_attn_workspace_bytes(1, chunk, 32, 8, 128, 8), dtype=torch.uint8,
+                         device="cuda")
+        ql = torch.tensor([chunk], dtype=torch.int32, device="cuda")
+        for a in range(0, SEQ, chunk):
+            sl = torch.tensor([a + chunk], dtype=torch.int32, device="cuda")
+            cuda_lib.cpp_chunked_prefill_attn_write_kv(q[a:a + chunk], k[a:a + chunk], v[a:a + chunk],
+                                                       slots[a:a + chunk], kc, vc, ql, sl, bt, out[a:a + chunk],
+                                                       ws, err, max_kv_splits=8)
+        torch.cuda.synchronize()
+        assert cuda_lib.cpp_read_device_error(err) == 0
+        outs.append(out)
+        caches.append((kc, vc))
+    assert torch.equal(caches[0][0].view(torch.int16), caches[1][0].view(torch.int16))
+    assert torch.equal(caches[0][1].view(torch.int16), caches[1][1].view(torch.int16))
+    a, b = outs[0].float(), outs[1].float()
+    assert bool(torch.isfinite(a).all()) and bool(torch.isfinite(b).all())
+    max_abs = float((a - b).abs().max())
+    rel_f = float(torch.linalg.vector_norm(a - b) / torch.linalg.vector_norm(b))
+    assert max_abs <= 1e-2 and rel_f <= 3e-3, f"64 chunks vs one: max-abs {max_abs:.3e} rel-F {rel_f:.3e}"
+
+
+def test_dynamic_chunks_sampled_rows(cuda_lib):
+    """The dynamic-chunking workload: the 32768-token prompt (page 128) in the
+    chunk sizes the planner gives for a fixed quadratic latency model, fused
+    calls; sampled rows of every chunk (first, last and six drawn) against the
+    oracle."""
+    import torch
+    SEQ, P = 32768, 128
+    # a latency model of the size the profile fits give on this GPU (ms)
+    chunks = cuda_lib.cpp_plan_chunk_sizes(4.75e-9, 3.87e-5, 0.024, SEQ, 4096, P, 64, 0, 0, 1.0)
+    assert sum(chunks) == SEQ and chunks[0] == 4096 and len(chunks) > 8
+    q, k, v, slots, bt = W.device_sequence(SEQ, P, seed=4)
+    n_pages = bt.shape[1]
+    kc = torch.full((n_pages, 8, P, 128), float("nan"), dtype=torch.bfloat16, device="cuda")
+    vc = kc.clone()
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    out = torch.empty_like(q)
+    ws = torch.empty(cuda_lib.cpp_attn_workspace_bytes(1, max(chunks), 32, 8, 128, 8), dtype=torch.uint8,
+                     device="cuda")
+    a = 0
+    for c in chunks:
+        ql = torch.tensor([c], dtype=torch.int32, device="cuda")
+        sl = torch.tensor([a + c], dtype=torch.int32, device="cuda")
+        cuda_lib.cpp_chunked_prefill_attn_write_kv(q[a:a + c], k[a:a + c], v[a:a + c], slots[a:a + c], kc, vc,
+                                                   ql, sl, bt, out[a:a + c], ws, err, max_kv_splits=8)
+        a += c
+    torch.cuda.synchronize()
+    assert cuda_lib.cpp_read_device_error(err) == 0
+    rng = np.random.default_rng(44)
+    rows = []
+    a = 0
+    for c in chunks:
+        rows.extend([a, a + c - 1] + [a + int(x) for x in rng.choice(c, 6, replace=False)])
+        a += c
+    rows = np.unique(np.asarray(rows))
+    n_pg = SEQ // P
+    kk = np.full((n_pg, 8, P, 128), W.BF16_NAN_SENTINEL, dtype=np.uint16)
+    vv = kk.copy()
+    pos = np.arange(SEQ)
+    oracle.kv_cache_write(_u16(k), _u16(v), ((pos // P) * P + pos % P).astype(np.int64), P, kk, vv)
+    # the whole prompt as one request: row t sees keys 0..t, whichever chunk held it
+    ref = oracle.paged_attention(_u16(q), kk, vv, [SEQ], [SEQ], np.arange(n_pg, dtype=np.int32)[None, :],
+                                 rows=rows)
+    got = out[torch.from_numpy(rows).cuda()].float().cpu().numpy().astype(np.float64)
+    compare(got, ref, what="dynamic chunks")
