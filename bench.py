@@ -36,6 +36,7 @@ if ROOT not in sys.path:
 
 SEQ, CHUNK, HQ, HKV, D, PAGE = 32768, 512, 32, 8, 128, 128
 N_CHUNKS = SEQ // CHUNK
+E2E_BATCH = 8   # chunks per host<->device copy in the end-to-end measurement
 WORKLOAD = "llama3-8b-attn-layer 32768-token prefill in 64 chunks of 512 (32/8 heads, d128, bf16, page 128)"
 METRIC = "chunked-prefill attention TFLOP/s"
 
@@ -217,31 +218,69 @@ class ChunkedPrefill:
     def chunk_kernel_ms(self):
         return [self.marks[i][0].elapsed_time(self.marks[i][1]) for i in range(N_CHUNKS)]
 
-    # host-buffer variant for the end-to-end number
+    # host-buffer variant for the end-to-end number: the step's inputs come from
+    # pinned host memory and its output goes back there. Chunks are grouped in
+    # batches of E2E_BATCH; each batch's inputs are copied in on one side stream
+    # and its outputs copied out on another, into double buffers, so the copies
+    # of batch b +- 1 overlap the attention of batch b. A plain torch kernel sits
+    # between every cross-stream event and the library's kernels, so no event
+    # operation is adjacent to a programmatically launched kernel.
     def make_host(self):
         torch = self.torch
         pin = lambda t: t.cpu().pin_memory()
         self.host = dict(q=pin(self.q), k=pin(self.k), v=pin(self.v), slots=pin(self.slots),
                          out=torch.empty(self.out.shape, dtype=self.out.dtype).pin_memory())
-        self.dq = torch.empty((CHUNK, HQ, D), dtype=torch.bfloat16, device=self.dev)
-        self.dk = torch.empty((CHUNK, HKV, D), dtype=torch.bfloat16, device=self.dev)
-        self.dv = torch.empty_like(self.dk)
-        self.ds = torch.empty(CHUNK, dtype=torch.int64, device=self.dev)
-        self.dout = torch.empty_like(self.dq)
-        h2d = (self.dq.numel() + self.dk.numel() + self.dv.numel()) * 2 + self.ds.numel() * 8
-        return h2d * N_CHUNKS, self.dout.numel() * 2 * N_CHUNKS
+        n = E2E_BATCH * CHUNK
+        self.e2e_in = [dict(q=torch.empty((n, HQ, D), dtype=torch.bfloat16, device=self.dev),
+                            k=torch.empty((n, HKV, D), dtype=torch.bfloat16, device=self.dev),
+                            v=torch.empty((n, HKV, D), dtype=torch.bfloat16, device=self.dev),
+                            slots=torch.empty(n, dtype=torch.int64, device=self.dev)) for _ in range(2)]
+        self.e2e_out = [torch.empty((n, HQ, D), dtype=torch.bfloat16, device=self.dev) for _ in range(2)]
+        self.e2e_streams = (torch.cuda.Stream(device=self.dev), torch.cuda.Stream(device=self.dev))
+        self.e2e_tick = torch.zeros(1, dtype=torch.int32, device=self.dev)
+        h2d = (self.q.numel() + self.k.numel() + self.v.numel()) * 2 + self.slots.numel() * 8
+        return h2d, self.out.numel() * 2
 
     def step_e2e(self, stream):
-        h = self.host
-        with self.torch.cuda.stream(stream):
-            for i in range(N_CHUNKS):
-                a, b = i * CHUNK, (i + 1) * CHUNK
-                self.dq.copy_(h["q"][a:b], non_blocking=True)
-                self.dk.copy_(h["k"][a:b], non_blocking=True)
-                self.dv.copy_(h["v"][a:b], non_blocking=True)
-                self.ds.copy_(h["slots"][a:b], non_blocking=True)
-                self.chunk(i, self.dq, self.dk, self.dv, self.ds, self.dout, stream)
-                h["out"][a:b].copy_(self.dout, non_blocking=True)
+        torch, h = self.torch, self.host
+        s_in, s_out = self.e2e_streams
+        nb = N_CHUNKS // E2E_BATCH
+        ev = lambda: torch.cuda.Event()
+        start = ev()
+        start.record(stream)
+        h2d_done, comp_done, d2h_done = [None] * nb, [None] * nb, [None] * nb
+        for b in range(nb):
+            buf, out = self.e2e_in[b % 2], self.e2e_out[b % 2]
+            a0, a1 = b * E2E_BATCH * CHUNK, (b + 1) * E2E_BATCH * CHUNK
+            # inputs of batch b, once batch b - 2 (same buffers) has been computed
+            s_in.wait_event(start if b < 2 else comp_done[b - 2])
+            with torch.cuda.stream(s_in):
+                for name in ("q", "k", "v", "slots"):
+                    buf[name].copy_(h[name][a0:a1], non_blocking=True)
+            h2d_done[b] = ev()
+            h2d_done[b].record(s_in)
+            # attention of batch b, once its inputs are in and batch b - 2's outputs are out
+            stream.wait_event(h2d_done[b])
+            if b >= 2:
+                stream.wait_event(d2h_done[b - 2])
+            with torch.cuda.stream(stream):
+                self.e2e_tick.add_(1)
+            for j in range(E2E_BATCH):
+                i = b * E2E_BATCH + j
+                sl = slice(j * CHUNK, (j + 1) * CHUNK)
+                self.chunk(i, buf["q"][sl], buf["k"][sl], buf["v"][sl], buf["slots"][sl], out[sl], stream)
+            with torch.cuda.stream(stream):
+                self.e2e_tick.add_(1)
+            comp_done[b] = ev()
+            comp_done[b].record(stream)
+            # outputs of batch b
+            s_out.wait_event(comp_done[b])
+            with torch.cuda.stream(s_out):
+                h["out"][a0:a1].copy_(out, non_blocking=True)
+            d2h_done[b] = ev()
+            d2h_done[b].record(s_out)
+        stream.wait_event(d2h_done[nb - 1])
+        stream.wait_event(d2h_done[nb - 2])
 
 
 # ----------------------------------------------------------------------------- oracle (CPU) leg
