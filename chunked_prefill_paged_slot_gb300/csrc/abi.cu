@@ -285,6 +285,7 @@ int attn_impl(const void *q, const void *k_new, const void *v_new, const int64_t
     int32_t *counts = reinterpret_cast<int32_t *>(ws + L.off_counts);
     int32_t *cu_q = reinterpret_cast<int32_t *>(ws + L.off_cuq);
     int32_t *run_first = reinterpret_cast<int32_t *>(ws + L.off_runs);
+    int32_t *flags = reinterpret_cast<int32_t *>(ws + L.off_flags);
     PrefillItem *pitems = reinterpret_cast<PrefillItem *>(ws + L.off_pitems);
     DecodeItem *ditems = reinterpret_cast<DecodeItem *>(ws + L.off_ditems);
     CombineItem *citems = reinterpret_cast<CombineItem *>(ws + L.off_citems);
@@ -310,6 +311,7 @@ int attn_impl(const void *q, const void *k_new, const void *v_new, const int64_t
     pp.counts = counts;
     pp.cu_q = cu_q;
     pp.run_first = run_first;
+    pp.flags = flags;
     pp.pitems = pitems;
     pp.ditems = ditems;
     pp.citems = citems;
@@ -377,6 +379,7 @@ int attn_impl(const void *q, const void *k_new, const void *v_new, const int64_t
     static_cast<AttnCommon &>(cp) = ac;
     cp.pitems = pitems;
     cp.run_first = run_first;
+    cp.flags = flags;
     // A single request is either one decode row or one prefill: the other
     // kernel would find no items, so it is not launched.
     const bool single_prefill = num_reqs == 1 && num_tokens >= 2;
@@ -397,7 +400,9 @@ int attn_impl(const void *q, const void *k_new, const void *v_new, const int64_t
         return CPSA_ERR_CUDA;
     mark(3, s);
 
-    if (cap > 0) {
+    // the combine kernel merges split decode rows (split prefill units are merged
+    // in the chunk kernel): a single prefill request has none
+    if (cap > 0 && !single_prefill) {
         CombineParams cb{counts, citems, part_o, part_ml, out, num_q_heads};
         const int grid_m = 4 * sms;
         if (grid_m > 0 && launch_combine(cb, head_dim, grid_m, s, early) != cudaSuccess)

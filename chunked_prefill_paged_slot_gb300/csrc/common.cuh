@@ -126,6 +126,16 @@ __device__ __forceinline__ bool mbar_wait_sleep(uint64_t *bar, uint32_t parity, 
     }
 }
 
+// GPU-scope acquire load and ordering fence (cross-CTA hand-offs through global memory).
+__device__ __forceinline__ int ld_acquire_gpu(const int *p)
+{
+    int v;
+    asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+    return v;
+}
+
+__device__ __forceinline__ void fence_acq_rel_gpu() { asm volatile("fence.acq_rel.gpu;" ::: "memory"); }
+
 // ---------------------------------------------------------------------------
 // TMA: tiled tensor loads into shared memory, completion on an mbarrier
 // ---------------------------------------------------------------------------

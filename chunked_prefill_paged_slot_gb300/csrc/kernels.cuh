@@ -37,6 +37,7 @@ struct AttnCommon {
 struct ChunkParams : AttnCommon {
     const PrefillItem *pitems;
     const int32_t *run_first;   // CTA c processes pieces [run_first[c], run_first[c + 1])
+    int32_t *flags;             // per split unit, q head and softmax warp: pieces done (zeroed by the plan)
 };
 
 struct DecodeParams : AttnCommon {

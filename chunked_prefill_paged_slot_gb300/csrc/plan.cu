@@ -22,7 +22,7 @@ namespace cpsa {
 namespace {
 
 constexpr int kPlanThreads = 1024;
-constexpr int kScan = 5;
+constexpr int kScan = 6;
 
 __device__ __forceinline__ int ceil_div(int a, int b) { return (a + b - 1) / b; }
 
@@ -69,10 +69,10 @@ __device__ int decode_splits(const Req &rq, int max_splits)
     return max(ns, 1);
 }
 
-// pieces; partial rows; combine units and combine items (split decode rows and
-// split prefill units); decode items
+// pieces; partial rows; combine units and combine items (split decode rows);
+// decode items; split prefill units
 struct Counts {
-    int pieces, prows, cunits, citems, ditems;
+    int pieces, prows, cunits, citems, ditems, sunits;
 };
 
 __device__ __forceinline__ int warp_excl_scan(int x, int lane, int &total)
@@ -97,7 +97,7 @@ __device__ __forceinline__ int warp_excl_scan(int x, int lane, int &total)
 __device__ Counts request_work(const PlanParams &p, int r, const Req &rq, int tile_off, int run, bool cut,
                                int max_splits, bool emit, int q_off, const Counts &off, int lane)
 {
-    Counts c{0, 0, 0, 0, 0};
+    Counts c{0, 0, 0, 0, 0, 0};
     if (!rq.valid || rq.q == 0)
         return c;
     if (rq.q == 1) {
@@ -137,11 +137,11 @@ __device__ Counts request_work(const PlanParams &p, int r, const Req &rq, int ti
             const int u0 = tile_run + j * nkv, u1 = u0 + nkv;
             const int np = active ? (cut ? (u1 - 1) / run - u0 / run + 1 : 1) : 0;
             const bool split = np > 1;
-            int t_np, t_ci, t_pr, t_cu;
+            int t_np, t_su, t_pr;
             const int e_np = warp_excl_scan(np, lane, t_np);
-            const int e_ci = warp_excl_scan(split ? 1 : 0, lane, t_ci);
-            const int e_pr = warp_excl_scan(split ? rows * p.nq * np : 0, lane, t_pr);
-            const int e_cu = warp_excl_scan(split ? rows * p.nq : 0, lane, t_cu);
+            const int e_su = warp_excl_scan(split ? 1 : 0, lane, t_su);
+            // a split unit's partials: kTileM rows x nq heads x np pieces (see the chunk kernel's merge)
+            const int e_pr = warp_excl_scan(split ? kTileM * p.nq * np : 0, lane, t_pr);
             if (emit && active) {
                 const int kvh = j / pairs, hp = j % pairs;
                 const int pbase = split ? off.prows + c.prows + e_pr : -1;
@@ -153,25 +153,22 @@ __device__ Counts request_work(const PlanParams &p, int r, const Req &rq, int ti
                     if (cut && u0 % run == 0)
                         p.run_first[u0 / run] = pi;
                 } else {
+                    const int sunit = off.sunits + c.sunits + e_su;
                     int x = u0;
                     for (int pc = 0; pc < np; ++pc) {
                         const int owner = x / run;
                         const int end = min(u1, (owner + 1) * run);
                         p.pitems[pi + pc] =
-                            PrefillItem{r, i0, kvh | (hp << 16), x - u0, end - u0, pc | (np << 16), pbase, owner};
+                            PrefillItem{r, i0, kvh | (hp << 16), x - u0, end - u0, pc | (np << 16), pbase, sunit};
                         if (x == owner * run)
                             p.run_first[owner] = pi + pc;
                         x = end;
                     }
-                    p.citems[off.citems + c.citems + e_ci] =
-                        CombineItem{q_off + i0, rows, kvh * p.group + hp * p.nq, p.nq, pbase, np,
-                                    off.cunits + c.cunits + e_cu, 0};
                 }
             }
             c.pieces += t_np;
-            c.citems += t_ci;
+            c.sunits += t_su;
             c.prows += t_pr;
-            c.cunits += t_cu;
         }
         tile_run += upq * nkv;
     }
@@ -216,8 +213,8 @@ __device__ void fill_run_first(const PlanParams &p, int n_pieces, int grid, bool
         return;
     }
     for (int i = tid; i <= n_pieces; i += nthreads) {
-        const int lo = i == 0 ? 0 : p.pitems[i - 1].owner + 1;
-        const int hi = i == n_pieces ? grid : p.pitems[i].owner;
+        const int lo = i == 0 ? 0 : p.pitems[i - 1].aux + 1;   // without cuts, aux is the owner CTA
+        const int hi = i == n_pieces ? grid : p.pitems[i].aux;
         for (int c = lo; c <= hi; ++c) p.run_first[c] = i;
     }
 }
@@ -316,7 +313,7 @@ __global__ void __launch_bounds__(kPlanThreads, 1) plan_kernel(PlanParams p)
     __shared__ int s_cnt[kPlanThreads][kScan];
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     int carry_a[2] = {0, 0};                        // tokens, tiles
-    int carry_b[kScan] = {0, 0, 0, 0, 0};           // pieces, prows, cunits, citems, ditems
+    int carry_b[kScan] = {0, 0, 0, 0, 0, 0};        // pieces, prows, cunits, citems, ditems, sunits
     for (int base = 0; base < p.num_reqs; base += kPlanThreads) {
         const int nloc = min(kPlanThreads, p.num_reqs - base);
         // (a) token and tile offsets: one thread per request
@@ -344,13 +341,14 @@ __global__ void __launch_bounds__(kPlanThreads, 1) plan_kernel(PlanParams p)
         for (int l = warp; l < nloc; l += kPlanThreads / 32) {
             const Req rq = load_req(p, base + l);
             const Counts c = request_work(p, base + l, rq, s_toff[l], run, split_prefill, max_splits, false,
-                                          s_qoff[l], Counts{0, 0, 0, 0, 0}, lane);
+                                          s_qoff[l], Counts{0, 0, 0, 0, 0, 0}, lane);
             if (lane == 0) {
                 s_cnt[l][0] = c.pieces;
                 s_cnt[l][1] = c.prows;
                 s_cnt[l][2] = c.cunits;
                 s_cnt[l][3] = c.citems;
                 s_cnt[l][4] = c.ditems;
+                s_cnt[l][5] = c.sunits;
             }
         }
         __syncthreads();
@@ -367,7 +365,7 @@ __global__ void __launch_bounds__(kPlanThreads, 1) plan_kernel(PlanParams p)
         // (d) the lists: one warp per request
         for (int l = warp; l < nloc; l += kPlanThreads / 32) {
             const Req rq = load_req(p, base + l);
-            const Counts off{s_cnt[l][0], s_cnt[l][1], s_cnt[l][2], s_cnt[l][3], s_cnt[l][4]};
+            const Counts off{s_cnt[l][0], s_cnt[l][1], s_cnt[l][2], s_cnt[l][3], s_cnt[l][4], s_cnt[l][5]};
             request_work(p, base + l, rq, s_toff[l], run, split_prefill, max_splits, true, s_qoff[l], off, lane);
         }
         __syncthreads();
@@ -375,6 +373,8 @@ __global__ void __launch_bounds__(kPlanThreads, 1) plan_kernel(PlanParams p)
     __syncthreads();   // this block's piece writes are visible to the whole block
     const int n_pieces = (int)min((int64_t)carry_b[0], p.max_pitems);
     fill_run_first(p, n_pieces, grid, split_prefill, tiles, run, threadIdx.x, kPlanThreads);
+    const int n_flags = min(carry_b[5], kMaxSplitUnits) * p.nq * 4;
+    for (int i = threadIdx.x; i < n_flags; i += kPlanThreads) p.flags[i] = 0;
     if (threadIdx.x == 0) {
         p.cu_q[p.num_reqs] = carry_a[0];
         p.counts[kCntPrefill] = (int)min((int64_t)carry_b[0], p.max_pitems);
@@ -383,7 +383,8 @@ __global__ void __launch_bounds__(kPlanThreads, 1) plan_kernel(PlanParams p)
         p.counts[kCntCombineUnits] = carry_b[2];
         p.counts[kCntDecode] = (int)min((int64_t)carry_b[4], p.max_ditems);
         p.counts[kCntRunTiles] = run;
-        for (int j = kCntRunTiles + 1; j < kCntSlots; ++j) p.counts[j] = 0;
+        p.counts[kCntSplitUnits] = carry_b[5];
+        for (int j = kCntSplitUnits + 1; j < kCntSlots; ++j) p.counts[j] = 0;
     }
 }
 
@@ -431,7 +432,7 @@ __global__ void __launch_bounds__(32, 1) plan_small_kernel(PlanParams p)
     const SplitChoice sc = choose_split(p, tile_sum, dprow_sum);
     if (sc.clamped && lane == 0)
         set_dev_error(p.dev_err, CPSA_DEV_SPLITS_CLAMPED);
-    Counts off{0, 0, 0, 0, 0};
+    Counts off{0, 0, 0, 0, 0, 0};
     for (int r = 0; r < p.num_reqs; ++r) {
         Req rr;
         rr.valid = __shfl_sync(0xffffffffu, rq.valid ? 1 : 0, r) != 0;
@@ -446,10 +447,13 @@ __global__ void __launch_bounds__(32, 1) plan_small_kernel(PlanParams p)
         off.cunits += c.cunits;
         off.citems += c.citems;
         off.ditems += c.ditems;
+        off.sunits += c.sunits;
     }
     __syncwarp();   // the warp's piece writes are visible to all its lanes
     const int n_pieces = (int)min((int64_t)off.pieces, p.max_pitems);
     fill_run_first(p, n_pieces, grid, sc.split_prefill, tile_sum, sc.run, lane, 32);
+    const int n_flags = min(off.sunits, kMaxSplitUnits) * p.nq * 4;
+    for (int i = lane; i < n_flags; i += 32) p.flags[i] = 0;
     if (lane == 0) {
         p.cu_q[p.num_reqs] = tok_total;
         p.counts[kCntPrefill] = n_pieces;
@@ -458,7 +462,8 @@ __global__ void __launch_bounds__(32, 1) plan_small_kernel(PlanParams p)
         p.counts[kCntCombineUnits] = off.cunits;
         p.counts[kCntDecode] = (int)min((int64_t)off.ditems, p.max_ditems);
         p.counts[kCntRunTiles] = sc.run;
-    } else if (lane > kCntRunTiles && lane < kCntSlots) {
+        p.counts[kCntSplitUnits] = off.sunits;
+    } else if (lane > kCntSplitUnits && lane < kCntSlots) {
         p.counts[lane] = 0;
     }
 }

@@ -20,8 +20,9 @@ namespace cpsa {
 // Prefill: stream-K. The KV tiles of all prefill units (one unit = a 128-row
 // query tile x kv head x head pair) are laid end to end and cut into equal runs
 // of max(ceil(W / grid), kMinRunTiles) tiles, one run per CTA of the chunk
-// kernel; a unit cut by a run boundary becomes several pieces whose partial
-// results the combine kernel merges. Every CTA gets the same amount of work.
+// kernel; a unit cut by a run boundary becomes several pieces, merged inside the
+// chunk kernel by whichever piece finishes last (a counter per unit and q head;
+// no CTA waits for another). Every CTA gets the same amount of work.
 // Decode: a row splits into pieces of kDecodeKeysPerSplit keys (at most
 // max_kv_splits), depending only on its own length.
 // KV tiles of a unit: tile kt holds keys [128 kt, 128 kt + 128). With the KV
@@ -34,13 +35,16 @@ constexpr int kMinRunTiles = 4;             // shortest run of KV tiles per CTA
 constexpr int kMaxChunkGrid = 256;          // upper bound of the chunk kernel's grid (SMs)
 constexpr int kDecodeChunk = 64;            // keys per decode pipeline stage
 constexpr int kDecodeKeysPerSplit = 4096;   // keys per decode split (multiple of kDecodeChunk)
+constexpr int kMaxSplitUnits = kMaxChunkGrid;   // a split unit holds a run boundary: at most grid - 1
+constexpr int kMergeCounters = 2 * 4;          // per split unit: q heads (<= 2) x 4 softmax warps
 
 // A prefill piece: KV tiles [kt0, kt1) of the unit (request r, query tile at
-// row i0, kv head kvh, head pair hp), processed by CTA `owner`; piece `piece` of
-// `npieces` of that unit (partials at pbase when npieces > 1, merged by the
-// combine kernel).
+// row i0, kv head kvh, head pair hp); piece `piece` of `npieces` of that unit.
+// aux: for a whole unit (npieces = 1) the CTA that processes it; for a piece of
+// a split unit, the unit's ordinal among the batch's split units (its merge
+// counters), its partial rows at pbase.
 struct PrefillItem {
-    int32_t r, i0, kvh_hp, kt0, kt1, piece_np, pbase, owner;
+    int32_t r, i0, kvh_hp, kt0, kt1, piece_np, pbase, aux;
 };
 
 // A decode item: the single new token (global row t) of request r, all q heads
@@ -49,6 +53,7 @@ struct DecodeItem {
     int32_t r, kvh, key0, key1, split, nsplit, pbase, t;
 };
 
+// Split decode rows for the combine kernel.
 // Rows [t0, t0 + nrows) x q heads [h0, h0 + nh) had nsplit partials each:
 // unit u = row * nh + (head - h0) at pbase + u * nsplit + s.
 // u0: number of (row, head) units of all earlier combine items.
@@ -63,11 +68,13 @@ enum CountSlot {
     kCntPartialRows = 3,
     kCntCombineUnits = 4,
     kCntRunTiles = 5,
+    kCntSplitUnits = 6,
     kCntSlots = 16
 };
 
 struct WsLayout {
-    size_t off_counts, off_cuq, off_runs, off_pitems, off_ditems, off_citems, off_pml, off_po, end_meta, end_full;
+    size_t off_counts, off_cuq, off_runs, off_flags, off_pitems, off_ditems, off_citems, off_pml, off_po, end_meta,
+        end_full;
     int64_t max_pitems, max_ditems, max_citems, max_prows_full;
 };
 
@@ -86,7 +93,7 @@ inline WsLayout ws_layout(int num_reqs, int64_t num_tokens, int Hq, int Hkv, int
     int64_t units = qtiles * Hkv * ((Hq / Hkv) / nq_per_cta);
     L.max_pitems = units + kMaxChunkGrid;
     L.max_ditems = ndecode * Hkv * max_splits;
-    L.max_citems = ndecode + 2 * kMaxChunkGrid;   // split decode rows + split prefill units
+    L.max_citems = ndecode;   // split decode rows
     // prefill: a cut inside a unit adds one piece, at most 2 pieces' partials per cut
     const int64_t prefill_rows = max_splits > 1 ? (int64_t)2 * kMaxChunkGrid * 128 * nq_per_cta : 0;
     const int64_t decode_rows = max_splits > 1 ? ndecode * Hq * max_splits : 0;
@@ -95,6 +102,7 @@ inline WsLayout ws_layout(int num_reqs, int64_t num_tokens, int Hq, int Hkv, int
     L.off_counts = o; o = ws_align(o + sizeof(int32_t) * kCntSlots);
     L.off_cuq = o;    o = ws_align(o + sizeof(int32_t) * (size_t)(B + 1));
     L.off_runs = o;   o = ws_align(o + sizeof(int32_t) * (size_t)(kMaxChunkGrid + 1));
+    L.off_flags = o;  o = ws_align(o + sizeof(int32_t) * (size_t)kMaxSplitUnits * kMergeCounters);
     L.off_pitems = o; o = ws_align(o + sizeof(PrefillItem) * (size_t)L.max_pitems);
     L.off_ditems = o; o = ws_align(o + sizeof(DecodeItem) * (size_t)L.max_ditems);
     L.off_citems = o; o = ws_align(o + sizeof(CombineItem) * (size_t)L.max_citems);
@@ -130,6 +138,7 @@ struct PlanParams {
     int32_t *counts;
     int32_t *cu_q;
     int32_t *run_first;        // [chunk_grid + 1]: first piece of each CTA's run
+    int32_t *flags;            // [kMaxSplitUnits][nq][4]: merge counters, zeroed by the plan
     PrefillItem *pitems;
     DecodeItem *ditems;
     CombineItem *citems;

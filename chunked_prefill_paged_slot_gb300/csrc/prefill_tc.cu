@@ -130,6 +130,70 @@ __device__ __forceinline__ void store_tile_rows(const ChunkParams &p, const CUte
     }
 }
 
+// The merge of a split unit's row (see the epilogue): sums in piece order, this
+// piece's own terms (its TMEM O, m, l) taken at its place, so the bits do not
+// depend on which piece merges; writes the bf16 row. Kept out of line so that
+// its registers do not weigh on the softmax loop.
+template <int D, int NQ>
+__device__ __noinline__ void merge_split_row(const ChunkParams &p, uint32_t tO, const float2 *pml, const float4 *po,
+                                             int piece, int npieces, int wg, int row, float m_use, float l,
+                                             bool valid_row, int64_t out_off)
+{
+    float M = m_use;
+    for (int q = 0; q < npieces; ++q)
+        if (q != piece)
+            M = fmaxf(M, __ldcg(pml + (q * NQ + wg) * 128 + row).x);
+    const float Mref = M == -INFINITY ? 0.f : M;
+    float L = 0.f;
+    for (int q = 0; q < npieces; ++q) {
+        const float2 ml = q == piece ? make_float2(m_use, l) : __ldcg(pml + (q * NQ + wg) * 128 + row);
+        L += ex2_approx(ml.x - Mref) * ml.y;
+    }
+    const float inv_l = L > 0.f ? 1.f / L : 0.f;
+#pragma unroll 1
+    for (int c = 0; c < D / 32; ++c) {
+        uint32_t r[32];
+        tmem_ld32(tO + c * 32, r);
+        tmem_wait_ld();
+        float acc[32];
+#pragma unroll
+        for (int x = 0; x < 32; ++x) acc[x] = 0.f;
+        for (int q = 0; q < npieces; ++q) {
+            float4 v[8];
+            float mq;
+            if (q == piece) {
+                mq = m_use;
+#pragma unroll
+                for (int x = 0; x < 8; ++x)
+                    v[x] = make_float4(__uint_as_float(r[4 * x]), __uint_as_float(r[4 * x + 1]),
+                                       __uint_as_float(r[4 * x + 2]), __uint_as_float(r[4 * x + 3]));
+            } else {
+                mq = __ldcg(pml + (q * NQ + wg) * 128 + row).x;
+                const float4 *src = po + ((int64_t)(q * NQ + wg) * (D / 4) + c * 8) * 128 + row;
+#pragma unroll
+                for (int x = 0; x < 8; ++x) v[x] = __ldcg(src + x * 128);
+            }
+            const float fq = ex2_approx(mq - Mref);
+#pragma unroll
+            for (int x = 0; x < 8; ++x) {
+                acc[4 * x] = fmaf(fq, v[x].x, acc[4 * x]);
+                acc[4 * x + 1] = fmaf(fq, v[x].y, acc[4 * x + 1]);
+                acc[4 * x + 2] = fmaf(fq, v[x].z, acc[4 * x + 2]);
+                acc[4 * x + 3] = fmaf(fq, v[x].w, acc[4 * x + 3]);
+            }
+        }
+        if (valid_row) {
+            uint4 *dst = reinterpret_cast<uint4 *>(reinterpret_cast<__nv_bfloat16 *>(p.out) + out_off + c * 32);
+#pragma unroll
+            for (int x = 0; x < 4; ++x)
+                dst[x] = make_uint4(pack_bf16x2(acc[8 * x + 0] * inv_l, acc[8 * x + 1] * inv_l),
+                                    pack_bf16x2(acc[8 * x + 2] * inv_l, acc[8 * x + 3] * inv_l),
+                                    pack_bf16x2(acc[8 * x + 4] * inv_l, acc[8 * x + 5] * inv_l),
+                                    pack_bf16x2(acc[8 * x + 6] * inv_l, acc[8 * x + 7] * inv_l));
+        }
+    }
+}
+
 template <int D, int NQ>
 __global__ void __launch_bounds__(352, 1)
 chunk_attn_kernel(const ChunkParams p, const __grid_constant__ CUtensorMap tm_q,
@@ -536,7 +600,7 @@ chunk_attn_kernel(const ChunkParams p, const __grid_constant__ CUtensorMap tm_q,
                 const bool from_new = kt >= nh;
                 const int key0 = from_new ? hist + (kt - nh) * 128 : kt * 128;
                 const int lim = from_new ? limit : limit_hist;
-                if (!(ok = mbar_wait(&bars->s_full[wg], s_uses & 1, abort)))
+                if (!(ok = __all_sync(0xffffffffu, mbar_wait(&bars->s_full[wg], s_uses & 1, abort))))
                     break;
                 ++s_uses;
                 tc_fence_after_sync();
@@ -605,7 +669,7 @@ chunk_attn_kernel(const ChunkParams p, const __grid_constant__ CUtensorMap tm_q,
                 tmem_wait_st();
                 if (__any_sync(0xffffffffu, need) && t > 0) {
                     // O holds the sum through tile t-1: wait for that P.V, then rescale
-                    if (!(ok = mbar_wait(&bars->o_done[wg], (o_base + t - 1) & 1, abort)))
+                    if (!(ok = __all_sync(0xffffffffu, mbar_wait(&bars->o_done[wg], (o_base + t - 1) & 1, abort))))
                         break;
                     tc_fence_after_sync();
 #pragma unroll
@@ -626,7 +690,7 @@ chunk_attn_kernel(const ChunkParams p, const __grid_constant__ CUtensorMap tm_q,
             }
             if (!ok)
                 break;
-            if (!mbar_wait(&bars->o_done[wg], (o_base + n - 1) & 1, abort))
+            if (!__all_sync(0xffffffffu, mbar_wait(&bars->o_done[wg], (o_base + n - 1) & 1, abort)))
                 break;
             o_base += n;
             tc_fence_after_sync();
@@ -634,23 +698,47 @@ chunk_attn_kernel(const ChunkParams p, const __grid_constant__ CUtensorMap tm_q,
             const int64_t t_row = (int64_t)p.cu_q[w.r] + i;
             const int npieces = w.piece_np >> 16;
             if (npieces > 1) {
-                // partial of piece (piece_np & 0xffff) of this unit: unit-local (row, head) major
-                const int64_t pr = (int64_t)w.pbase + ((int64_t)row * NQ + wg) * npieces + (w.piece_np & 0xFFFF);
+                // A piece of a split unit. Every warp (32 rows) decides on its own:
+                // if every other piece has left its partial, it merges them with its
+                // own O at once (the usual case for the piece that ends a CTA's run);
+                // else it leaves its partial and counts itself in, and the piece whose
+                // count completes the set merges. No warp waits for another piece.
+                // Partials are column-major per (piece, head): float4 column j of row
+                // `row` at ((piece * NQ + wg) * D/4 + j) * 128 + row, so a warp's
+                // accesses are 512 contiguous bytes.
+                const int piece = w.piece_np & 0xFFFF;
+                int *cnt = p.flags + ((int64_t)w.aux * NQ + wg) * 4 + sub;
+                float4 *po = reinterpret_cast<float4 *>(p.part_o) + (int64_t)w.pbase * (D / 4);
+                float2 *pml = reinterpret_cast<float2 *>(p.part_ml) + w.pbase;
+                int seen = lane == 0 ? ld_acquire_gpu(cnt) : 0;
+                seen = __shfl_sync(0xffffffffu, seen, 0);
+                bool merge = seen == npieces - 1;
+                if (!merge) {
+                    const int64_t pc = (int64_t)(piece * NQ + wg) * (D / 4);
 #pragma unroll
-                for (int c = 0; c < D / 32; ++c) {
-                    uint32_t r[32];
-                    tmem_ld32(tO + c * 32, r);
-                    tmem_wait_ld();
-                    if (valid_row) {
-                        float4 *dst = reinterpret_cast<float4 *>(p.part_o + pr * D + c * 32);
+                    for (int c = 0; c < D / 32; ++c) {
+                        uint32_t r[32];
+                        tmem_ld32(tO + c * 32, r);
+                        tmem_wait_ld();
 #pragma unroll
                         for (int x = 0; x < 8; ++x)
-                            dst[x] = make_float4(__uint_as_float(r[4 * x]), __uint_as_float(r[4 * x + 1]),
-                                                 __uint_as_float(r[4 * x + 2]), __uint_as_float(r[4 * x + 3]));
+                            po[(pc + c * 8 + x) * 128 + row] =
+                                make_float4(__uint_as_float(r[4 * x]), __uint_as_float(r[4 * x + 1]),
+                                            __uint_as_float(r[4 * x + 2]), __uint_as_float(r[4 * x + 3]));
                     }
+                    pml[(piece * NQ + wg) * 128 + row] = make_float2(m_use, l);
+                    __syncwarp();
+                    if (lane == 0) {
+                        fence_acq_rel_gpu();   // this warp's partial, then the count
+                        seen = atomicAdd(cnt, 1);
+                        fence_acq_rel_gpu();   // the count, then the other partials
+                    }
+                    seen = __shfl_sync(0xffffffffu, seen, 0);
+                    merge = seen == npieces - 1;
                 }
-                if (valid_row)
-                    reinterpret_cast<float2 *>(p.part_ml)[pr] = make_float2(m_use, l);
+                if (merge)
+                    merge_split_row<D, NQ>(p, tO, pml, po, piece, npieces, wg, row, m_use, l, valid_row,
+                                           (t_row * p.num_q_heads + h) * D);
             } else {
                 const float inv_l = l > 0.f ? 1.f / l : 0.f;
 #pragma unroll
