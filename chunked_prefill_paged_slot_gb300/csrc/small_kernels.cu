@@ -293,6 +293,78 @@ __global__ void exp2_selftest_kernel(const float *x, float *poly, float *hw, int
     }
 }
 
+// The same split for batches of at most kSplitSmallMax requests, by one warp
+// with no shared memory: the running prefix is carried across 32-request
+// chunks, and the winning boundary carries its own prefix, so n1 needs no second
+// pass. A lone warp fits beside a chunk-kernel CTA on its SM, so it can start
+// as soon as the attention call before it ends.
+constexpr int kSplitSmallMax = 256;
+
+__global__ void __launch_bounds__(32, 1)
+split_small_kernel(const int32_t *__restrict__ query_lens, int num_reqs, float balance_threshold,
+                   int32_t length_threshold, int32_t *out3)
+{
+    const int lane = threadIdx.x;
+    pdl_trigger();
+    pdl_wait();
+    if (num_reqs < 2) {
+        if (lane == 0) {
+            out3[0] = 0;
+            out3[1] = 0;
+            out3[2] = 0;
+        }
+        return;
+    }
+    long long total = 0;
+    for (int r = lane; r < num_reqs; r += 32) total += query_lens[r];
+    for (int o = 16; o > 0; o >>= 1) total += __shfl_xor_sync(0xffffffffu, total, o);
+    const long long best = total / 2;
+    // key = (|cum_k - best| << 24 | k) for k = 1 .. num_reqs-1 (cum_k: inclusive prefix at r = k-1)
+    unsigned long long my_best = ~0ull;
+    long long my_cum = 0, carry = 0;
+    for (int base = 0; base < num_reqs - 1; base += 32) {
+        const int r = base + lane;
+        long long x = r < num_reqs - 1 ? query_lens[r] : 0;
+        for (int o = 1; o < 32; o <<= 1) {
+            const long long y = __shfl_up_sync(0xffffffffu, x, o);
+            if (lane >= o) x += y;
+        }
+        if (r < num_reqs - 1) {
+            const long long cum = carry + x;
+            const long long diff = cum > best ? cum - best : best - cum;
+            const unsigned long long key = ((unsigned long long)diff << 24) | (unsigned long long)(r + 1);
+            if (key < my_best) {
+                my_best = key;
+                my_cum = cum;
+            }
+        }
+        carry += __shfl_sync(0xffffffffu, x, 31);
+    }
+    for (int o = 16; o > 0; o >>= 1) {
+        const unsigned long long y = __shfl_xor_sync(0xffffffffu, my_best, o);
+        const long long c = __shfl_xor_sync(0xffffffffu, my_cum, o);
+        if (y < my_best) {
+            my_best = y;
+            my_cum = c;
+        }
+    }
+    if (lane == 0) {
+        const int k = (int)(my_best & 0xFFFFFFull);
+        const long long n1 = my_cum;
+        const long long n2 = total - n1;
+        const long long small = n1 < n2 ? n1 : n2;
+        int use_two = 0;
+        if (small > 0) {
+            const long long gap = n1 > n2 ? n1 - n2 : n2 - n1;
+            const bool balanced = (double)gap / (double)small <= (double)balance_threshold;
+            use_two = balanced && small >= (long long)length_threshold;
+        }
+        out3[0] = k;
+        out3[1] = (int32_t)n1;
+        out3[2] = use_two;
+    }
+}
+
 }  // namespace
 
 cudaError_t launch_exp2_selftest(const float *x, float *poly, float *hw, int64_t n, cudaStream_t s)
@@ -332,6 +404,9 @@ cudaError_t launch_combine(const CombineParams &p, int head_dim, int grid, cudaS
 cudaError_t launch_split_microbatch(const int32_t *query_lens, int num_reqs, float balance_threshold,
                                     int32_t length_threshold, int32_t *out3, cudaStream_t s)
 {
+    if (num_reqs <= kSplitSmallMax)
+        return launch_pdl(true, split_small_kernel, dim3(1), dim3(32), 0, s, query_lens, num_reqs, balance_threshold,
+                          length_threshold, out3);
     return launch_pdl(true, split_kernel, dim3(1), dim3(kSplitThreads), 0, s, query_lens, num_reqs, balance_threshold,
                       length_threshold, out3);
 }
