@@ -777,9 +777,9 @@ def main():
                 "per_launch_flops": per_launch_flops, "per_launch_ms": round(per_launch_ms, 4),
                 "last_chunk_ms": round(float(km[:, -1].mean()), 4),
                 "last_chunk_tflops": round(chunk_flops((N_CHUNKS - 1) * CHUNK, CHUNK) / (km[:, -1].mean() * 1e-3) / 1e12, 2)}
-    # per chunk: split, [KV write,] plan, chunk attention, combine (a single
-    # prefill request launches no decode kernel)
-    launches = args.steps * N_CHUNKS * (4 if wl.fused else 5)
+    # per chunk: split, [KV write,] plan, chunk attention (a single prefill
+    # request launches neither the decode nor the combine kernel)
+    launches = args.steps * N_CHUNKS * (3 if wl.fused else 4)
 
     # the other variant of the step (two calls, or the fused call) on the same inputs
     other = {}
