@@ -653,6 +653,24 @@ def suite(dev):
     return out
 
 
+# ----------------------------------------------------------------------------- replicas
+def max_over_ranks(x, dist, dev):
+    """The largest value of x over all ranks (the slowest replica sets the job's
+    time); x itself when there is no process group."""
+    if dist is None:
+        return float(x)
+    import torch
+    t = torch.tensor([float(x)], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_tflops(world, flops_per_replica_step, steps, total_ms):
+    """Whole-job TFLOP/s: each of the `world` replicas does one step's FLOPs per
+    step, and the job takes the slowest replica's `total_ms` for `steps` steps."""
+    return world * flops_per_replica_step * steps / (total_ms * 1e-3) / 1e12
+
+
 # ----------------------------------------------------------------------------- main
 def main():
     ap = argparse.ArgumentParser()
@@ -732,14 +750,10 @@ def main():
     clocks.mark(t_wall, t_end)
     clk = clocks.stop()
     step_ms = [ev0[s].elapsed_time(ev1[s]) for s in range(args.steps)]
-    total_ms = float(sum(step_ms))
-    if dist:
-        t = torch.tensor([total_ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        total_ms = float(t.item())
+    total_ms = max_over_ranks(float(sum(step_ms)), dist, dev)
     flags = cpsa.cpp_read_device_error(wl.err)
     ms_per_step = total_ms / args.steps
-    value = world * STEP_FLOPS * args.steps / (total_ms * 1e-3) / 1e12
+    value = job_tflops(world, STEP_FLOPS, args.steps, total_ms)
 
     # end-to-end through host buffers
     h2d, d2h = wl.make_host()
@@ -755,7 +769,8 @@ def main():
         e1.record(stream)
         torch.cuda.synchronize()
         e2e_ms.append(e0.elapsed_time(e1))
-    e2e_val = world * STEP_FLOPS / (float(np.mean(e2e_ms)) * 1e-3) / 1e12
+    e2e_step_ms = max_over_ranks(float(np.mean(e2e_ms)), dist, dev)
+    e2e_val = job_tflops(world, STEP_FLOPS, 1, e2e_step_ms)
 
     # roofline of the dominant kernel (the tensor-core chunk kernel): separate steps
     # with events around every chunk-kernel launch (events between kernels keep
@@ -812,7 +827,7 @@ def main():
                        "l2": "flushed between steps (256 MB write)", "max_kv_splits": wl.max_kv_splits,
                        "step_flops": STEP_FLOPS},
             "e2e": {"value": round(e2e_val, 3), "unit": "TFLOP/s", "h2d_bytes_per_step": h2d,
-                    "d2h_bytes_per_step": d2h, "ms_per_step": round(float(np.mean(e2e_ms)), 4)},
+                    "d2h_bytes_per_step": d2h, "ms_per_step": round(e2e_step_ms, 4)},
             "roofline": roofline, "gpu_launches": launches, "clocks": clk,
             "tokens_per_s": round(world * SEQ / (ms_per_step * 1e-3), 1),
             "step_roofline": step_roofline(ms_per_step, peak_tf, peak_bw),
