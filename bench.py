@@ -410,7 +410,7 @@ def kv_write_bandwidth(dev, reps=5):
     return res
 
 
-def serving_loop(dev, chunk_caps=(), tile_align=0, budget=2048, n_req=32, decode_tokens=32, seed=11):
+def serving_loop(dev, chunk_caps=(), tile_align=0, budget=2048, n_req=32, decode_tokens=32, seed=11, fused=True):
     """Closed loop: the library's token-budget batch builder sizes every step
     (decode rows first, then started prompts, then new ones) and allocates pages;
     each step runs the KV write and the attention kernels on it. Llama-3-8B
@@ -452,9 +452,13 @@ def serving_loop(dev, chunk_caps=(), tile_align=0, budget=2048, n_req=32, decode
         meta = [torch.from_numpy(x).to(dev, non_blocking=True) for x in (ql, sl, b["block_table"], b["slot_mapping"])]
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         e0.record(stream)
-        cpsa.cpp_kv_cache_write(kp[:T], vp[:T], meta[3], kc, vc, err, stream=stream)
-        cpsa.cpp_chunked_prefill_attn(qp[:T], kc, vc, meta[0], meta[1], meta[2], out[:T], ws, err,
-                                      max_kv_splits=8, stream=stream)
+        if fused:
+            cpsa.cpp_chunked_prefill_attn_write_kv(qp[:T], kp[:T], vp[:T], meta[3], kc, vc, meta[0], meta[1],
+                                                   meta[2], out[:T], ws, err, max_kv_splits=8, stream=stream)
+        else:
+            cpsa.cpp_kv_cache_write(kp[:T], vp[:T], meta[3], kc, vc, err, stream=stream)
+            cpsa.cpp_chunked_prefill_attn(qp[:T], kc, vc, meta[0], meta[1], meta[2], out[:T], ws, err,
+                                          max_kv_splits=8, stream=stream)
         e1.record(stream)
         evs.append((e0, e1))
         dec = ql == 1
@@ -621,7 +625,8 @@ def suite(dev):
                     "32/8 heads d128; every step sized by the library's batch builder",
         "budget_only": serving_loop(dev),
         "progressive_2048_1024_512": serving_loop(dev, chunk_caps=(2048, 1024, 512)),
-        "budget_tile_128": serving_loop(dev, tile_align=128)}
+        "budget_tile_128": serving_loop(dev, tile_align=128),
+        "budget_only_two_calls": serving_loop(dev, fused=False)}
     # --- micro-batch workload: one stream vs the balanced split on two streams
     spec = W.spec_microbatch()
     d = W.device_batch(spec, device=dev)

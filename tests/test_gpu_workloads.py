@@ -72,7 +72,7 @@ def test_llama_chunk_sampled_rows(cuda_lib, history):
     compare(got, ref, what=f"llama chunk h={history}")
 
 
-def _sampled_parity(cuda_lib, spec, sample_reqs, rows_per_req, seed):
+def _sampled_parity(cuda_lib, spec, sample_reqs, rows_per_req, seed, fused=False):
     import torch
     d = W.device_batch(spec)
     B, T = len(spec.qlen), sum(spec.qlen)
@@ -88,11 +88,26 @@ def _sampled_parity(cuda_lib, spec, sample_reqs, rows_per_req, seed):
     out = torch.empty_like(d["q"])
     ws = torch.empty(cuda_lib.cpp_attn_workspace_bytes(B, T, spec.num_q_heads, spec.num_kv_heads, spec.head_dim, 8),
                      dtype=torch.uint8, device="cuda")
-    cuda_lib.cpp_kv_cache_write(d["k"], d["v"], d["slot_mapping"], d["k_cache"], d["v_cache"], err)
-    cuda_lib.cpp_chunked_prefill_attn(d["q"], d["k_cache"], d["v_cache"], d["query_lens"], d["seq_lens"],
-                                      d["block_table"], out, ws, err, max_kv_splits=8)
+    if fused:
+        cuda_lib.cpp_chunked_prefill_attn_write_kv(d["q"], d["k"], d["v"], d["slot_mapping"], d["k_cache"],
+                                                   d["v_cache"], d["query_lens"], d["seq_lens"], d["block_table"],
+                                                   out, ws, err, max_kv_splits=8)
+    else:
+        cuda_lib.cpp_kv_cache_write(d["k"], d["v"], d["slot_mapping"], d["k_cache"], d["v_cache"], err)
+        cuda_lib.cpp_chunked_prefill_attn(d["q"], d["k_cache"], d["v_cache"], d["query_lens"], d["seq_lens"],
+                                          d["block_table"], out, ws, err, max_kv_splits=8)
     torch.cuda.synchronize()
     assert cuda_lib.cpp_read_device_error(err) == 0
+    # the sampled requests' new rows sit in their cache slots, bit for bit
+    cu0 = np.concatenate([[0], np.cumsum(spec.qlen)])
+    slots_h = d["slot_mapping"].cpu().numpy()
+    for r in sample_reqs:
+        t0, t1 = int(cu0[r]), int(cu0[r + 1])
+        s = torch.from_numpy(slots_h[t0:t1]).cuda()
+        rows_k = d["k_cache"][s // P, :, s % P]          # [tokens, Hkv, D]
+        rows_v = d["v_cache"][s // P, :, s % P]
+        assert torch.equal(rows_k.view(torch.int16), d["k"][t0:t1].view(torch.int16))
+        assert torch.equal(rows_v.view(torch.int16), d["v"][t0:t1].view(torch.int16))
     cu = np.concatenate([[0], np.cumsum(spec.qlen)])
     rng = np.random.default_rng(seed)
     gots, refs = [], []
@@ -109,21 +124,24 @@ def _sampled_parity(cuda_lib, spec, sample_reqs, rows_per_req, seed):
     return np.concatenate(gots), np.concatenate(refs), d, out
 
 
-def test_sarathi_mixed_sampled(cuda_lib):
-    """1536 decode rows (context U[1024, 8192]) + one 512-token chunk at h = 8192, page 16."""
+@pytest.mark.parametrize("fused", [False, True])
+def test_sarathi_mixed_sampled(cuda_lib, fused):
+    """1536 decode rows (context U[1024, 8192]) + one 512-token chunk at h = 8192, page 16;
+    the KV write as its own call or fused into the attention call."""
     spec = W.spec_sarathi_mixed()
     rng = np.random.default_rng(33)
     reqs = sorted(set(rng.choice(1536, 24, replace=False).tolist()) | {0, 1535, 1536})
-    got, ref, _, _ = _sampled_parity(cuda_lib, spec, reqs, rows_per_req=24, seed=34)
-    compare(got, ref, what="sarathi mixed")
+    got, ref, _, _ = _sampled_parity(cuda_lib, spec, reqs, rows_per_req=24, seed=34, fused=fused)
+    compare(got, ref, what="sarathi mixed" + (" (fused)" if fused else ""))
 
 
-def test_microbatch_sampled(cuda_lib):
+@pytest.mark.parametrize("fused", [False, True])
+def test_microbatch_sampled(cuda_lib, fused):
     """128 decode rows (context U[2600, 5200]) + 64 prompts of 2600 tokens, page 16."""
     spec = W.spec_microbatch()
     reqs = [0, 5, 77, 127, 128, 150, 191]
-    got, ref, _, _ = _sampled_parity(cuda_lib, spec, reqs, rows_per_req=16, seed=35)
-    compare(got, ref, what="microbatch")
+    got, ref, _, _ = _sampled_parity(cuda_lib, spec, reqs, rows_per_req=16, seed=35, fused=fused)
+    compare(got, ref, what="microbatch" + (" (fused)" if fused else ""))
 
 
 def test_two_streams_match_one(cuda_lib):
