@@ -74,7 +74,7 @@ def run_gpu_batch(cpsa, batch, max_kv_splits=8, workspace_bytes=None, scale=0.0,
     return bf16_tensor_to_f64(out), flags, kc, vc
 
 
-def run_gpu_batch_fused(cpsa, batch, max_kv_splits=8, scale=0.0, slot_mapping=None):
+def run_gpu_batch_fused(cpsa, batch, max_kv_splits=8, scale=0.0, slot_mapping=None, workspace_bytes=None):
     """History written by cpp_kv_cache_write into NaN-filled caches, then one
     cpp_chunked_prefill_attn_write_kv call that writes the new tokens and attends.
     Returns (out float64, flags, k_cache, v_cache)."""
@@ -88,8 +88,10 @@ def run_gpu_batch_fused(cpsa, batch, max_kv_splits=8, scale=0.0, slot_mapping=No
                                 to_dev(batch.hist_slot_mapping), kc, vc, err)
     T = batch.num_tokens
     B = len(s.qlen)
-    ws = torch.empty(cpsa.cpp_attn_workspace_bytes(B, T, s.num_q_heads, s.num_kv_heads, s.head_dim, max_kv_splits),
-                     dtype=torch.uint8, device="cuda")
+    if workspace_bytes is None:
+        workspace_bytes = cpsa.cpp_attn_workspace_bytes(B, T, s.num_q_heads, s.num_kv_heads, s.head_dim,
+                                                        max_kv_splits)
+    ws = torch.empty(workspace_bytes, dtype=torch.uint8, device="cuda")
     out = torch.full((T, s.num_q_heads, s.head_dim), float("nan"), dtype=torch.bfloat16, device="cuda")
     sm = batch.slot_mapping if slot_mapping is None else slot_mapping
     cpsa.cpp_chunked_prefill_attn_write_kv(to_dev_bf16(batch.q), to_dev_bf16(batch.k), to_dev_bf16(batch.v),

@@ -237,3 +237,18 @@ def test_fused_events_entry_point(cuda_lib):
     assert np.array_equal(a.view(np.uint64), out.float().cpu().numpy().astype(np.float64).view(np.uint64))
     assert torch.equal(ka.view(torch.int16), kc.view(torch.int16))
     assert torch.equal(va.view(torch.int16), vc.view(torch.int16))
+
+
+def test_fused_workspace_clamp(cuda_lib):
+    """A workspace with room for the work lists only: nothing is split (flagged),
+    the output and the caches are still right."""
+    spec = W.BatchSpec(hist=[9000, 5000, 70], qlen=[1, 150, 300], num_q_heads=8, num_kv_heads=2, head_dim=128,
+                       page_size=16, seed=906)
+    b = W.make_batch(spec)
+    minb = cuda_lib.cpp_attn_workspace_min_bytes(3, b.num_tokens, 8, 2, 128, 8)
+    got, flags, kc, vc = run_gpu_batch_fused(cuda_lib, b, workspace_bytes=minb)
+    assert flags == cuda_lib.DEV_SPLITS_CLAMPED
+    okc, ovc = oracle_caches(b)
+    assert np.array_equal(cache_bits(kc), okc) and np.array_equal(cache_bits(vc), ovc)
+    ref = oracle.paged_attention(b.q, okc, ovc, b.query_lens, b.seq_lens, b.block_table)
+    compare(got, ref, what="fused, clamped workspace")
