@@ -21,16 +21,19 @@
 //   warps 0..7   softmax, one warpgroup per q head n; thread = query row:
 //                S row from TMEM, causal mask on the diagonal/tail tiles, online
 //                max/sum in fp32 (base-2 exponent, scale folded in), P as bf16
-//                back into TMEM over S; final O / l epilogue.
+//                back into TMEM over S; final O / l epilogue, or for a piece of
+//                a unit cut by the stream-K split, its partial or the merge of
+//                all the unit's pieces (whichever piece finishes last merges).
 //   warp 10      cache writer (fused KV write only): for each tile of new rows
 //                this CTA owns (the diagonal tile of head pair 0), TMA-loads its
 //                K and then its V rows into a staging buffer of its own and
 //                TMA-stores them to the cache pages slot_mapping names, apart
 //                from the attention pipeline (rows whose slots do not form whole
 //                page boxes are stored row by row).
-// Exponentials: in tiles without masked columns kFmaExpPairsPer8 of every 8
-// pairs go to the FMA pipe (exp2_poly_x2), the rest to MUFU ex2, so neither unit
-// sets the pace alone; the row sum and the exponent arguments use packed f32x2 arithmetic.
+// Exponentials: MUFU ex2. A build-time knob (kFmaExpPairsPer8, 0 by default:
+// measured fastest on GB300) sends that many of every 8 pairs of an unmasked
+// tile to the FMA pipe instead (exp2_poly_x2). The row sum and the exponent
+// arguments use packed f32x2 arithmetic.
 // Rescaling of O is lazy: the running maximum is only raised when a tile's
 // maximum exceeds it by more than 8 (a factor 256 in the exponent), which keeps
 // p <= 256 and leaves the final O / l unchanged.
