@@ -2,10 +2,12 @@
 // the attention kernels.
 //
 // One call of cpp_chunked_prefill_attn runs:
-//   plan      one CTA: scan of query_lens, validation, work lists, split choice
-//   chunk     tensor-core kernel over prefill items (query_len >= 2)
+//   plan      one CTA (one warp for up to 32 requests): scan of query_lens,
+//             validation, work lists, split choice, merge counters zeroed
+//   chunk     tensor-core kernel over prefill items (query_len >= 2); merges
+//             the units the stream-K cut split
 //   decode    split-KV kernel over decode items (query_len == 1)
-//   combine   merges the partial results of rows that were split along keys
+//   combine   merges the partial results of decode rows split along keys
 // The lists live in the caller's workspace; every kernel is persistent and reads
 // its item count from the workspace, so the host never needs the lengths.
 #pragma once

@@ -123,9 +123,11 @@ size_t cpp_attn_workspace_min_bytes(int num_reqs, int64_t num_tokens, int num_q_
  * depends only on the row's own seq_len and max_kv_splits. Prefill rows are split
  * stream-K style: the KV tiles of all prefill units of the batch (128 query rows
  * x kv head x q-head pair) are laid end to end and cut into equal runs, one per
- * CTA of the chunk kernel, and a unit cut by a run boundary is merged from fp32
- * partial results. Where the cuts fall depends on the whole batch, so a prefill
- * row's last-bit rounding (not its value) can depend on the other requests.
+ * CTA of the chunk kernel, and a unit cut by a run boundary is merged inside the
+ * chunk kernel from fp32 partial results (split decode rows by the combine
+ * kernel, launched only when the batch holds decode rows). Where the cuts fall
+ * depends on the whole batch, so a prefill row's last-bit rounding (not its
+ * value) can depend on the other requests; it does not depend on timing.
  * max_kv_splits = 1 turns off both kinds of split.
  * workspace: device memory of at least cpp_attn_workspace_min_bytes(...) with
  * the same (num_reqs, num_tokens, heads, head_dim, max_kv_splits); it is
@@ -143,8 +145,10 @@ int cpp_chunked_prefill_attn(const void *q, const void *k_cache, const void *v_c
  * cpp_chunked_prefill_attn with timing marks: when `events` is not NULL it
  * points to 5 cudaEvent_t handles (any may be NULL) recorded on `stream`:
  * [0] before the plan kernel, [1] before the chunk kernel, [2] after it,
- * [3] after the decode kernel, [4] after the combine kernel. For profiling
- * harnesses; the computation is identical.
+ * [3] after the decode kernel, [4] after the combine kernel (kernels that a
+ * batch does not need are not launched; their marks follow the previous one).
+ * For profiling harnesses; the computation is identical, its kernels launched
+ * in plain stream order.
  */
 int cpp_chunked_prefill_attn_events(const void *q, const void *k_cache, const void *v_cache,
                                     const int32_t *query_lens, const int32_t *seq_lens,
