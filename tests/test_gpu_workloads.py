@@ -275,3 +275,45 @@ def test_dynamic_chunks_sampled_rows(cuda_lib):
                                  rows=rows)
     got = out[torch.from_numpy(rows).cuda()].float().cpu().numpy().astype(np.float64)
     compare(got, ref, what="dynamic chunks")
+
+
+def test_fused_headline_step_sampled_rows(cuda_lib):
+    """The headline step exactly as the bench runs it (64 fused chunks of 512,
+    page 128, max_kv_splits 8): 64 rows of chunks 0, 1, 7, 31 and 63 (rows 0,
+    127, 128 and 511 always among them) against the oracle, and the cache bit for
+    bit after the last chunk."""
+    import torch
+    SEQ, C, P = 32768, 512, 128
+    q, k, v, slots, bt = W.device_sequence(SEQ, P)
+    n_pages = bt.shape[1]
+    kc = torch.full((n_pages, 8, P, 128), float("nan"), dtype=torch.bfloat16, device="cuda")
+    vc = kc.clone()
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    ws = torch.empty(cuda_lib.cpp_attn_workspace_bytes(1, C, 32, 8, 128, 8), dtype=torch.uint8, device="cuda")
+    out = torch.empty_like(q)
+    ql = torch.tensor([C], dtype=torch.int32, device="cuda")
+    for a in range(0, SEQ, C):
+        sl = torch.tensor([a + C], dtype=torch.int32, device="cuda")
+        cuda_lib.cpp_chunked_prefill_attn_write_kv(q[a:a + C], k[a:a + C], v[a:a + C], slots[a:a + C], kc, vc, ql,
+                                                   sl, bt, out[a:a + C], ws, err, max_kv_splits=8)
+    torch.cuda.synchronize()
+    assert cuda_lib.cpp_read_device_error(err) == 0
+    # cache: page bt[0, j] holds positions j*P .. j*P+P-1 of the prompt
+    npg = SEQ // P
+    assert np.array_equal(_u16(kc[bt[0].long()]), _u16(k).reshape(npg, P, 8, 128).transpose(0, 2, 1, 3))
+    assert np.array_equal(_u16(vc[bt[0].long()]), _u16(v).reshape(npg, P, 8, 128).transpose(0, 2, 1, 3))
+    # oracle: the whole prompt as one request on identity pages; row t sees keys 0..t
+    kk = np.full((npg, 8, P, 128), W.BF16_NAN_SENTINEL, dtype=np.uint16)
+    vv = kk.copy()
+    pos = np.arange(SEQ)
+    oracle.kv_cache_write(_u16(k), _u16(v), ((pos // P) * P + pos % P).astype(np.int64), P, kk, vv)
+    rng = np.random.default_rng(63)
+    rows = []
+    for ci in (0, 1, 7, 31, 63):
+        fixed = np.array([0, 127, 128, C - 1])
+        pick = np.concatenate([fixed, rng.choice(np.setdiff1d(np.arange(C), fixed), 60, replace=False)])
+        rows.append(ci * C + pick)
+    rows = np.sort(np.concatenate(rows))
+    ref = oracle.paged_attention(_u16(q), kk, vv, [SEQ], [SEQ], np.arange(npg, dtype=np.int32)[None, :], rows=rows)
+    got = out[torch.from_numpy(rows).cuda()].float().cpu().numpy().astype(np.float64)
+    compare(got, ref, what="headline step, sampled rows")
