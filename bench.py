@@ -824,6 +824,7 @@ def main():
 
     line = {"metric": METRIC, "value": round(value, 3), "unit": "TFLOP/s", "n_gpus": world,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_per_step, 4),
+            "ms_per_step_median": round(float(np.median(step_ms)), 4),
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
             "data": "synthetic (seeded N(0,1) bf16 q/k/v, permuted page pool)",
             "config": {"workload": WORKLOAD, "global_batch": world, "seq_len": SEQ, "chunk": CHUNK,
