@@ -276,7 +276,7 @@ __device__ T block_sum(T x)
 
 __global__ void __launch_bounds__(kPlanThreads, 1) plan_kernel(PlanParams p)
 {
-    pdl_trigger();
+    // dependents are released at the end (see plan_small_kernel)
     pdl_wait();
     // ---- pass 1: tokens, prefill tiles, decode partial rows
     long long tok = 0, tiles = 0, dprows = 0;
@@ -386,6 +386,7 @@ __global__ void __launch_bounds__(kPlanThreads, 1) plan_kernel(PlanParams p)
         p.counts[kCntSplitUnits] = carry_b[5];
         for (int j = kCntSplitUnits + 1; j < kCntSlots; ++j) p.counts[j] = 0;
     }
+    pdl_trigger();
 }
 
 // The same lists for a batch of at most 32 requests, built by one warp: lane r
@@ -394,7 +395,9 @@ __global__ void __launch_bounds__(kPlanThreads, 1) plan_kernel(PlanParams p)
 // totals of the ones before it (one pass, no block-wide barriers).
 __global__ void __launch_bounds__(32, 1) plan_small_kernel(PlanParams p)
 {
-    pdl_trigger();
+    // The attention kernels that follow are released only at the end: CTAs
+    // launched early wait beside this warp and halve its speed (measured), while
+    // what they would overlap is short.
     pdl_wait();
     const int lane = threadIdx.x;
     const bool mine = lane < p.num_reqs;
@@ -466,6 +469,7 @@ __global__ void __launch_bounds__(32, 1) plan_small_kernel(PlanParams p)
     } else if (lane > kCntSplitUnits && lane < kCntSlots) {
         p.counts[lane] = 0;
     }
+    pdl_trigger();
 }
 
 }  // namespace

@@ -240,7 +240,6 @@ chunk_attn_kernel(const ChunkParams p, const __grid_constant__ CUtensorMap tm_q,
         tmem_relinquish();
     }
     // the set-up above touches no global memory; from here on the plan's output
-    pdl_trigger();
     pdl_wait();
     if (threadIdx.x == 0) {
         // this CTA's run of pieces, from the plan's table
@@ -766,6 +765,9 @@ chunk_attn_kernel(const ChunkParams p, const __grid_constant__ CUtensorMap tm_q,
 
     if (threadIdx.x == 0 && bars->abort)
         set_dev_error(p.dev_err, CPSA_DEV_WAIT_TIMEOUT);
+    // The next kernels are released only as CTAs finish: launched at the start
+    // they would wait beside this CTA's warps for its whole run (measured slower).
+    pdl_trigger();
     tc_fence_before_sync();
     __syncthreads();
     if (warp == C::kMmaWarp) {
