@@ -122,55 +122,69 @@ __device__ Counts request_work(const PlanParams &p, int r, const Req &rq, int ti
         }
         return c;
     }
-    // prefill units in order: query tiles (longest KV range first), kv heads, head pairs
+    // prefill units in order: query tiles (longest KV range first), kv heads, head
+    // pairs. Lane l of pass g0 takes unit g = g0 + l, the a-th query tile from the
+    // last; its first tile is found in closed form (unit_tiles is hb + qt + 1 for
+    // every query tile but the last, which may be short).
+    static_assert(kTileM == kTileN, "unit tile counts assume square tiles");
     const int pairs = p.group / p.nq;
     const int upq = p.Hkv * pairs;            // units per query tile
     const int nqt = ceil_div(rq.q, kTileM);
-    int tile_run = tile_off;
-    for (int qt = nqt - 1; qt >= 0; --qt) {
-        const int i0 = qt * kTileM;
-        const int rows = min(kTileM, rq.q - i0);
-        const int nkv = unit_tiles(p, rq, qt, rows);
-        for (int jb = 0; jb < upq; jb += 32) {
-            const int j = jb + lane;
-            const bool active = j < upq;
-            const int u0 = tile_run + j * nkv, u1 = u0 + nkv;
-            const int np = active ? (cut ? (u1 - 1) / run - u0 / run + 1 : 1) : 0;
-            const bool split = np > 1;
-            int t_np, t_su, t_pr;
-            const int e_np = warp_excl_scan(np, lane, t_np);
-            const int e_su = warp_excl_scan(split ? 1 : 0, lane, t_su);
-            // a split unit's partials: kTileM rows x nq heads x np pieces (see the chunk kernel's merge)
-            const int e_pr = warp_excl_scan(split ? kTileM * p.nq * np : 0, lane, t_pr);
-            if (emit && active) {
-                const int kvh = j / pairs, hp = j % pairs;
-                const int pbase = split ? off.prows + c.prows + e_pr : -1;
-                const int pi = off.pieces + c.pieces + e_np;
-                // with cuts, every run starts a piece: the piece starting at tile
-                // c * run is the first of CTA c's run
-                if (!split) {
-                    p.pitems[pi] = PrefillItem{r, i0, kvh | (hp << 16), 0, nkv, (1 << 16), -1, u0 / run};
-                    if (cut && u0 % run == 0)
-                        p.run_first[u0 / run] = pi;
-                } else {
-                    const int sunit = off.sunits + c.sunits + e_su;
-                    int x = u0;
-                    for (int pc = 0; pc < np; ++pc) {
-                        const int owner = x / run;
-                        const int end = min(u1, (owner + 1) * run);
-                        p.pitems[pi + pc] =
-                            PrefillItem{r, i0, kvh | (hp << 16), x - u0, end - u0, pc | (np << 16), pbase, sunit};
-                        if (x == owner * run)
-                            p.run_first[owner] = pi + pc;
-                        x = end;
-                    }
+    const int hb = ceil_div(rq.hist, kTileN);
+    const int nkv_last = unit_tiles(p, rq, nqt - 1, rq.q - (nqt - 1) * kTileM);
+    const int prow_unit = kTileM * p.nq;      // partial rows of one piece of a split unit
+    const unsigned lanes_below = (1u << lane) - 1u;
+    for (int g0 = 0; g0 < nqt * upq; g0 += 32) {
+        const int g = g0 + lane;
+        const bool active = g < nqt * upq;
+        const int a = g / upq, j = g - a * upq;
+        const int qt = nqt - 1 - a;
+        const int nkv = a == 0 ? nkv_last : hb + qt + 1;
+        // tiles of the units of query tiles nqt - 1 .. qt + 1: nkv_last, then hb + nqt - a' for a' = 1 .. a - 1
+        const int before = a == 0 ? 0 : nkv_last + (a - 1) * (hb + nqt) - (a - 1) * a / 2;
+        const int u0 = tile_off + upq * before + j * nkv, u1 = u0 + nkv;
+        const int first = u0 / run;
+        const int np = active ? (cut ? (u1 - 1) / run - first + 1 : 1) : 0;
+        const bool split = np > 1;
+        // one scan for two sums: pieces (low word) and pieces of split units (high word)
+        long long sc = (long long)np | ((long long)(split ? np : 0) << 32);
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const long long y = __shfl_up_sync(0xffffffffu, sc, o);
+            if (lane >= o) sc += y;
+        }
+        const long long tot = __shfl_sync(0xffffffffu, sc, 31);
+        const long long ex = sc - ((long long)np | ((long long)(split ? np : 0) << 32));
+        const unsigned split_lanes = __ballot_sync(0xffffffffu, split);
+        if (emit && active) {
+            const int kvh = j / pairs, hp = j - kvh * pairs;
+            const int i0 = qt * kTileM;
+            const int pi = off.pieces + c.pieces + (int)(ex & 0xffffffffll);
+            // with cuts, every run starts a piece: the piece starting at tile
+            // c * run is the first of CTA c's run
+            if (!split) {
+                p.pitems[pi] = PrefillItem{r, i0, kvh | (hp << 16), 0, nkv, (1 << 16), -1, first};
+                if (cut && u0 == first * run)
+                    p.run_first[first] = pi;
+            } else {
+                // a split unit's partials: kTileM rows x nq heads x np pieces (see the chunk kernel's merge)
+                const int pbase = off.prows + c.prows + prow_unit * (int)(ex >> 32);
+                const int sunit = off.sunits + c.sunits + __popc(split_lanes & lanes_below);
+                int x = u0;
+                for (int pc = 0; pc < np; ++pc) {
+                    const int owner = first + pc;
+                    const int end = min(u1, (owner + 1) * run);
+                    p.pitems[pi + pc] =
+                        PrefillItem{r, i0, kvh | (hp << 16), x - u0, end - u0, pc | (np << 16), pbase, sunit};
+                    if (x == owner * run)
+                        p.run_first[owner] = pi + pc;
+                    x = end;
                 }
             }
-            c.pieces += t_np;
-            c.sunits += t_su;
-            c.prows += t_pr;
         }
-        tile_run += upq * nkv;
+        c.pieces += (int)(tot & 0xffffffffll);
+        c.sunits += __popc(split_lanes);
+        c.prows += prow_unit * (int)(tot >> 32);
     }
     return c;
 }

@@ -45,7 +45,7 @@ constexpr int kMergeCounters = 2 * 4;          // per split unit: q heads (<= 2)
 // aux: for a whole unit (npieces = 1) the CTA that processes it; for a piece of
 // a split unit, the unit's ordinal among the batch's split units (its merge
 // counters), its partial rows at pbase.
-struct PrefillItem {
+struct alignas(16) PrefillItem {
     int32_t r, i0, kvh_hp, kt0, kt1, piece_np, pbase, aux;
 };
 
