@@ -370,6 +370,18 @@ __host__ __device__ constexpr uint32_t idesc_bf16_f32(int M, int N, bool b_mn_ma
 // ---------------------------------------------------------------------------
 // math
 // ---------------------------------------------------------------------------
+// 16-byte asynchronous copy global -> shared, cached in L2 only (the source
+// may have been written by another SM); completion by cp_async_wait_all.
+__device__ __forceinline__ void cp_async_cg16(void *smem_dst, const void *gmem_src)
+{
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_u32(smem_dst)), "l"(gmem_src) : "memory");
+}
+
+__device__ __forceinline__ void cp_async_wait_all()
+{
+    asm volatile("cp.async.commit_group;\n\tcp.async.wait_group 0;" ::: "memory");
+}
+
 __device__ __forceinline__ float ex2_approx(float x)
 {
     float y;

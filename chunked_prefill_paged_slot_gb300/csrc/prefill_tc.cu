@@ -52,6 +52,11 @@ namespace {
 #endif
 constexpr int kFmaExpPairsPer8 = CPSA_FMA_EXP_PAIRS_PER_8;
 
+// The staged merge (merge_split_row_staged): pieces besides the merging one, and
+// the shared memory each softmax warp takes for them.
+constexpr int kMergeMaxOthers = 3;
+constexpr int kMergeStageBytes = kMergeMaxOthers * 2 * 32 * 128;   // others x 2 column blocks x 32 rows x 128 B
+
 template <int D, int NQ>
 struct ChunkCfg {
     static constexpr int kHalves = D / 64;             // 128-byte swizzle atoms across a row
@@ -64,6 +69,8 @@ struct ChunkCfg {
     static constexpr int kBarOff = kStageOff + kTileBytes;
     static constexpr int kSmemBytes = kBarOff + 1024 + 1024;   // barriers + alignment slack
     static_assert(kSmemBytes <= 232448, "beyond the 227 KB of shared memory a CTA may have");
+    static_assert(D != 128 || NQ * 4 * kMergeStageBytes <= kSlotOff + kSlots * kTileBytes,
+                  "the staged merge uses the Q and K/V buffers");
     static constexpr int kThreads = 352;
     static constexpr int kLoadWarp = 8;
     static constexpr int kMmaWarp = 9;
@@ -137,6 +144,101 @@ __device__ __forceinline__ void store_tile_rows(const ChunkParams &p, const CUte
 // piece's own terms (its TMEM O, m, l) taken at its place, so the bits do not
 // depend on which piece merges; writes the bf16 row. Kept out of line so that
 // its registers do not weigh on the softmax loop.
+// The same merge at the end of a CTA's run, when the Q and K/V buffers are free:
+// the other pieces' partial columns come through shared memory, 64 columns at a
+// time for all of them at once (cp.async), so the L2 latency is paid twice
+// rather than once per piece and column block. Same sums in the same order as
+// merge_split_row, so the bits agree. stage: this warp's kMergeStageBytes.
+
+template <int D, int NQ>
+__device__ __noinline__ void merge_split_row_staged(const ChunkParams &p, uint32_t tO, const float2 *pml,
+                                                    const float4 *po, int piece, int npieces, int wg, int row,
+                                                    int lane, float m_use, float l, bool valid_row, int64_t out_off,
+                                                    float4 *stage)
+{
+    // (m, l) of every piece (at most kMergeMaxOthers + 1; loops unrolled so the
+    // arrays stay in registers)
+    float mq[kMergeMaxOthers + 1], lq[kMergeMaxOthers + 1];
+    float M = m_use;
+#pragma unroll
+    for (int q = 0; q <= kMergeMaxOthers; ++q) {
+        mq[q] = m_use;
+        lq[q] = l;
+        if (q < npieces && q != piece) {
+            const float2 ml = __ldcg(pml + (q * NQ + wg) * 128 + row);
+            mq[q] = ml.x;
+            lq[q] = ml.y;
+            M = fmaxf(M, ml.x);
+        }
+    }
+    const float Mref = M == -INFINITY ? 0.f : M;
+    float L = 0.f, fq[kMergeMaxOthers + 1];
+#pragma unroll
+    for (int q = 0; q <= kMergeMaxOthers; ++q) {
+        fq[q] = ex2_approx(mq[q] - Mref);
+        if (q < npieces)
+            L = fmaf(fq[q], lq[q], L);
+    }
+    const float inv_l = L > 0.f ? 1.f / L : 0.f;
+#pragma unroll 1
+    for (int c0 = 0; c0 < D / 32; c0 += 2) {
+        // columns [32 c0, 32 c0 + 64) of every other piece: float4 x of block cc of
+        // the qi-th other piece at stage[((qi * 2 + cc) * 8 + x) * 32 + lane]
+#pragma unroll
+        for (int q = 0; q <= kMergeMaxOthers; ++q) {
+            if (q < npieces && q != piece) {
+                const int qi = q - (q > piece ? 1 : 0);
+                const float4 *src = po + ((int64_t)(q * NQ + wg) * (D / 4) + c0 * 8) * 128 + row;
+#pragma unroll
+                for (int y = 0; y < 16; ++y) cp_async_cg16(stage + (qi * 16 + y) * 32 + lane, src + y * 128);
+            }
+        }
+        cp_async_wait_all();
+#pragma unroll 1
+        for (int cc = 0; cc < 2; ++cc) {
+            const int c = c0 + cc;
+            uint32_t r[32];
+            tmem_ld32(tO + c * 32, r);
+            tmem_wait_ld();
+            float acc[32];
+#pragma unroll
+            for (int x = 0; x < 32; ++x) acc[x] = 0.f;
+#pragma unroll
+            for (int q = 0; q <= kMergeMaxOthers; ++q) {
+                if (q >= npieces)
+                    continue;
+                float4 v[8];
+                if (q == piece) {
+#pragma unroll
+                    for (int x = 0; x < 8; ++x)
+                        v[x] = make_float4(__uint_as_float(r[4 * x]), __uint_as_float(r[4 * x + 1]),
+                                           __uint_as_float(r[4 * x + 2]), __uint_as_float(r[4 * x + 3]));
+                } else {
+                    const int qi = q - (q > piece ? 1 : 0);
+#pragma unroll
+                    for (int x = 0; x < 8; ++x) v[x] = stage[((qi * 2 + cc) * 8 + x) * 32 + lane];
+                }
+#pragma unroll
+                for (int x = 0; x < 8; ++x) {
+                    acc[4 * x] = fmaf(fq[q], v[x].x, acc[4 * x]);
+                    acc[4 * x + 1] = fmaf(fq[q], v[x].y, acc[4 * x + 1]);
+                    acc[4 * x + 2] = fmaf(fq[q], v[x].z, acc[4 * x + 2]);
+                    acc[4 * x + 3] = fmaf(fq[q], v[x].w, acc[4 * x + 3]);
+                }
+            }
+            if (valid_row) {
+                uint4 *dst = reinterpret_cast<uint4 *>(reinterpret_cast<__nv_bfloat16 *>(p.out) + out_off + c * 32);
+#pragma unroll
+                for (int x = 0; x < 4; ++x)
+                    dst[x] = make_uint4(pack_bf16x2(acc[8 * x + 0] * inv_l, acc[8 * x + 1] * inv_l),
+                                        pack_bf16x2(acc[8 * x + 2] * inv_l, acc[8 * x + 3] * inv_l),
+                                        pack_bf16x2(acc[8 * x + 4] * inv_l, acc[8 * x + 5] * inv_l),
+                                        pack_bf16x2(acc[8 * x + 6] * inv_l, acc[8 * x + 7] * inv_l));
+            }
+        }
+    }
+}
+
 template <int D, int NQ>
 __device__ __noinline__ void merge_split_row(const ChunkParams &p, uint32_t tO, const float2 *pml, const float4 *po,
                                              int piece, int npieces, int wg, int row, float m_use, float l,
@@ -150,7 +252,7 @@ __device__ __noinline__ void merge_split_row(const ChunkParams &p, uint32_t tO, 
     float L = 0.f;
     for (int q = 0; q < npieces; ++q) {
         const float2 ml = q == piece ? make_float2(m_use, l) : __ldcg(pml + (q * NQ + wg) * 128 + row);
-        L += ex2_approx(ml.x - Mref) * ml.y;
+        L = fmaf(ex2_approx(ml.x - Mref), ml.y, L);
     }
     const float inv_l = L > 0.f ? 1.f / L : 0.f;
 #pragma unroll 1
@@ -738,9 +840,22 @@ chunk_attn_kernel(const ChunkParams p, const __grid_constant__ CUtensorMap tm_q,
                     seen = __shfl_sync(0xffffffffu, seen, 0);
                     merge = seen == npieces - 1;
                 }
-                if (merge)
-                    merge_split_row<D, NQ>(p, tO, pml, po, piece, npieces, wg, row, m_use, l, valid_row,
-                                           (t_row * p.num_q_heads + h) * D);
+                if (merge) {
+                    // at the run's last item the Q and K/V buffers are free once the
+                    // other head's last P.V is done: the merge stages through them
+                    bool staged = false;
+                    if (D == 128 && it + 1 == it_end && npieces - 1 <= kMergeMaxOthers)
+                        staged = NQ == 1 || __all_sync(0xffffffffu, mbar_wait(&bars->o_done[NQ - 1 - wg],
+                                                                              (o_base - 1) & 1, abort));
+                    if (staged)
+                        merge_split_row_staged<D, NQ>(
+                            p, tO, pml, po, piece, npieces, wg, row, lane, m_use, l, valid_row,
+                            (t_row * p.num_q_heads + h) * D,
+                            reinterpret_cast<float4 *>(smem + (wg * 4 + sub) * kMergeStageBytes));
+                    else
+                        merge_split_row<D, NQ>(p, tO, pml, po, piece, npieces, wg, row, m_use, l, valid_row,
+                                               (t_row * p.num_q_heads + h) * D);
+                }
             } else {
                 const float inv_l = l > 0.f ? 1.f / l : 0.f;
 #pragma unroll
