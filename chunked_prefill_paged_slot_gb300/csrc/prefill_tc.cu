@@ -52,10 +52,11 @@ namespace {
 #endif
 constexpr int kFmaExpPairsPer8 = CPSA_FMA_EXP_PAIRS_PER_8;
 
-// The staged merge (merge_split_row_staged): pieces besides the merging one, and
-// the shared memory each softmax warp takes for them.
+// The merge of split units (merge_split_row): pieces besides the merging one,
+// and the shared memory each softmax warp takes for their bf16 partials when it
+// stages them (others x 32 rows x 128 columns x 2 B).
 constexpr int kMergeMaxOthers = 3;
-constexpr int kMergeStageBytes = kMergeMaxOthers * 2 * 32 * 128;   // others x 2 column blocks x 32 rows x 128 B
+constexpr int kMergeStageBytes = kMergeMaxOthers * 32 * 128 * 2;
 
 template <int D, int NQ>
 struct ChunkCfg {
@@ -144,20 +145,29 @@ __device__ __forceinline__ void store_tile_rows(const ChunkParams &p, const CUte
 // piece's own terms (its TMEM O, m, l) taken at its place, so the bits do not
 // depend on which piece merges; writes the bf16 row. Kept out of line so that
 // its registers do not weigh on the softmax loop.
-// The same merge at the end of a CTA's run, when the Q and K/V buffers are free:
-// the other pieces' partial columns come through shared memory, 64 columns at a
-// time for all of them at once (cp.async), so the L2 latency is paid twice
-// rather than once per piece and column block. Same sums in the same order as
-// merge_split_row, so the bits agree. stage: this warp's kMergeStageBytes.
-
-template <int D, int NQ>
-__device__ __noinline__ void merge_split_row_staged(const ChunkParams &p, uint32_t tO, const float2 *pml,
-                                                    const float4 *po, int piece, int npieces, int wg, int row,
-                                                    int lane, float m_use, float l, bool valid_row, int64_t out_off,
-                                                    float4 *stage)
+// bf16 of x, back in fp32 (round to nearest even, as pack_bf16x2)
+__device__ __forceinline__ float bf16_round(float x)
 {
-    // (m, l) of every piece (at most kMergeMaxOthers + 1; loops unrolled so the
-    // arrays stay in registers)
+    return __uint_as_float(pack_bf16x2(x, 0.f) << 16);
+}
+
+__device__ __forceinline__ void bf16x8_unpack(const uint4 &u, float *v)
+{
+    const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+        v[2 * k] = __uint_as_float(w[k] << 16);
+        v[2 * k + 1] = __uint_as_float(w[k] & 0xffff0000u);
+    }
+}
+
+// (m, l) of every piece of a split unit's row and the weights of the merge:
+// out = sum_q wq[q] * Ohat_q / L with wq[q] = 2^(m_q - M) l_q, L = sum_q wq[q],
+// Ohat_q = O_q / l_q as stored (bf16). At most kMergeMaxOthers + 1 pieces.
+template <int NQ>
+__device__ __forceinline__ float merge_weights(const float2 *pml, int piece, int npieces, int wg, int row, float m_use,
+                                               float l, float (&wq)[kMergeMaxOthers + 1])
+{
     float mq[kMergeMaxOthers + 1], lq[kMergeMaxOthers + 1];
     float M = m_use;
 #pragma unroll
@@ -172,77 +182,91 @@ __device__ __noinline__ void merge_split_row_staged(const ChunkParams &p, uint32
         }
     }
     const float Mref = M == -INFINITY ? 0.f : M;
-    float L = 0.f, fq[kMergeMaxOthers + 1];
+    float L = 0.f;
 #pragma unroll
     for (int q = 0; q <= kMergeMaxOthers; ++q) {
-        fq[q] = ex2_approx(mq[q] - Mref);
+        wq[q] = ex2_approx(mq[q] - Mref) * lq[q];
         if (q < npieces)
-            L = fmaf(fq[q], lq[q], L);
+            L += wq[q];
     }
-    const float inv_l = L > 0.f ? 1.f / L : 0.f;
-#pragma unroll 1
-    for (int c0 = 0; c0 < D / 32; c0 += 2) {
-        // columns [32 c0, 32 c0 + 64) of every other piece: float4 x of block cc of
-        // the qi-th other piece at stage[((qi * 2 + cc) * 8 + x) * 32 + lane]
+    return L > 0.f ? 1.f / L : 0.f;
+}
+
+// The merge of a split unit's row (see the epilogue): every piece's normalized
+// partial Ohat_q (this piece's own from its TMEM O, rounded to bf16 exactly as it
+// would have been stored) weighted in piece order, so the bits do not depend on
+// which piece merges; writes the bf16 row. Up to kMergeMaxOthers + 1 pieces.
+// The other pieces' partials come either straight from L2 (stage == nullptr) or,
+// at the end of a CTA's run when the Q and K/V buffers are free, all at once
+// through this warp's kMergeStageBytes of them (cp.async), so the L2 latency is
+// paid once. Kept out of line so that its registers do not weigh on the softmax
+// loop.
+template <int D, int NQ>
+__device__ __noinline__ void merge_split_row(const ChunkParams &p, uint32_t tO, const float2 *pml, const uint4 *ph,
+                                             int piece, int npieces, int wg, int row, int lane, float m_use, float l,
+                                             bool valid_row, int64_t out_off, uint4 *stage)
+{
+    float wq[kMergeMaxOthers + 1];
+    const float inv_L = merge_weights<NQ>(pml, piece, npieces, wg, row, m_use, l, wq);
+    const float inv_own = l > 0.f ? 1.f / l : 0.f;
+    if (stage != nullptr) {
 #pragma unroll
         for (int q = 0; q <= kMergeMaxOthers; ++q) {
             if (q < npieces && q != piece) {
                 const int qi = q - (q > piece ? 1 : 0);
-                const float4 *src = po + ((int64_t)(q * NQ + wg) * (D / 4) + c0 * 8) * 128 + row;
+                const uint4 *src = ph + (int64_t)(q * NQ + wg) * (D / 8) * 128 + row;
 #pragma unroll
-                for (int y = 0; y < 16; ++y) cp_async_cg16(stage + (qi * 16 + y) * 32 + lane, src + y * 128);
+                for (int j = 0; j < D / 8; ++j) cp_async_cg16(stage + (qi * (D / 8) + j) * 32 + lane, src + j * 128);
             }
         }
         cp_async_wait_all();
+    }
 #pragma unroll 1
-        for (int cc = 0; cc < 2; ++cc) {
-            const int c = c0 + cc;
-            uint32_t r[32];
-            tmem_ld32(tO + c * 32, r);
-            tmem_wait_ld();
-            float acc[32];
+    for (int c = 0; c < D / 32; ++c) {
+        uint32_t r[32];
+        tmem_ld32(tO + c * 32, r);
+        tmem_wait_ld();
+        float acc[32];
 #pragma unroll
-            for (int x = 0; x < 32; ++x) acc[x] = 0.f;
+        for (int x = 0; x < 32; ++x) acc[x] = 0.f;
 #pragma unroll
-            for (int q = 0; q <= kMergeMaxOthers; ++q) {
-                if (q >= npieces)
-                    continue;
-                float4 v[8];
-                if (q == piece) {
+        for (int q = 0; q <= kMergeMaxOthers; ++q) {
+            if (q >= npieces)
+                continue;
+            float v[32];
+            if (q == piece) {
 #pragma unroll
-                    for (int x = 0; x < 8; ++x)
-                        v[x] = make_float4(__uint_as_float(r[4 * x]), __uint_as_float(r[4 * x + 1]),
-                                           __uint_as_float(r[4 * x + 2]), __uint_as_float(r[4 * x + 3]));
-                } else {
-                    const int qi = q - (q > piece ? 1 : 0);
-#pragma unroll
-                    for (int x = 0; x < 8; ++x) v[x] = stage[((qi * 2 + cc) * 8 + x) * 32 + lane];
-                }
-#pragma unroll
-                for (int x = 0; x < 8; ++x) {
-                    acc[4 * x] = fmaf(fq[q], v[x].x, acc[4 * x]);
-                    acc[4 * x + 1] = fmaf(fq[q], v[x].y, acc[4 * x + 1]);
-                    acc[4 * x + 2] = fmaf(fq[q], v[x].z, acc[4 * x + 2]);
-                    acc[4 * x + 3] = fmaf(fq[q], v[x].w, acc[4 * x + 3]);
-                }
-            }
-            if (valid_row) {
-                uint4 *dst = reinterpret_cast<uint4 *>(reinterpret_cast<__nv_bfloat16 *>(p.out) + out_off + c * 32);
+                for (int x = 0; x < 32; ++x) v[x] = bf16_round(__uint_as_float(r[x]) * inv_own);
+            } else {
+                const int qi = q - (q > piece ? 1 : 0);
 #pragma unroll
                 for (int x = 0; x < 4; ++x)
-                    dst[x] = make_uint4(pack_bf16x2(acc[8 * x + 0] * inv_l, acc[8 * x + 1] * inv_l),
-                                        pack_bf16x2(acc[8 * x + 2] * inv_l, acc[8 * x + 3] * inv_l),
-                                        pack_bf16x2(acc[8 * x + 4] * inv_l, acc[8 * x + 5] * inv_l),
-                                        pack_bf16x2(acc[8 * x + 6] * inv_l, acc[8 * x + 7] * inv_l));
+                    bf16x8_unpack(stage != nullptr ? stage[(qi * (D / 8) + c * 4 + x) * 32 + lane]
+                                                   : __ldcg(ph + ((int64_t)(q * NQ + wg) * (D / 8) + c * 4 + x) * 128 + row),
+                                  v + 8 * x);
             }
+#pragma unroll
+            for (int x = 0; x < 32; ++x) acc[x] = fmaf(wq[q], v[x], acc[x]);
+        }
+        if (valid_row) {
+            uint4 *dst = reinterpret_cast<uint4 *>(reinterpret_cast<__nv_bfloat16 *>(p.out) + out_off + c * 32);
+#pragma unroll
+            for (int x = 0; x < 4; ++x)
+                dst[x] = make_uint4(pack_bf16x2(acc[8 * x + 0] * inv_L, acc[8 * x + 1] * inv_L),
+                                    pack_bf16x2(acc[8 * x + 2] * inv_L, acc[8 * x + 3] * inv_L),
+                                    pack_bf16x2(acc[8 * x + 4] * inv_L, acc[8 * x + 5] * inv_L),
+                                    pack_bf16x2(acc[8 * x + 6] * inv_L, acc[8 * x + 7] * inv_L));
         }
     }
 }
 
+// The same merge for units of more than kMergeMaxOthers + 1 pieces (long KV
+// ranges against short runs), every partial straight from L2; the same weights,
+// order and rounding as merge_split_row.
 template <int D, int NQ>
-__device__ __noinline__ void merge_split_row(const ChunkParams &p, uint32_t tO, const float2 *pml, const float4 *po,
-                                             int piece, int npieces, int wg, int row, float m_use, float l,
-                                             bool valid_row, int64_t out_off)
+__device__ __noinline__ void merge_split_row_any(const ChunkParams &p, uint32_t tO, const float2 *pml, const uint4 *ph,
+                                                 int piece, int npieces, int wg, int row, float m_use, float l,
+                                                 bool valid_row, int64_t out_off)
 {
     float M = m_use;
     for (int q = 0; q < npieces; ++q)
@@ -252,9 +276,10 @@ __device__ __noinline__ void merge_split_row(const ChunkParams &p, uint32_t tO, 
     float L = 0.f;
     for (int q = 0; q < npieces; ++q) {
         const float2 ml = q == piece ? make_float2(m_use, l) : __ldcg(pml + (q * NQ + wg) * 128 + row);
-        L = fmaf(ex2_approx(ml.x - Mref), ml.y, L);
+        L += ex2_approx(ml.x - Mref) * ml.y;
     }
-    const float inv_l = L > 0.f ? 1.f / L : 0.f;
+    const float inv_L = L > 0.f ? 1.f / L : 0.f;
+    const float inv_own = l > 0.f ? 1.f / l : 0.f;
 #pragma unroll 1
     for (int c = 0; c < D / 32; ++c) {
         uint32_t r[32];
@@ -264,37 +289,30 @@ __device__ __noinline__ void merge_split_row(const ChunkParams &p, uint32_t tO, 
 #pragma unroll
         for (int x = 0; x < 32; ++x) acc[x] = 0.f;
         for (int q = 0; q < npieces; ++q) {
-            float4 v[8];
-            float mq;
+            float v[32];
+            float2 ml;
             if (q == piece) {
-                mq = m_use;
+                ml = make_float2(m_use, l);
 #pragma unroll
-                for (int x = 0; x < 8; ++x)
-                    v[x] = make_float4(__uint_as_float(r[4 * x]), __uint_as_float(r[4 * x + 1]),
-                                       __uint_as_float(r[4 * x + 2]), __uint_as_float(r[4 * x + 3]));
+                for (int x = 0; x < 32; ++x) v[x] = bf16_round(__uint_as_float(r[x]) * inv_own);
             } else {
-                mq = __ldcg(pml + (q * NQ + wg) * 128 + row).x;
-                const float4 *src = po + ((int64_t)(q * NQ + wg) * (D / 4) + c * 8) * 128 + row;
+                ml = __ldcg(pml + (q * NQ + wg) * 128 + row);
 #pragma unroll
-                for (int x = 0; x < 8; ++x) v[x] = __ldcg(src + x * 128);
+                for (int x = 0; x < 4; ++x)
+                    bf16x8_unpack(__ldcg(ph + ((int64_t)(q * NQ + wg) * (D / 8) + c * 4 + x) * 128 + row), v + 8 * x);
             }
-            const float fq = ex2_approx(mq - Mref);
+            const float wq = ex2_approx(ml.x - Mref) * ml.y;
 #pragma unroll
-            for (int x = 0; x < 8; ++x) {
-                acc[4 * x] = fmaf(fq, v[x].x, acc[4 * x]);
-                acc[4 * x + 1] = fmaf(fq, v[x].y, acc[4 * x + 1]);
-                acc[4 * x + 2] = fmaf(fq, v[x].z, acc[4 * x + 2]);
-                acc[4 * x + 3] = fmaf(fq, v[x].w, acc[4 * x + 3]);
-            }
+            for (int x = 0; x < 32; ++x) acc[x] = fmaf(wq, v[x], acc[x]);
         }
         if (valid_row) {
             uint4 *dst = reinterpret_cast<uint4 *>(reinterpret_cast<__nv_bfloat16 *>(p.out) + out_off + c * 32);
 #pragma unroll
             for (int x = 0; x < 4; ++x)
-                dst[x] = make_uint4(pack_bf16x2(acc[8 * x + 0] * inv_l, acc[8 * x + 1] * inv_l),
-                                    pack_bf16x2(acc[8 * x + 2] * inv_l, acc[8 * x + 3] * inv_l),
-                                    pack_bf16x2(acc[8 * x + 4] * inv_l, acc[8 * x + 5] * inv_l),
-                                    pack_bf16x2(acc[8 * x + 6] * inv_l, acc[8 * x + 7] * inv_l));
+                dst[x] = make_uint4(pack_bf16x2(acc[8 * x + 0] * inv_L, acc[8 * x + 1] * inv_L),
+                                    pack_bf16x2(acc[8 * x + 2] * inv_L, acc[8 * x + 3] * inv_L),
+                                    pack_bf16x2(acc[8 * x + 4] * inv_L, acc[8 * x + 5] * inv_L),
+                                    pack_bf16x2(acc[8 * x + 6] * inv_L, acc[8 * x + 7] * inv_L));
         }
     }
 }
@@ -807,28 +825,33 @@ chunk_attn_kernel(const ChunkParams p, const __grid_constant__ CUtensorMap tm_q,
                 // own O at once (the usual case for the piece that ends a CTA's run);
                 // else it leaves its partial and counts itself in, and the piece whose
                 // count completes the set merges. No warp waits for another piece.
-                // Partials are column-major per (piece, head): float4 column j of row
-                // `row` at ((piece * NQ + wg) * D/4 + j) * 128 + row, so a warp's
-                // accesses are 512 contiguous bytes.
+                // Partials are O / l in bf16 (m and l in fp32 beside them), column-major
+                // per (piece, head): the 8 columns 8j .. 8j + 7 of row `row` as one
+                // 16-byte unit at ((piece * NQ + wg) * D/8 + j) * 128 + row, so a warp's
+                // accesses are 512 contiguous bytes. The unit's partial rows keep
+                // the fp32 row pitch of the workspace (decode partials share it).
                 const int piece = w.piece_np & 0xFFFF;
                 int *cnt = p.flags + ((int64_t)w.aux * NQ + wg) * 4 + sub;
-                float4 *po = reinterpret_cast<float4 *>(p.part_o) + (int64_t)w.pbase * (D / 4);
+                uint4 *ph = reinterpret_cast<uint4 *>(p.part_o) + (int64_t)w.pbase * (D / 4);
                 float2 *pml = reinterpret_cast<float2 *>(p.part_ml) + w.pbase;
                 int seen = lane == 0 ? ld_acquire_gpu(cnt) : 0;
                 seen = __shfl_sync(0xffffffffu, seen, 0);
                 bool merge = seen == npieces - 1;
                 if (!merge) {
-                    const int64_t pc = (int64_t)(piece * NQ + wg) * (D / 4);
+                    const float inv_own = l > 0.f ? 1.f / l : 0.f;
+                    uint4 *dst = ph + (int64_t)(piece * NQ + wg) * (D / 8) * 128 + row;
 #pragma unroll
                     for (int c = 0; c < D / 32; ++c) {
                         uint32_t r[32];
                         tmem_ld32(tO + c * 32, r);
                         tmem_wait_ld();
 #pragma unroll
-                        for (int x = 0; x < 8; ++x)
-                            po[(pc + c * 8 + x) * 128 + row] =
-                                make_float4(__uint_as_float(r[4 * x]), __uint_as_float(r[4 * x + 1]),
-                                            __uint_as_float(r[4 * x + 2]), __uint_as_float(r[4 * x + 3]));
+                        for (int x = 0; x < 4; ++x)
+                            dst[(c * 4 + x) * 128] =
+                                make_uint4(pack_bf16x2(__uint_as_float(r[8 * x + 0]) * inv_own, __uint_as_float(r[8 * x + 1]) * inv_own),
+                                           pack_bf16x2(__uint_as_float(r[8 * x + 2]) * inv_own, __uint_as_float(r[8 * x + 3]) * inv_own),
+                                           pack_bf16x2(__uint_as_float(r[8 * x + 4]) * inv_own, __uint_as_float(r[8 * x + 5]) * inv_own),
+                                           pack_bf16x2(__uint_as_float(r[8 * x + 6]) * inv_own, __uint_as_float(r[8 * x + 7]) * inv_own));
                     }
                     pml[(piece * NQ + wg) * 128 + row] = make_float2(m_use, l);
                     __syncwarp();
@@ -841,20 +864,22 @@ chunk_attn_kernel(const ChunkParams p, const __grid_constant__ CUtensorMap tm_q,
                     merge = seen == npieces - 1;
                 }
                 if (merge) {
-                    // at the run's last item the Q and K/V buffers are free once the
-                    // other head's last P.V is done: the merge stages through them
-                    bool staged = false;
-                    if (D == 128 && it + 1 == it_end && npieces - 1 <= kMergeMaxOthers)
-                        staged = NQ == 1 || __all_sync(0xffffffffu, mbar_wait(&bars->o_done[NQ - 1 - wg],
-                                                                              (o_base - 1) & 1, abort));
-                    if (staged)
-                        merge_split_row_staged<D, NQ>(
-                            p, tO, pml, po, piece, npieces, wg, row, lane, m_use, l, valid_row,
-                            (t_row * p.num_q_heads + h) * D,
-                            reinterpret_cast<float4 *>(smem + (wg * 4 + sub) * kMergeStageBytes));
-                    else
-                        merge_split_row<D, NQ>(p, tO, pml, po, piece, npieces, wg, row, m_use, l, valid_row,
-                                               (t_row * p.num_q_heads + h) * D);
+                    const int64_t out_off = (t_row * p.num_q_heads + h) * D;
+                    if (npieces - 1 <= kMergeMaxOthers) {
+                        // at the run's last item the Q and K/V buffers are free once the
+                        // other head's last P.V is done: the merge stages through them
+                        bool staged = false;
+                        if (D == 128 && it + 1 == it_end)
+                            staged = NQ == 1 || __all_sync(0xffffffffu, mbar_wait(&bars->o_done[NQ - 1 - wg],
+                                                                                  (o_base - 1) & 1, abort));
+                        merge_split_row<D, NQ>(p, tO, pml, ph, piece, npieces, wg, row, lane, m_use, l, valid_row,
+                                               out_off,
+                                               staged ? reinterpret_cast<uint4 *>(smem + (wg * 4 + sub) * kMergeStageBytes)
+                                                      : nullptr);
+                    } else {
+                        merge_split_row_any<D, NQ>(p, tO, pml, ph, piece, npieces, wg, row, m_use, l, valid_row,
+                                                   out_off);
+                    }
                 }
             } else {
                 const float inv_l = l > 0.f ? 1.f / l : 0.f;
