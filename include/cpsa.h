@@ -124,8 +124,9 @@ size_t cpp_attn_workspace_min_bytes(int num_reqs, int64_t num_tokens, int num_q_
  * stream-K style: the KV tiles of all prefill units of the batch (128 query rows
  * x kv head x q-head pair) are laid end to end and cut into equal runs, one per
  * CTA of the chunk kernel, and a unit cut by a run boundary is merged inside the
- * chunk kernel from fp32 partial results (split decode rows by the combine
- * kernel, launched only when the batch holds decode rows). Where the cuts fall
+ * chunk kernel from partial results (per piece O / l in bf16 with fp32 row max
+ * and sum; split decode rows by the combine kernel from fp32 partials, launched
+ * only when the batch holds decode rows). Where the cuts fall
  * depends on the whole batch, so a prefill row's last-bit rounding (not its
  * value) can depend on the other requests; it does not depend on timing.
  * max_kv_splits = 1 turns off both kinds of split.
