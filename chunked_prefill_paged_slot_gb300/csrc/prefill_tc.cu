@@ -821,8 +821,9 @@ chunk_attn_kernel(const ChunkParams p, const __grid_constant__ CUtensorMap tm_q,
             const int npieces = w.piece_np >> 16;
             if (npieces > 1) {
                 // A piece of a split unit. Every warp (32 rows) decides on its own:
-                // if every other piece has left its partial, it merges them with its
-                // own O at once (the usual case for the piece that ends a CTA's run);
+                // at the end of its CTA's run, if every other piece has left its
+                // partial, it merges them with its own O at once (the usual case:
+                // its partner pieces ran at the start of the next CTAs' runs);
                 // else it leaves its partial and counts itself in, and the piece whose
                 // count completes the set merges. No warp waits for another piece.
                 // Partials are O / l in bf16 (m and l in fp32 beside them), column-major
@@ -834,7 +835,7 @@ chunk_attn_kernel(const ChunkParams p, const __grid_constant__ CUtensorMap tm_q,
                 int *cnt = p.flags + ((int64_t)w.aux * NQ + wg) * 4 + sub;
                 uint4 *ph = reinterpret_cast<uint4 *>(p.part_o) + (int64_t)w.pbase * (D / 4);
                 float2 *pml = reinterpret_cast<float2 *>(p.part_ml) + w.pbase;
-                int seen = lane == 0 ? ld_acquire_gpu(cnt) : 0;
+                int seen = lane == 0 && it + 1 == it_end ? ld_acquire_gpu(cnt) : 0;
                 seen = __shfl_sync(0xffffffffu, seen, 0);
                 bool merge = seen == npieces - 1;
                 if (!merge) {
