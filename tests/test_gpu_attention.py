@@ -9,7 +9,7 @@ import pytest
 
 import oracle
 import workloads as W
-from helpers import bf16_tensor_to_f64, compare, oracle_caches, run_gpu_batch, to_dev, to_dev_bf16
+from helpers import bf16_tensor_to_f64, compare, oracle_caches, run_gpu_batch, run_gpu_batch_fused, to_dev, to_dev_bf16
 
 pytestmark = pytest.mark.gpu
 
@@ -171,3 +171,23 @@ def test_events_entry_point_on_a_mixed_batch(cuda_lib):
     okc, okv = oracle_caches(b)
     ref = oracle.paged_attention(b.q, okc, okv, b.query_lens, b.seq_lens, b.block_table)
     compare(bf16_tensor_to_f64(out), ref, what="events entry point")
+
+
+def test_split_merges_are_repeatable_bit_for_bit(cuda_lib):
+    """Units cut into 2 to 10+ pieces: whichever piece finishes last merges (at the
+    end of a CTA's run through shared memory, else from L2), and the merge sums in
+    piece order with the merging piece's own O rounded as it would have been
+    stored, so repeated calls give identical bits; the output matches the oracle."""
+    spec = W.BatchSpec(hist=[3000, 700, 12000, 64, 0], qlen=[300, 256, 40, 2, 600], num_q_heads=32,
+                       num_kv_heads=8, head_dim=128, page_size=16, seed=510)
+    b = W.make_batch(spec)
+    runs = [run_gpu_batch(cuda_lib, b)[0] for _ in range(4)]
+    runs += [run_gpu_batch_fused(cuda_lib, b)[0] for _ in range(4)]
+    for r in runs[1:4]:
+        assert np.array_equal(runs[0].view(np.uint64), r.view(np.uint64))
+    for r in runs[5:]:
+        assert np.array_equal(runs[4].view(np.uint64), r.view(np.uint64))
+    kc, vc = oracle_caches(b)
+    ref = oracle.paged_attention(b.q, kc, vc, b.query_lens, b.seq_lens, b.block_table)
+    compare(runs[0], ref, what="split merges")
+    compare(runs[4], ref, what="split merges, fused")
