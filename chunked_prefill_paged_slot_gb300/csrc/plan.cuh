@@ -34,6 +34,7 @@ namespace cpsa {
 // [h + 128 j, h + 128 j + 128), and the unit of query tile i has ceil(h / 128) +
 // i + 1 tiles (the same count whenever h is a multiple of 128).
 constexpr int kMinRunTiles = 4;             // shortest run of KV tiles per CTA
+constexpr int kCutCostTiles = 6;            // a run's extra item and merge when a unit is cut, in KV tiles
 constexpr int kMaxChunkGrid = 256;          // upper bound of the chunk kernel's grid (SMs)
 constexpr int kDecodeChunk = 64;            // keys per decode pipeline stage
 constexpr int kDecodeKeysPerSplit = 4096;   // keys per decode split (multiple of kDecodeChunk)
