@@ -22,7 +22,7 @@ struct AttnCommon {
     int num_q_heads, num_kv_heads, group;
     float scale_log2;          // scale * log2(e): scores go straight to the base-2 exponent
     void *out;                 // bf16 [T][Hq][D]
-    float *part_o;             // fp32 [rows][D] partial outputs of split rows
+    float *part_o;             // [rows][D] fp32 partial outputs of split rows (prefill pieces: O / l in bf16 in the same pitch)
     float *part_ml;            // fp32 [rows][2]  (max in log2 units, row sum)
     uint32_t *dev_err;
     // KV write fused into the attention (fused != 0): the new tokens' keys and

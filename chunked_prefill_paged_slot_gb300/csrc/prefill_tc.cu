@@ -22,8 +22,10 @@
 //                S row from TMEM, causal mask on the diagonal/tail tiles, online
 //                max/sum in fp32 (base-2 exponent, scale folded in), P as bf16
 //                back into TMEM over S; final O / l epilogue, or for a piece of
-//                a unit cut by the stream-K split, its partial or the merge of
-//                all the unit's pieces (whichever piece finishes last merges).
+//                a unit cut by the stream-K split, its partial (O / l in bf16,
+//                m and l in fp32) or the merge of all the unit's pieces
+//                (whichever piece finishes last merges; at the end of a run
+//                through the then idle Q and K/V buffers).
 //   warp 10      cache writer (fused KV write only): for each tile of new rows
 //                this CTA owns (the diagonal tile of head pair 0), TMA-loads its
 //                K and then its V rows into a staging buffer of its own and
