@@ -70,6 +70,15 @@ __device__ int longest_unit(const PlanParams &p, const Req &rq)
     return unit_tiles(p, rq, nqt - 1, rq.q - (nqt - 1) * kTileM);
 }
 
+// KV tiles of the request's shortest unit (its first query tile), INT_MAX for
+// decode / invalid / empty requests.
+__device__ int shortest_unit(const PlanParams &p, const Req &rq)
+{
+    if (!rq.valid || rq.q < 2)
+        return 0x7fffffff;
+    return unit_tiles(p, rq, 0, min(kTileM, rq.q));
+}
+
 __device__ int decode_splits(const Req &rq, int max_splits)
 {
     const int nch = ceil_div(rq.s, kDecodeChunk);
@@ -200,16 +209,19 @@ __device__ Counts request_work(const PlanParams &p, int r, const Req &rq, int ti
 }
 
 // Stream-K run length; cuts inside units only when splitting is allowed and the
-// partials' bound fits the workspace (else nothing is split and the flag is set),
-// and only when the batch's longest unit is more than kCutCostTiles beyond the
-// run: a cut costs its run a second item and, at the end, a merge (about that
-// many tiles of work, measured), while whole units cost at most their length.
+// partials' bound fits the workspace (else nothing is split and the flag is set).
+// A cut costs the run that holds it a second item and, at its end, a merge
+// (about kCutCostTiles tiles of work, measured). When every unit is at least a
+// run long, whole units land one per CTA (no run holds two unit starts) and cost
+// the longest unit's length: then, if that is within kCutCostTiles of the run,
+// nothing is cut.
 struct SplitChoice {
     int run, max_splits;
     bool split_prefill, clamped;
 };
 
-__device__ SplitChoice choose_split(const PlanParams &p, long long tiles, int longest, long long dprows)
+__device__ SplitChoice choose_split(const PlanParams &p, long long tiles, int shortest, int longest,
+                                    long long dprows)
 {
     const int grid = max(1, p.chunk_grid);
     SplitChoice c;
@@ -223,7 +235,7 @@ __device__ SplitChoice choose_split(const PlanParams &p, long long tiles, int lo
         c.split_prefill = false;
         c.clamped = true;
     }
-    if (c.split_prefill && longest <= c.run + kCutCostTiles)
+    if (c.split_prefill && shortest >= c.run && longest <= c.run + kCutCostTiles)
         c.split_prefill = false;
     return c;
 }
@@ -289,14 +301,18 @@ __device__ void block_scan(int (&v)[N], int (&tot)[N])
     __syncthreads();
 }
 
-__device__ int block_max(int x)
+// Block-wide maximum (hi) or minimum (!hi).
+__device__ int block_extreme(int x, bool hi)
 {
     __shared__ int red[kPlanThreads / 32];
-    for (int o = 16; o > 0; o >>= 1) x = max(x, __shfl_xor_sync(0xffffffffu, x, o));
+    for (int o = 16; o > 0; o >>= 1) {
+        const int y = __shfl_xor_sync(0xffffffffu, x, o);
+        x = hi ? max(x, y) : min(x, y);
+    }
     if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = x;
     __syncthreads();
-    int m = 0;
-    for (int w = 0; w < kPlanThreads / 32; ++w) m = max(m, red[w]);
+    int m = red[0];
+    for (int w = 1; w < kPlanThreads / 32; ++w) m = hi ? max(m, red[w]) : min(m, red[w]);
     __syncthreads();
     return m;
 }
@@ -321,7 +337,7 @@ __global__ void __launch_bounds__(kPlanThreads, 1) plan_kernel(PlanParams p)
     pdl_wait();
     // ---- pass 1: tokens, prefill tiles, decode partial rows
     long long tok = 0, tiles = 0, dprows = 0;
-    int longest = 0;
+    int longest = 0, shortest = 0x7fffffff;
     for (int base = 0; base < p.num_reqs; base += kPlanThreads) {
         const int r = base + threadIdx.x;
         if (r < p.num_reqs) {
@@ -329,6 +345,7 @@ __global__ void __launch_bounds__(kPlanThreads, 1) plan_kernel(PlanParams p)
             tok += rq.q > 0 ? rq.q : 0;   // invalid requests still occupy their rows
             tiles += prefill_tiles(p, rq);
             longest = max(longest, longest_unit(p, rq));
+            shortest = min(shortest, shortest_unit(p, rq));
             if (rq.valid && rq.q == 1) {
                 const int ns = decode_splits(rq, p.max_splits);
                 if (ns > 1) dprows += (long long)p.Hq * ns;
@@ -338,7 +355,8 @@ __global__ void __launch_bounds__(kPlanThreads, 1) plan_kernel(PlanParams p)
     tok = block_sum(tok);
     tiles = block_sum(tiles);
     dprows = block_sum(dprows);
-    longest = block_max(longest);
+    longest = block_extreme(longest, true);
+    shortest = block_extreme(shortest, false);
     if (tok != p.num_tokens) {
         if (threadIdx.x == 0) set_dev_error(p.dev_err, CPSA_DEV_TOKENS_MISMATCH);
         if (threadIdx.x < kCntSlots) p.counts[threadIdx.x] = 0;
@@ -346,7 +364,7 @@ __global__ void __launch_bounds__(kPlanThreads, 1) plan_kernel(PlanParams p)
         return;
     }
     const int grid = max(1, p.chunk_grid);
-    const SplitChoice sc = choose_split(p, tiles, longest, dprows);
+    const SplitChoice sc = choose_split(p, tiles, shortest, longest, dprows);
     const int run = sc.run, max_splits = sc.max_splits;
     const bool split_prefill = sc.split_prefill;
     if (sc.clamped && threadIdx.x == 0)
@@ -451,6 +469,7 @@ __global__ void __launch_bounds__(32, 1) plan_small_kernel(PlanParams p)
     const int tok = mine && rq.q > 0 ? rq.q : 0;   // invalid requests still occupy their rows
     const int tiles = mine ? prefill_tiles(p, rq) : 0;
     int longest = mine ? longest_unit(p, rq) : 0;
+    int shortest = mine ? shortest_unit(p, rq) : 0x7fffffff;
     int dprows = 0;
     if (mine && rq.valid && rq.q == 1) {
         const int ns = decode_splits(rq, p.max_splits);
@@ -460,6 +479,7 @@ __global__ void __launch_bounds__(32, 1) plan_small_kernel(PlanParams p)
     long long tok_sum = tok, tile_sum = tiles, dprow_sum = dprows;
     for (int o = 16; o > 0; o >>= 1) {
         longest = max(longest, __shfl_xor_sync(0xffffffffu, longest, o));
+        shortest = min(shortest, __shfl_xor_sync(0xffffffffu, shortest, o));
         tok_sum += __shfl_xor_sync(0xffffffffu, tok_sum, o);
         tile_sum += __shfl_xor_sync(0xffffffffu, tile_sum, o);
         dprow_sum += __shfl_xor_sync(0xffffffffu, dprow_sum, o);
@@ -478,7 +498,7 @@ __global__ void __launch_bounds__(32, 1) plan_small_kernel(PlanParams p)
     const int tile_off = warp_excl_scan(tiles, lane, tile_total);
     if (mine)
         p.cu_q[lane] = tok_off;
-    const SplitChoice sc = choose_split(p, tile_sum, longest, dprow_sum);
+    const SplitChoice sc = choose_split(p, tile_sum, shortest, longest, dprow_sum);
     if (sc.clamped && lane == 0)
         set_dev_error(p.dev_err, CPSA_DEV_SPLITS_CLAMPED);
     Counts off{0, 0, 0, 0, 0, 0};
