@@ -8,12 +8,14 @@
 //   pieces    the stream-K cut of all prefill units' KV tiles into one run per
 //             chunk-kernel CTA (see plan.cuh), decode items, combine items,
 // and stores the counts that the persistent kernels read.
-// Pass 1 sums tokens, prefill tiles (W) and decode partial rows, which fixes the
-// run length and whether the partials fit the workspace (if not, nothing is
-// split). Pass 2 walks the requests in chunks of 1024: one block scan gives each
-// request its token and tile offsets, a second gives its list offsets, and each
-// thread then writes its own request's entries. Batches of at most 32 requests
-// take a one-warp kernel that builds the same lists without block barriers.
+// Pass 1 sums tokens, prefill tiles (W) and decode partial rows and finds the
+// shortest and longest unit, which fix the run length, whether the partials fit
+// the workspace (if not, nothing is split) and whether units are cut at all (see
+// choose_split). Pass 2 walks the requests in chunks of 1024: one block scan
+// gives each request its token and tile offsets, a second its list offsets, and
+// a warp per request then writes that request's entries. Batches of at most 32
+// requests take a one-warp kernel that builds the same lists without block
+// barriers.
 #include "common.cuh"
 #include "plan.cuh"
 
@@ -108,8 +110,8 @@ __device__ __forceinline__ int warp_excl_scan(int x, int lane, int &total)
 
 // One request's work, walked by a whole warp (all arguments warp-uniform).
 // With emit == false only the counts are returned (warp-uniform); with
-// emit == true the entries are written at the given offsets, the lanes sharing
-// the units of each query tile and placing them by warp scans.
+// emit == true the entries are written at the given offsets, lane l of each pass
+// taking one unit and placing its pieces by a warp scan.
 // tile_off: global index of the request's first prefill tile; run: tiles per CTA
 // run; cut: whether a run boundary may split a unit (else a unit goes whole to
 // the run that holds its first tile).
