@@ -191,3 +191,18 @@ def test_split_merges_are_repeatable_bit_for_bit(cuda_lib):
     ref = oracle.paged_attention(b.q, kc, vc, b.query_lens, b.seq_lens, b.block_table)
     compare(runs[0], ref, what="split merges")
     compare(runs[4], ref, what="split merges, fused")
+
+
+@pytest.mark.parametrize("fused", [False, True])
+def test_short_histories_keep_units_whole(cuda_lib, fused):
+    """When every unit is at least a stream-K run long and the longest is within
+    a cut's cost of it, the plan keeps units whole, one per CTA (a 512-token chunk
+    at history 512; two such requests side by side): every row against the oracle."""
+    for hist, qlen, seed in (([512], [512], 520), ([512, 640], [512, 384], 521)):
+        spec = W.BatchSpec(hist=hist, qlen=qlen, num_q_heads=32, num_kv_heads=8, head_dim=128, page_size=128,
+                           seed=seed)
+        b = W.make_batch(spec)
+        got = (run_gpu_batch_fused if fused else run_gpu_batch)(cuda_lib, b)[0]
+        kc, vc = oracle_caches(b)
+        ref = oracle.paged_attention(b.q, kc, vc, b.query_lens, b.seq_lens, b.block_table)
+        compare(got, ref, what=f"whole units {hist}")
