@@ -55,19 +55,23 @@ KERNEL_SOURCES = [os.path.join(ROOT, "chunked_prefill_paged_slot_gb300", "csrc",
                   for x in ("prefill_tc.cu", "common.cuh", "plan.cu", "plan.cuh")]
 
 
+def source_code_only(text):
+    """C/CUDA source with its comments removed and whitespace collapsed."""
+    import re
+    text = re.sub(r"/\*.*?\*/", " ", text, flags=re.S)
+    text = re.sub(r"//[^\n]*", " ", text)
+    return " ".join(text.split())
+
+
 def kernel_source_digest():
     """sha256 over the chunk kernel's sources (the kernel and the plan that feeds it),
     comments and whitespace left out, so that only a change of code voids the
     recorded counters."""
     import hashlib
-    import re
     h = hashlib.sha256()
     for p in KERNEL_SOURCES:
         with open(p, "r") as f:
-            text = f.read()
-        text = re.sub(r"/\*.*?\*/", " ", text, flags=re.S)
-        text = re.sub(r"//[^\n]*", " ", text)
-        h.update(" ".join(text.split()).encode())
+            h.update(source_code_only(f.read()).encode())
     return h.hexdigest()
 
 

@@ -57,3 +57,15 @@ def test_reference_arm_runs_on_rank_zero_only():
                        cwd=ROOT, env=env, capture_output=True, text=True, timeout=300)
     assert r.returncode == 0, r.stderr[-2000:]
     assert r.stdout.strip() == ""
+
+
+def test_recorded_counters_follow_code_not_comments():
+    """The digest that keeps roofline.traffic tied to the sources it was measured
+    on ignores comments and layout but not code."""
+    sys.path.insert(0, ROOT)
+    import bench
+    a = "int f(int x) {\n    return x + 1;   // one more\n}\n"
+    b = "/* header */ int f(int x) { return x + 1; }"
+    c = "int f(int x) { return x + 2; }"
+    assert bench.source_code_only(a) == bench.source_code_only(b)
+    assert bench.source_code_only(a) != bench.source_code_only(c)
