@@ -123,7 +123,9 @@ size_t cpp_attn_workspace_min_bytes(int num_reqs, int64_t num_tokens, int num_q_
  * depends only on the row's own seq_len and max_kv_splits. Prefill rows are split
  * stream-K style: the KV tiles of all prefill units of the batch (128 query rows
  * x kv head x q-head pair) are laid end to end and cut into equal runs, one per
- * CTA of the chunk kernel, and a unit cut by a run boundary is merged inside the
+ * CTA of the chunk kernel (unless every unit is at least a run long and the
+ * longest within a few tiles of it: then units stay whole, one per CTA), and a
+ * unit cut by a run boundary is merged inside the
  * chunk kernel from partial results (per piece O / l in bf16 with fp32 row max
  * and sum; split decode rows by the combine kernel from fp32 partials, launched
  * only when the batch holds decode rows). Where the cuts fall
