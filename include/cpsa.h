@@ -125,12 +125,12 @@ size_t cpp_attn_workspace_min_bytes(int num_reqs, int64_t num_tokens, int num_q_
  * x kv head x q-head pair) are laid end to end and cut into equal runs, one per
  * CTA of the chunk kernel (unless every unit is at least a run long and the
  * longest within a few tiles of it: then units stay whole, one per CTA), and a
- * unit cut by a run boundary is merged inside the
- * chunk kernel from partial results (per piece O / l in bf16 with fp32 row max
- * and sum; split decode rows by the combine kernel from fp32 partials, launched
- * only when the batch holds decode rows). Where the cuts fall
- * depends on the whole batch, so a prefill row's last-bit rounding (not its
- * value) can depend on the other requests; it does not depend on timing.
+ * unit cut by a run boundary is merged inside the chunk kernel from partial
+ * results (per piece O / l in bf16 with fp32 row max and sum; split decode rows
+ * by the combine kernel from fp32 partials, launched only when the batch holds
+ * decode rows). Where the cuts fall depends on the whole batch, so a prefill
+ * row's last-bit rounding (not its value) can depend on the other requests; it
+ * does not depend on timing.
  * max_kv_splits = 1 turns off both kinds of split.
  * workspace: device memory of at least cpp_attn_workspace_min_bytes(...) with
  * the same (num_reqs, num_tokens, heads, head_dim, max_kv_splits); it is
