@@ -206,3 +206,12 @@ def test_short_histories_keep_units_whole(cuda_lib, fused):
         kc, vc = oracle_caches(b)
         ref = oracle.paged_attention(b.q, kc, vc, b.query_lens, b.seq_lens, b.block_table)
         compare(got, ref, what=f"whole units {hist}")
+
+
+def test_whole_units_in_the_block_plan(cuda_lib):
+    """More than 32 requests take the block-wide plan kernel; 40 requests of 128
+    rows at history 1024 (one kv head, one q-head pair) give 40 units of 9 tiles
+    against runs of 4, so units stay whole there too: every row against the oracle."""
+    spec = W.BatchSpec(hist=[1024] * 40, qlen=[128] * 40, num_q_heads=2, num_kv_heads=1, head_dim=64,
+                       page_size=64, seed=530)
+    check(cuda_lib, spec)
