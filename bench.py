@@ -701,8 +701,9 @@ def main():
     ap.add_argument("--two-call", action="store_true",
                     help="time the KV write and the attention as two calls (default: the fused call)")
     ap.add_argument("--profile-decode", action="store_true",
-                    help="only the mixed decode step with 128 decode rows (about 2.5 GB of cache), "
-                         "a small case for ncu captures of the decode kernel")
+                    help="only the mixed decode step with 128 decode rows (about 2.5 GB of cache), timed with "
+                         "CUDA events; an ncu --set full capture of this case once ended in a GPU fault (see the "
+                         "design notes on measurement) and is not to be repeated")
     args = ap.parse_args()
     if args.profile_decode:
         import torch
@@ -875,10 +876,42 @@ def main():
             line["suite"] = {"error": repr(e)}
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(host_inputs())
+    # the decode and KV-write bandwidths and a compact summary close the line, so
+    # that a reader who keeps only its tail still has them
+    for key in ("kv_write", "secondary"):
+        if key in line:
+            line[key] = line.pop(key)
+    if rank == 0 and not args.no_secondary:
+        line["summary"] = summary_of(line)
     if rank == 0:
         print(json.dumps(line), flush=True)
     if dist:
         dist.destroy_process_group()
+
+
+def summary_of(line):
+    """The secondary figures in a few keys: decode and KV-write HBM GB/s against the
+    measured copy bandwidth, the page-16 chunk and the micro-batch workload."""
+    out = {}
+    sec, kvw, su = line.get("secondary", {}), line.get("kv_write", {}), line.get("suite", {})
+    if "decode_hbm_gbs" in sec:
+        out["decode_hbm_gbs"] = round(sec["decode_hbm_gbs"], 1)
+        out["decode_frac_of_measured_hbm"] = sec.get("decode_frac_of_hbm")
+        out["decode_frac_of_nominal_8tbs"] = sec.get("decode_frac_of_nominal_8tbs")
+        out["sarathi_chunk_page16_ms"] = round(sec.get("chunk_kernel_ms", float("nan")), 4)
+        out["sarathi_chunk_page16_tflops"] = round(sec.get("chunk_tflops", float("nan")), 1)
+    for k, v in kvw.items():
+        if isinstance(v, dict) and "gbs" in v:
+            out[f"kv_write_{k}_gbs"] = v["gbs"]
+    mb = su.get("microbatch_two_streams", {})
+    if "two_vs_one" in mb:
+        out["microbatch_two_vs_one"] = round(mb["two_vs_one"], 4)
+        out["microbatch_prefill_tflops_one_stream"] = round(mb["prefill_tflops_one_stream"], 1)
+    if "tile_alignment_h8192" in su:
+        out["tile_alignment_h8192_ms"] = su["tile_alignment_h8192"]
+    out["headline_tflops"] = line.get("value")
+    out["roofline_frac"] = line.get("roofline", {}).get("frac")
+    return out
 
 
 def reference_arm(args, world, rank):

@@ -19,7 +19,8 @@ from ._lib import (  # noqa: F401
     cpp_chunked_prefill_attn, cpp_chunked_prefill_attn_events, cpp_chunked_prefill_attn_noalloc,
     cpp_chunked_prefill_attn_write_kv,
     cpp_split_microbatch, cpp_read_device_error, cpp_get_device_error, cpp_plan_chunk_sizes,
-    cpp_fit_latency_quadratic, cpp_fit_latency_two_var, cpp_selftest_exp2, OnlineChunker, BatchScheduler,
+    cpp_fit_latency_quadratic, cpp_fit_latency_two_var, cpp_selftest_exp2, cpp_selftest_wait_timeout,
+    OnlineChunker, BatchScheduler,
     DEV_SLOT_OUT_OF_RANGE, DEV_PAGE_OUT_OF_RANGE, DEV_SEQ_LT_QUERY, DEV_TOKENS_MISMATCH, DEV_SEQ_GT_TABLE,
     DEV_SPLITS_CLAMPED, DEV_WAIT_TIMEOUT,
 )

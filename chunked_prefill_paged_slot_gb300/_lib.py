@@ -105,6 +105,8 @@ def load():
     lib.cpp_sched_stats.argtypes = [_c_p, _c_p, _c_p, _c_p, _c_p]
     lib.cpp_selftest_exp2.restype = _c_int
     lib.cpp_selftest_exp2.argtypes = [_c_p, _c_p, _c_p, _c_i64, _c_p]
+    lib.cpp_selftest_wait_timeout.restype = _c_int
+    lib.cpp_selftest_wait_timeout.argtypes = [_c_i64, _c_p, _c_p, _c_p]
     lib.cpp_status_string.restype = ctypes.c_char_p
     lib.cpp_status_string.argtypes = [_c_int]
     _lib = lib
@@ -284,7 +286,9 @@ def cpp_plan_chunk_sizes(a, b, c, prompt_len, base_chunk_size, page_size, min_ch
                          max_num_scheduled_tokens=0, smooth_factor=1.0):
     lib = load()
     n = ctypes.c_int64(0)
-    cap = max(16, int(prompt_len) // max(1, int(min_chunk)) + 2)
+    # caps (max_model_len - L, max_num_scheduled_tokens) may cut chunks below
+    # min_chunk, down to one token: a prompt has at most prompt_len chunks
+    cap = max(16, int(prompt_len) + 1)
     buf = (ctypes.c_int64 * cap)()
     st = lib.cpp_plan_chunk_sizes(a, b, c, prompt_len, base_chunk_size, page_size, min_chunk, max_model_len,
                                   max_num_scheduled_tokens, smooth_factor, buf, cap, ctypes.byref(n))
@@ -413,3 +417,13 @@ def cpp_selftest_exp2(x, stream=None):
                                     _dev(hw, torch.float32, "hw"), x.numel(), _stream_ptr(stream)),
            "cpp_selftest_exp2")
     return poly, hw
+
+
+def cpp_selftest_wait_timeout(limit_ns, dev_err, stream=None):
+    """Runs the bounded-wait self-test; returns the int32 [3] device tensor
+    (warp 0 wait ok, warp 1 wait ok, microseconds warp 1 waited)."""
+    out = torch.full((3,), -1, dtype=torch.int32, device=dev_err.device)
+    _check(load().cpp_selftest_wait_timeout(int(limit_ns), _dev(dev_err, torch.int32, "dev_err"),
+                                            _dev(out, torch.int32, "out3"), _stream_ptr(stream)),
+           "cpp_selftest_wait_timeout")
+    return out

@@ -123,6 +123,9 @@ const char *cpp_status_string(int status)
     case CPSA_ERR_CUDA: return "CUDA error";
     case CPSA_ERR_NO_DEVICE: return "no usable device";
     case CPSA_ERR_SCRATCH_TOO_SMALL: return "batch needs more than the library's built-in scratch area";
+    case CPSA_ERR_SCRATCH_UNAVAILABLE:
+        return "the library's built-in scratch area could not be reserved (device memory exhausted when its "
+               "device code was loaded?)";
     default: return "unknown status";
     }
 }
@@ -251,8 +254,9 @@ int attn_impl(const void *q, const void *k_new, const void *v_new, const int64_t
         if (ev[i])
             cudaEventRecord(ev[i], st);
     };
-    // programmatic dependent launch between the kernels, except when events are
-    // recorded between them (each kernel then runs in plain stream order)
+    // programmatic dependent launch between the call's own kernels, except when
+    // events are recorded between them (each kernel then runs in plain stream
+    // order); the call's first kernel always launches in plain stream order
     const bool early = events == nullptr;
     int st = check_attn_shape(num_reqs, num_tokens, num_q_heads, num_kv_heads, head_dim, max_kv_splits);
     if (st != CPSA_OK)
@@ -320,7 +324,7 @@ int attn_impl(const void *q, const void *k_new, const void *v_new, const int64_t
     pp.max_citems = L.max_citems;
     pp.dev_err = dev_err;
     mark(0, s);
-    if (launch_plan(pp, s, early) != cudaSuccess)
+    if (launch_plan(pp, s, false) != cudaSuccess)
         return CPSA_ERR_CUDA;
     mark(1, s);
 
@@ -436,6 +440,17 @@ int cpp_selftest_exp2(const float *x, float *out_poly, float *out_hw, int64_t n,
         return CPSA_ERR_NULL_ARG;
     return launch_exp2_selftest(x, out_poly, out_hw, n, (cudaStream_t)stream) == cudaSuccess ? CPSA_OK
                                                                                              : CPSA_ERR_CUDA;
+}
+
+int cpp_selftest_wait_timeout(int64_t limit_ns, uint32_t *dev_err, int32_t *out3, void *stream)
+{
+    if (limit_ns < 1000 || limit_ns > 100000000)
+        return CPSA_ERR_BAD_SHAPE;
+    if (!dev_err || !out3)
+        return CPSA_ERR_NULL_ARG;
+    return launch_wait_selftest((uint64_t)limit_ns, dev_err, out3, (cudaStream_t)stream) == cudaSuccess
+               ? CPSA_OK
+               : CPSA_ERR_CUDA;
 }
 
 int cpp_read_device_error(uint32_t *dev_err, uint32_t *host_flags, int clear, void *stream)

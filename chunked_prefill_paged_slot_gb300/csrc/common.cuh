@@ -80,9 +80,12 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity)
     return ok != 0;
 }
 
-// Wait for the phase with the given parity to complete. Gives up after
-// kWaitLimitNs, or at once when *abort is set by another warp; returns false then.
-__device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, volatile int *abort)
+// Wait for the phase with the given parity to complete. Gives up after limit_ns
+// (kWaitLimitNs unless a self-test passes a shorter one), setting *abort so the
+// other roles of the CTA leave their loops too, or at once when *abort is set by
+// another warp; returns false then.
+__device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, volatile int *abort,
+                                          uint64_t limit_ns = kWaitLimitNs)
 {
     if (mbar_try_wait(bar, parity))
         return true;
@@ -93,7 +96,7 @@ __device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, volati
         if ((it & 63u) == 0) {
             if (*abort)
                 return false;
-            if (global_timer_ns() - t0 > kWaitLimitNs) {
+            if (global_timer_ns() - t0 > limit_ns) {
                 *abort = 1;
                 return false;
             }
@@ -105,7 +108,7 @@ __device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, volati
 // waiting warp leaves the issue slots of its SM sub-partition to the warps that
 // share it. Same limits and result as mbar_wait.
 __device__ __forceinline__ bool mbar_wait_sleep(uint64_t *bar, uint32_t parity, volatile int *abort,
-                                                uint32_t sleep_ns = 256)
+                                                uint32_t sleep_ns = 256, uint64_t limit_ns = kWaitLimitNs)
 {
     uint64_t t0 = 0;
     for (uint32_t it = 0;; ++it) {
@@ -118,7 +121,7 @@ __device__ __forceinline__ bool mbar_wait_sleep(uint64_t *bar, uint32_t parity, 
             const uint64_t now = global_timer_ns();
             if (t0 == 0) {
                 t0 = now;
-            } else if (now - t0 > kWaitLimitNs) {
+            } else if (now - t0 > limit_ns) {
                 *abort = 1;
                 return false;
             }
@@ -276,8 +279,12 @@ __device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;"
 __device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
 
 // With early == false the kernel is launched in plain stream order (its
-// pdl_wait / pdl_trigger are then no-ops): the profiling entry point, which
-// records events between the kernels, launches that way.
+// pdl_wait / pdl_trigger are then no-ops). The first kernel of every public
+// call launches that way, so a call never overlaps whatever the caller put on
+// the stream before it (an event record, a wait, another library's kernel);
+// only a call's own later kernels launch early, after a kernel of the same call.
+// The profiling entry points, which record events between their kernels,
+// launch every kernel that way.
 template <typename... KArgs, typename... Args>
 inline cudaError_t launch_pdl(bool early, void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem,
                               cudaStream_t s, Args &&...args)

@@ -73,6 +73,7 @@ cudaError_t launch_split_microbatch(const int32_t *query_lens, int num_reqs, flo
                                     int32_t length_threshold, int32_t *out3, cudaStream_t s);
 
 cudaError_t launch_exp2_selftest(const float *x, float *poly, float *hw, int64_t n, cudaStream_t s);
+cudaError_t launch_wait_selftest(uint64_t limit_ns, uint32_t *dev_err, int32_t *out, cudaStream_t s);
 
 
 }  // namespace cpsa

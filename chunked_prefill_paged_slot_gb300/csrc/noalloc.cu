@@ -12,6 +12,8 @@
 // cpp_chunked_prefill_attn, fed that array as its workspace.
 #include <mutex>
 
+#include <cudaTypedefs.h>
+
 #include "common.cuh"
 
 namespace {
@@ -22,25 +24,75 @@ constexpr size_t kScratchBytes = CPSA_NOALLOC_SCRATCH_BYTES;
 // cudaGetSymbolAddress, never a device address.
 static __device__ __align__(256) unsigned char g_noalloc_scratch[kScratchBytes];
 
-constexpr int kMaxDevices = 64;
+// A __device__ array has one address per CUDA context, not per device: a host
+// that drives contexts of its own through the driver API sees a different
+// address for each, and a primary context rebuilt after cudaDeviceReset may
+// hold the array elsewhere. So the address is cached per context, under the
+// context's unique ID (cuCtxGetId: never reused within a process, unlike a
+// context handle).
+constexpr int kMaxContexts = 64;
 std::mutex g_scratch_mutex;
-void *g_scratch_addr[kMaxDevices] = {};
+unsigned long long g_ctx_id[kMaxContexts] = {};
+void *g_ctx_addr[kMaxContexts] = {};
+int g_n_ctx = 0;
 
-// Device address of the scratch area on the current device, looked up once per
-// device (with that device current) and cached.
+PFN_cuCtxGetCurrent_v4000 g_get_current = nullptr;
+PFN_cuCtxGetId_v12000 g_get_id = nullptr;
+
+bool driver_fns()
+{
+    if (g_get_current && g_get_id)
+        return true;
+    void *f0 = nullptr, *f1 = nullptr;
+    cudaDriverEntryPointQueryResult q0, q1;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &f0, 4000, cudaEnableDefault, &q0) != cudaSuccess ||
+        q0 != cudaDriverEntryPointSuccess ||
+        cudaGetDriverEntryPointByVersion("cuCtxGetId", &f1, 12000, cudaEnableDefault, &q1) != cudaSuccess ||
+        q1 != cudaDriverEntryPointSuccess)
+        return false;
+    g_get_current = reinterpret_cast<PFN_cuCtxGetCurrent_v4000>(f0);
+    g_get_id = reinterpret_cast<PFN_cuCtxGetId_v12000>(f1);
+    return true;
+}
+
+// Device address of the scratch area in the calling thread's current context,
+// looked up once per context (that lookup loads the library's device code into
+// the context if it is not loaded yet, which is when the array is reserved).
 int scratch_address(void **addr)
 {
     int dev = -1;
-    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices)
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0)
         return CPSA_ERR_NO_DEVICE;
     std::lock_guard<std::mutex> lock(g_scratch_mutex);
-    if (!g_scratch_addr[dev]) {
-        void *p = nullptr;
-        if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || !p)
-            return CPSA_ERR_CUDA;
-        g_scratch_addr[dev] = p;
+    if (!driver_fns())
+        return CPSA_ERR_CUDA;
+    CUcontext ctx = nullptr;
+    unsigned long long id = 0;
+    void *p = nullptr;
+    if (g_get_current(&ctx) != CUDA_SUCCESS)
+        return CPSA_ERR_NO_DEVICE;
+    if (ctx) {
+        if (g_get_id(ctx, &id) != CUDA_SUCCESS)
+            return CPSA_ERR_NO_DEVICE;
+        for (int i = 0; i < g_n_ctx; ++i)
+            if (g_ctx_id[i] == id) {
+                *addr = g_ctx_addr[i];
+                return CPSA_OK;
+            }
     }
-    *addr = g_scratch_addr[dev];
+    // Not cached (or no context current yet: the runtime makes the device's
+    // primary context current here, on this lookup).
+    if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || !p) {
+        (void)cudaGetLastError();   // the failure is reported by the status, not left behind
+        return CPSA_ERR_SCRATCH_UNAVAILABLE;
+    }
+    if (!ctx && (g_get_current(&ctx) != CUDA_SUCCESS || !ctx || g_get_id(ctx, &id) != CUDA_SUCCESS))
+        return CPSA_ERR_NO_DEVICE;
+    // a full table overwrites an entry (that context's next call looks up again)
+    const int slot = g_n_ctx < kMaxContexts ? g_n_ctx++ : (int)(id % kMaxContexts);
+    g_ctx_id[slot] = id;
+    g_ctx_addr[slot] = p;
+    *addr = p;
     return CPSA_OK;
 }
 

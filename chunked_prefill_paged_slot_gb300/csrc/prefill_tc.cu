@@ -331,9 +331,11 @@ chunk_attn_kernel(const ChunkParams p, const __grid_constant__ CUtensorMap tm_q,
     ChunkBars *bars = reinterpret_cast<ChunkBars *>(smem + C::kBarOff);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     if (threadIdx.x == 0) {
+        // a K or V tile is filled by the producer's issuer lanes, one arrival each
+        const uint32_t issuers = (uint32_t)(128 / (p.page_size < 128 ? p.page_size : 128)) * C::kHalves;
         mbar_init(&bars->q_full, 1);
         mbar_init(&bars->q_empty, 1);
-        mbar_init(&bars->tail, 1);
+        mbar_init(&bars->tail, issuers);
         mbar_init(&bars->drain, 1);
         for (int n = 0; n < 2; ++n) {
             mbar_init(&bars->s_full[n], 1);
@@ -341,7 +343,7 @@ chunk_attn_kernel(const ChunkParams p, const __grid_constant__ CUtensorMap tm_q,
             mbar_init(&bars->o_done[n], 1);
         }
         for (int s = 0; s < C::kSlots; ++s) {
-            mbar_init(&bars->slot_full[s], 1);
+            mbar_init(&bars->slot_full[s], issuers);
             mbar_init(&bars->slot_empty[s], 1);
         }
         mbar_init(&bars->stage, 1);
@@ -403,12 +405,22 @@ chunk_attn_kernel(const ChunkParams p, const __grid_constant__ CUtensorMap tm_q,
             }
             ++q_uses;
             const int32_t *bt_row = p.block_table + (int64_t)w.r * p.max_blocks;
-            // lane j < NB holds the page of box j of a tile; the lookup for tile
-            // kt + 1 is issued while tile kt's copies are set up (one tile ahead)
+            // Lane l < NB * kHalves (an issuer lane) copies box j = l % NB (rows
+            // j*PB .. j*PB+PB-1 of a tile), half c = l / NB, so a tile's boxes go out
+            // in one warp instruction rather than one lane's serial loop (16 boxes a
+            // tile at page 16). Every issuer lane arrives once on the tile's barrier
+            // (the barrier counts NB * kHalves arrivals): with the expected bytes of
+            // its own copy right before issuing it, or without bytes when its box is
+            // not loaded. The bytes a copy delivers are thus always announced first
+            // by the lane that issues it, whatever order the lanes run in. Each issuer
+            // lane holds the page of its box; the lookup for tile kt + 1 is issued
+            // while tile kt's copies are set up (one tile ahead).
+            const int box = lane % NB, half = lane / NB;
+            const bool issuer = lane < NB * C::kHalves;
             auto lookup = [&](int kt) -> int {
                 int pg = -1;
-                const int key = kt * 128 + lane * PB;
-                if (lane < NB && kt < w.kt1 && kt < nh && key < hist_end)
+                const int key = kt * 128 + box * PB;
+                if (issuer && kt < w.kt1 && kt < nh && key < hist_end)
                     pg = __ldg(bt_row + key / p.page_size);
                 return pg;
             };
@@ -420,17 +432,13 @@ chunk_attn_kernel(const ChunkParams p, const __grid_constant__ CUtensorMap tm_q,
                 const int key_end = from_new ? s_len : hist_end;   // keys [key0, key_end) are used
                 const int page = next_page;
                 next_page = lookup(kt + 1);
-                const int off = (key0 + lane * PB) % p.page_size;
+                const int off = (key0 + box * PB) % p.page_size;
                 bool valid = false;
-                if (!from_new && lane < NB && key0 + lane * PB < key_end) {
+                if (!from_new && issuer && key0 + box * PB < key_end) {
                     valid = page >= 0 && page < p.num_pages;
-                    if (!valid)
+                    if (!valid && half == 0)
                         set_dev_error(p.dev_err, CPSA_DEV_PAGE_OUT_OF_RANGE);
                 }
-                const uint32_t vmask = __ballot_sync(0xffffffffu, valid);
-                // a box of new rows is always whole (rows past the last token read as zero)
-                const uint32_t bytes =
-                    from_new ? (uint32_t)C::kTileBytes : (uint32_t)__popc(vmask) * box_bytes * C::kHalves;
                 const bool tail = key0 + 128 > key_end;
                 for (int kv = 0; kv < 2 && !stop; ++kv) {
                     const int slot = slot_it % C::kSlots;
@@ -442,24 +450,23 @@ chunk_attn_kernel(const ChunkParams p, const __grid_constant__ CUtensorMap tm_q,
                     uint8_t *dst = smem + C::kSlotOff + slot * C::kTileBytes;
                     const bool fix = kv == 1 && tail;
                     uint64_t *bar = fix ? &bars->tail : &bars->slot_full[slot];
-                    if (lane == 0)
-                        mbar_arrive_expect_tx(bar, bytes);
                     if (from_new) {
-                        // rows of tokens cu + key0 - hist .. + 127, kv head kvh
-                        const CUtensorMap *map = kv == 0 ? &tm_kn : &tm_vn;
-                        if (lane == 0)
-                            for (int c = 0; c < C::kHalves; ++c)
-                                tma_load_3d(dst + c * C::kHalfBytes, map, bar, c * 64, kvh, cu + key0 - hist);
-                    } else {
-                        const CUtensorMap *map = kv == 0 ? &tm_k : &tm_v;
-                        for (int j = 0; j < NB; ++j) {
-                            int pj = __shfl_sync(0xffffffffu, page, j);
-                            int oj = __shfl_sync(0xffffffffu, off, j);
-                            if (lane == 0 && ((vmask >> j) & 1u))
-                                for (int c = 0; c < C::kHalves; ++c)
-                                    tma_load_3d(dst + c * C::kHalfBytes + j * box_bytes, map, bar, c * 64,
-                                                oj, pj * p.num_kv_heads + kvh);
+                        // rows of tokens cu + key0 - hist .. + 127, kv head kvh: lane c loads
+                        // half c (a box of new rows is always whole; rows past the tile's
+                        // last key are zeroed below when the tile is a tail)
+                        if (lane < C::kHalves) {
+                            mbar_arrive_expect_tx(bar, C::kHalfBytes);
+                            tma_load_3d(dst + lane * C::kHalfBytes, kv == 0 ? &tm_kn : &tm_vn, bar, lane * 64, kvh,
+                                        cu + key0 - hist);
+                        } else if (issuer) {
+                            mbar_arrive(bar);
                         }
+                    } else if (valid) {
+                        mbar_arrive_expect_tx(bar, box_bytes);
+                        tma_load_3d(dst + half * C::kHalfBytes + box * box_bytes, kv == 0 ? &tm_k : &tm_v, bar,
+                                    half * 64, off, page * p.num_kv_heads + kvh);
+                    } else if (issuer) {
+                        mbar_arrive(bar);
                     }
                     if (fix) {
                         // value rows >= key_end must be zero: P is zero there, but the
@@ -478,7 +485,7 @@ chunk_attn_kernel(const ChunkParams p, const __grid_constant__ CUtensorMap tm_q,
                             }
                         fence_proxy_async_smem();
                         __syncwarp();
-                        if (lane == 0)
+                        if (issuer)
                             mbar_arrive(&bars->slot_full[slot]);
                     }
                     ++slot_it;

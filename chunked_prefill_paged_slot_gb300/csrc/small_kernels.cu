@@ -293,6 +293,47 @@ __global__ void exp2_selftest_kernel(const float *x, float *poly, float *hw, int
     }
 }
 
+// Self-test of the bounded waits every kernel of the path uses (mbar_wait,
+// mbar_wait_sleep) and of the abort hand-off between a CTA's roles. Warp 0
+// waits, busy-polling, on an mbarrier that nothing arrives at, with the limit
+// the caller passes; when it runs out it sets the CTA's abort flag. Warp 1
+// waits, sleeping between polls, on a second such barrier with the kernels'
+// standard limit (one second): it must leave as soon as it sees the abort flag,
+// long before its own limit. Thread 0 then raises CPSA_DEV_WAIT_TIMEOUT exactly
+// as the attention kernels do. out[0], out[1]: whether each wait succeeded (1)
+// or gave up (0); out[2]: microseconds warp 1 waited. No copy or MMA is in
+// flight at any point, so the CTA ends as soon as both waits return.
+__global__ void wait_selftest_kernel(uint64_t limit_ns, uint32_t *dev_err, int32_t *out)
+{
+    __shared__ __align__(8) uint64_t bar_a, bar_b;
+    __shared__ int abort_flag;
+    if (threadIdx.x == 0) {
+        mbar_init(&bar_a, 1);
+        mbar_init(&bar_b, 1);
+        abort_flag = 0;
+        fence_barrier_init();
+    }
+    __syncthreads();
+    volatile int *abort = &abort_flag;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    if (warp == 0) {
+        const bool ok = mbar_wait(&bar_a, 0, abort, limit_ns);
+        if (lane == 0)
+            out[0] = ok ? 1 : 0;
+    } else if (warp == 1) {
+        const uint64_t t0 = global_timer_ns();
+        const bool ok = mbar_wait_sleep(&bar_b, 0, abort);
+        const uint64_t us = (global_timer_ns() - t0) / 1000u;
+        if (lane == 0) {
+            out[1] = ok ? 1 : 0;
+            out[2] = (int32_t)(us < 0x7fffffffu ? us : 0x7fffffffu);
+        }
+    }
+    __syncthreads();
+    if (threadIdx.x == 0 && *abort)
+        set_dev_error(dev_err, CPSA_DEV_WAIT_TIMEOUT);
+}
+
 // The same split for batches of at most kSplitSmallMax requests, by one warp
 // with no shared memory: the running prefix is carried across 32-request
 // chunks, and the winning boundary carries its own prefix, so n1 needs no second
@@ -375,6 +416,12 @@ cudaError_t launch_exp2_selftest(const float *x, float *poly, float *hw, int64_t
     return cudaGetLastError();
 }
 
+cudaError_t launch_wait_selftest(uint64_t limit_ns, uint32_t *dev_err, int32_t *out, cudaStream_t s)
+{
+    wait_selftest_kernel<<<1, 64, 0, s>>>(limit_ns, dev_err, out);
+    return cudaGetLastError();
+}
+
 cudaError_t launch_kv_cache_write(const void *k, const void *v, const int64_t *slot_mapping, int64_t num_tokens,
                                   int num_kv_heads, int head_dim, int page_size, int64_t num_pages, void *k_cache,
                                   void *v_cache, uint32_t *dev_err, int num_sms, cudaStream_t s)
@@ -386,10 +433,10 @@ cudaError_t launch_kv_cache_write(const void *k, const void *v, const int64_t *s
     const int64_t cap = (int64_t)num_sms * 8;
     if (blocks > cap) blocks = cap;
     if (head_dim == 128)
-        return launch_pdl(true, kv_write_kernel<16>, dim3((unsigned)blocks), dim3(256), 0, s, (const uint4 *)k,
+        return launch_pdl(false, kv_write_kernel<16>, dim3((unsigned)blocks), dim3(256), 0, s, (const uint4 *)k,
                           (const uint4 *)v, slot_mapping, num_tokens, num_kv_heads, page_size, num_pages,
                           (uint4 *)k_cache, (uint4 *)v_cache, dev_err);
-    return launch_pdl(true, kv_write_kernel<8>, dim3((unsigned)blocks), dim3(256), 0, s, (const uint4 *)k,
+    return launch_pdl(false, kv_write_kernel<8>, dim3((unsigned)blocks), dim3(256), 0, s, (const uint4 *)k,
                       (const uint4 *)v, slot_mapping, num_tokens, num_kv_heads, page_size, num_pages,
                       (uint4 *)k_cache, (uint4 *)v_cache, dev_err);
 }
@@ -405,9 +452,9 @@ cudaError_t launch_split_microbatch(const int32_t *query_lens, int num_reqs, flo
                                     int32_t length_threshold, int32_t *out3, cudaStream_t s)
 {
     if (num_reqs <= kSplitSmallMax)
-        return launch_pdl(true, split_small_kernel, dim3(1), dim3(32), 0, s, query_lens, num_reqs, balance_threshold,
+        return launch_pdl(false, split_small_kernel, dim3(1), dim3(32), 0, s, query_lens, num_reqs, balance_threshold,
                           length_threshold, out3);
-    return launch_pdl(true, split_kernel, dim3(1), dim3(kSplitThreads), 0, s, query_lens, num_reqs, balance_threshold,
+    return launch_pdl(false, split_kernel, dim3(1), dim3(kSplitThreads), 0, s, query_lens, num_reqs, balance_threshold,
                       length_threshold, out3);
 }
 

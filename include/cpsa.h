@@ -62,6 +62,7 @@ extern "C" {
 #define CPSA_ERR_CUDA (-6)                /* a CUDA runtime call or launch failed */
 #define CPSA_ERR_NO_DEVICE (-7)           /* no usable sm_103 device is current */
 #define CPSA_ERR_SCRATCH_TOO_SMALL (-8)   /* batch needs more than the built-in scratch area */
+#define CPSA_ERR_SCRATCH_UNAVAILABLE (-9) /* the built-in scratch area could not be reserved in this context */
 
 /* ---- device error flags (bits of *dev_err) --------------------------------- */
 #define CPSA_DEV_SLOT_OUT_OF_RANGE 0x01u  /* slot >= num_pages * page_size: token skipped */
@@ -219,20 +220,29 @@ int cpp_chunked_prefill_attn_write_kv_events(const void *q, const void *k, const
  * memory and forbids allocation on its serving path, or C callers with no
  * allocator of their own. Instead of a caller workspace it uses a scratch area
  * the library owns: a fixed array of CPSA_NOALLOC_SCRATCH_BYTES in device
- * global memory, reserved on every GPU that loads the library and kept until
- * the process exits. The call itself allocates nothing.
+ * global memory, kept until the process exits. The call itself allocates
+ * nothing: the array is reserved when the library's device code is loaded into
+ * a CUDA context, which with CUDA's default lazy module loading is the first
+ * call of this function in that context (or any earlier call of the library
+ * that loads the same code). A host that claims all device memory up front
+ * should therefore make one warm-up call at initialisation; when the array
+ * cannot be reserved the call returns CPSA_ERR_SCRATCH_UNAVAILABLE.
  *
  * Same arguments, results and device flags as cpp_chunked_prefill_attn, minus
  * the workspace. Returns CPSA_ERR_SCRATCH_TOO_SMALL when the batch's work lists
  * (cpp_attn_workspace_min_bytes) exceed the scratch area; when only the split
  * partials do not fit, every row runs with one KV split and
  * CPSA_DEV_SPLITS_CLAMPED is set, as with a small workspace.
- * The first call on a device looks up the scratch area's device address (with
- * that device current) and caches it: make that first call before any stream
- * capture. All calls in the process share the one area and find it holding the
- * previous call's data (the call rewrites everything it reads), so calls whose
- * execution overlaps on the GPU -- on different streams, or from different host
- * threads -- race and must be ordered by the caller.
+ * The array's device address belongs to a CUDA context: the first call in each
+ * context (the calling thread's current one; the device's primary context for
+ * runtime-API callers) looks it up and caches it under the context's unique ID,
+ * so contexts created through the driver API, and a primary context rebuilt
+ * after cudaDeviceReset, each get their own lookup. Make that first call in a
+ * context before any stream capture. All calls in a context share the one
+ * area and find it holding the previous call's data (the call rewrites
+ * everything it reads, the merge counters included), so calls whose execution
+ * overlaps on the GPU -- on different streams, or from different host threads
+ * -- race and must be ordered by the caller.
  */
 #define CPSA_NOALLOC_SCRATCH_BYTES ((size_t)64 << 20)
 int cpp_chunked_prefill_attn_noalloc(const void *q, const void *k_cache, const void *v_cache,
@@ -379,6 +389,20 @@ int cpp_sched_stats(const cpsa_sched *handle, int64_t *waiting, int64_t *running
  * error 7.5e-5), out_hw[i] = the hardware ex2.approx. Stream-ordered.
  */
 int cpp_selftest_exp2(const float *x, float *out_poly, float *out_hw, int64_t n, void *stream);
+
+/*
+ * Self-test of failure detection (no counterpart in the pages; the kernels'
+ * bounded waits). One CTA: warp 0 waits on an mbarrier that nothing arrives at,
+ * with a limit of limit_ns (1 us .. 100 ms, else CPSA_ERR_BAD_SHAPE); when it
+ * runs out it sets the CTA's abort flag, the way a stalled copy or MMA would in
+ * the attention kernels. Warp 1 waits on a second such barrier with the
+ * kernels' standard one-second limit and must leave as soon as it sees the
+ * abort flag. CPSA_DEV_WAIT_TIMEOUT is then set in *dev_err. out3 (device
+ * int32[3]): warp 0's wait succeeded (1) or gave up (0); the same for warp 1;
+ * microseconds warp 1 waited. Stream-ordered; the kernel always ends (within
+ * limit_ns plus the abort poll), and leaves the context usable.
+ */
+int cpp_selftest_wait_timeout(int64_t limit_ns, uint32_t *dev_err, int32_t *out3, void *stream);
 
 /* Human-readable name of a status code. */
 const char *cpp_status_string(int status);

@@ -144,30 +144,82 @@ def test_microbatch_sampled(cuda_lib, fused):
     compare(got, ref, what="microbatch" + (" (fused)" if fused else ""))
 
 
-def test_two_streams_match_one(cuda_lib):
-    """The micro-batch split run on two streams matches the one-stream run.
+def _saved_pages(spec, d, reqs):
+    """The sampled requests' cache pages as they are before this step's KV write
+    (the seeded input state the oracle starts from)."""
+    import torch
+    P = spec.page_size
+    bt = d["block_table_host"]
+    saved = {}
+    for r in reqs:
+        npg = (spec.seq[r] + P - 1) // P
+        idx = torch.from_numpy(bt[r, :npg].astype(np.int64)).cuda()
+        saved[r] = (_u16(d["k_cache"][idx]), _u16(d["v_cache"][idx]))
+    return saved
 
-    The prefill work is cut into equal runs per CTA over the whole batch, so the
-    two micro-batches cut their units elsewhere than the full batch does: the
-    results agree within the attention tolerance, decode rows bit for bit."""
+
+def _oracle_picks(spec, d, out, saved, picks):
+    """(got, ref) of the rows picks[r] (0-based within request r) of `out`."""
+    import torch
+    cu = np.concatenate([[0], np.cumsum(spec.qlen)])
+    gots, refs = [], []
+    for r, rows in picks.items():
+        ql, h = spec.qlen[r], spec.hist[r]
+        t0, t1 = int(cu[r]), int(cu[r + 1])
+        hk, hv = saved[r]
+        ref = oracle_rows(_u16(d["q"][t0:t1]), _u16(d["k"][t0:t1]), _u16(d["v"][t0:t1]), hk, hv, h, ql,
+                          spec.page_size, rows)
+        got = out[t0 + torch.from_numpy(np.asarray(rows)).cuda()].float().cpu().numpy().astype(np.float64)
+        gots.append(got)
+        refs.append(ref)
+    return np.concatenate(gots), np.concatenate(refs)
+
+
+@pytest.mark.parametrize("fused", [False, True])
+def test_two_streams_match_oracle(cuda_lib, fused):
+    """The micro-batch workload (128 decode rows, then 64 prompts of 2600) split at
+    the balanced point (160, 83328) and run as two micro-batches on two streams
+    ("Ascend dual-stream parallel" article, section 3.1: requests before the
+    split and tokens before token_split form micro-batch 0), with the KV write as
+    its own call or fused: sampled rows against the fp64 oracle -- the decode
+    rows of 8 decode requests and 16 rows (0 and 2599 among them) of 6 prompts,
+    three in each micro-batch -- and against the one-stream run.
+
+    The prefill work is cut into equal runs per CTA over each call's batch, so
+    the two micro-batches cut their units elsewhere than the full batch does:
+    two-stream and one-stream outputs agree within the attention tolerance, and
+    decode rows (split by their own length only) bit for bit."""
     import torch
     spec = W.spec_microbatch()
     d = W.device_batch(spec)
     B, T = len(spec.qlen), sum(spec.qlen)
-    step = cuda_lib.AttentionStep(B, T, 32, 8, 128, max_kv_splits=8, two_stream=True)
-    # the first KV write happens in both runs; history pages are read-only afterwards
+    dec_reqs = [0, 9, 31, 58, 64, 100, 126, 127]
+    pre_reqs = [128, 141, 159, 160, 177, 191]        # 128..159: micro-batch 0; 160..191: micro-batch 1
+    saved = _saved_pages(spec, d, dec_reqs + pre_reqs)
+    step = cuda_lib.AttentionStep(B, T, 32, 8, 128, max_kv_splits=8, two_stream=True, fused_kv_write=fused)
+    # the first KV write happens in both runs (the same bytes); history pages are read-only
     out1 = torch.empty_like(d["q"])
     step.run(d["q"], d["k"], d["v"], d["slot_mapping"], d["k_cache"], d["v_cache"], d["query_lens"],
              d["seq_lens"], d["block_table"], out1)
-    out2 = torch.empty_like(d["q"])
+    out2 = torch.full_like(d["q"], float("nan"))
     used = step.run_two_stream(d["q"], d["k"], d["v"], d["slot_mapping"], d["k_cache"], d["v_cache"],
                                d["query_lens"], d["seq_lens"], d["block_table"], out2)
     torch.cuda.synchronize()
     assert used and step.last_split == (160, 83328, True)
     assert step.read_errors() == 0
+    rng = np.random.default_rng(36 + int(fused))
+    picks = {r: [0] for r in dec_reqs}
+    for r in pre_reqs:
+        ql = spec.qlen[r]
+        picks[r] = np.unique(np.concatenate([[0, ql - 1], rng.choice(np.arange(1, ql - 1), 14, replace=False)]))
+        assert len(picks[r]) == 16
+    got, ref = _oracle_picks(spec, d, out2, saved, picks)
+    compare(got, ref, what="two streams vs oracle" + (" (fused)" if fused else ""))
+    got1, _ = _oracle_picks(spec, d, out1, saved, picks)
+    compare(got1, ref, what="one stream vs oracle" + (" (fused)" if fused else ""))
     compare(out2.float().cpu().numpy().astype(np.float64), out1.float().cpu().numpy().astype(np.float64),
             atol=1e-2, rtol_f=2e-3, what="two streams vs one")
-    n_dec = 128      # decode rows split by their own length only: identical bits
+    n_dec = 128
     assert torch.equal(out1[:n_dec].view(torch.int16), out2[:n_dec].view(torch.int16))
 
 

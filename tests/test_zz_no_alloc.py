@@ -4,15 +4,19 @@ cpp_chunked_prefill_attn_noalloc serves callers that cannot allocate device
 memory (a plugin inside a host that owns all device memory, or a C caller with
 no allocator of its own): it runs on a scratch area the library keeps in device
 global memory. This test calls it twice in a row through the C ABI, on two
-different batches, and checks each result against cpp_chunked_prefill_attn with
-a caller workspace, within the attention tolerance of the other tests. The file
-sorts last so that a run stopping at the first failure has run everything else.
+different batches (the second finding the first one's data in the scratch
+area), and checks each result bit for bit against cpp_chunked_prefill_attn with
+a caller workspace (the split partials fit in both, so both make the same
+choices), and both against the fp64 oracle within the attention tolerance of
+the other tests. The file sorts last so that a run stopping at the first
+failure has run everything else.
 """
 import numpy as np
 import pytest
 
+import oracle
 import workloads as W
-from helpers import bf16_tensor_to_f64, compare, to_dev, to_dev_bf16
+from helpers import bf16_tensor_to_f64, compare, oracle_caches, to_dev, to_dev_bf16
 
 pytestmark = pytest.mark.gpu
 
@@ -26,7 +30,13 @@ def _inputs(cpsa, spec):
     cpsa.cpp_kv_cache_write(to_dev_bf16(b.hist_k), to_dev_bf16(b.hist_v), to_dev(b.hist_slot_mapping), kc, vc, err)
     cpsa.cpp_kv_cache_write(to_dev_bf16(b.k), to_dev_bf16(b.v), to_dev(b.slot_mapping), kc, vc, err)
     return dict(q=to_dev_bf16(b.q), kc=kc, vc=vc, ql=to_dev(b.query_lens), sl=to_dev(b.seq_lens),
-                bt=to_dev(b.block_table), err=err, B=len(spec.qlen), T=b.num_tokens, spec=spec)
+                bt=to_dev(b.block_table), err=err, B=len(spec.qlen), T=b.num_tokens, spec=spec, batch=b)
+
+
+def _oracle(x):
+    b = x["batch"]
+    kc, vc = oracle_caches(b)
+    return oracle.paged_attention(b.q, kc, vc, b.query_lens, b.seq_lens, b.block_table)
 
 
 def _with_workspace(cpsa, x):
@@ -59,10 +69,12 @@ def test_noalloc_matches_workspace_entry_point_on_two_calls(cuda_lib):
     got1 = _without_workspace(cuda_lib, first)      # first call on this device sets the scratch up
     got2 = _without_workspace(cuda_lib, second)     # second call reuses the scratch the first one left
     torch.cuda.synchronize()
-    assert cuda_lib.cpp_read_device_error(first["err"]) & ~cuda_lib.DEV_SPLITS_CLAMPED == 0
-    assert cuda_lib.cpp_read_device_error(second["err"]) & ~cuda_lib.DEV_SPLITS_CLAMPED == 0
-    compare(bf16_tensor_to_f64(got1), bf16_tensor_to_f64(ref1), what="no-alloc call 1")
-    compare(bf16_tensor_to_f64(got2), bf16_tensor_to_f64(ref2), what="no-alloc call 2")
+    assert cuda_lib.cpp_read_device_error(first["err"]) == 0
+    assert cuda_lib.cpp_read_device_error(second["err"]) == 0
+    assert torch.equal(got1.view(torch.int16), ref1.view(torch.int16)), "no-alloc call 1 differs from the workspace call"
+    assert torch.equal(got2.view(torch.int16), ref2.view(torch.int16)), "no-alloc call 2 differs from the workspace call"
+    for got, x, what in ((got1, first, "call 1"), (got2, second, "call 2")):
+        compare(bf16_tensor_to_f64(got), _oracle(x), what=f"no-alloc {what} vs oracle")
 
 
 def test_noalloc_rejects_a_batch_beyond_the_scratch_area(cuda_lib):
