@@ -4,7 +4,9 @@
 Step = one pass of the whole path over the headline workload: a Llama-3-8B-shaped
 attention layer (32 q / 8 kv heads, head_dim 128, bf16, page 128) prefilling one
 32768-token sequence in 64 chunks of 512; per chunk the micro-batch split, the
-slot_mapping KV write and the causal attention over the paged cache. The KV
+slot_mapping KV write and the causal attention over the paged cache. The splits
+run on a side stream joined back before the step ends (a one-request batch is
+never split, so no attention call waits for one). The KV
 write runs fused into the attention call (cpp_chunked_prefill_attn_write_kv);
 `--two-call` times the separate write and attention calls instead, and the
 line's `two_call_step` reports that variant on the same inputs.
@@ -196,13 +198,30 @@ class ChunkedPrefill:
         self.ws = torch.empty(cpsa.cpp_attn_workspace_bytes(1, CHUNK, HQ, HKV, D, max_kv_splits),
                               dtype=torch.uint8, device=dev)
         self.err = torch.zeros(1, dtype=torch.int32, device=dev)
-        self.split_out = torch.zeros(3, dtype=torch.int32, device=dev)
+        self.split_outs = torch.zeros((N_CHUNKS, 3), dtype=torch.int32, device=dev)
+        self.split_stream = torch.cuda.Stream(device=dev)
         self.marks = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(N_CHUNKS)]
         self.host = None
 
+    def fork_splits(self, stream):
+        """Start the side stream that computes the balanced micro-batch split of
+        every chunk's batch (each result kept in split_outs). A one-request batch
+        is never split, so no attention call waits for its split: the split runs
+        beside the attention (its one warp fits next to a chunk-kernel CTA)
+        rather than between the calls. chunk() enqueues chunk i's split just
+        before its attention; join_splits() joins the side stream back."""
+        fork = self.torch.cuda.Event()
+        fork.record(stream)
+        self.split_stream.wait_event(fork)
+
+    def join_splits(self, stream):
+        join = self.torch.cuda.Event()
+        join.record(self.split_stream)
+        stream.wait_event(join)
+
     def chunk(self, i, q, k, v, slots, out, stream, marks=None):
         cpsa = self.cpsa
-        cpsa.cpp_split_microbatch(self.qlens[i], self.split_out, 0.1, 256, stream=stream)
+        cpsa.cpp_split_microbatch(self.qlens[i], self.split_outs[i], 0.1, 256, stream=self.split_stream)
         if self.fused:
             cpsa.cpp_chunked_prefill_attn_write_kv(q, k, v, slots, self.k_cache, self.v_cache, self.qlens[i],
                                                    self.slens[i], self.bt, out, self.ws, self.err,
@@ -220,10 +239,12 @@ class ChunkedPrefill:
                                                  max_kv_splits=self.max_kv_splits, stream=stream)
 
     def step(self, stream, with_marks=False):
+        self.fork_splits(stream)
         for i in range(N_CHUNKS):
             a, b = i * CHUNK, (i + 1) * CHUNK
             self.chunk(i, self.q[a:b], self.k[a:b], self.v[a:b], self.slots[a:b], self.out[a:b], stream,
                        self.marks[i] if with_marks else None)
+        self.join_splits(stream)
 
     def chunk_kernel_ms(self):
         return [self.marks[i][0].elapsed_time(self.marks[i][1]) for i in range(N_CHUNKS)]
@@ -256,6 +277,7 @@ class ChunkedPrefill:
         s_in, s_out = self.e2e_streams
         nb = N_CHUNKS // E2E_BATCH
         ev = lambda: torch.cuda.Event()
+        self.fork_splits(stream)
         start = ev()
         start.record(stream)
         h2d_done, comp_done, d2h_done = [None] * nb, [None] * nb, [None] * nb
@@ -291,6 +313,7 @@ class ChunkedPrefill:
             d2h_done[b].record(s_out)
         stream.wait_event(d2h_done[nb - 1])
         stream.wait_event(d2h_done[nb - 2])
+        self.join_splits(stream)
 
 
 # ----------------------------------------------------------------------------- oracle (CPU) leg
@@ -704,7 +727,15 @@ def main():
                     help="only the mixed decode step with 128 decode rows (about 2.5 GB of cache), timed with "
                          "CUDA events; an ncu --set full capture of this case once ended in a GPU fault (see the "
                          "design notes on measurement) and is not to be repeated")
+    ap.add_argument("--profile-kv-write", action="store_true",
+                    help="only the KV-write bandwidth measurement (T = 512 at page 128, T = 166528 at page 16)")
     args = ap.parse_args()
+    if args.profile_kv_write:
+        import torch
+        dev = torch.device("cuda", 0)
+        torch.cuda.set_device(dev)
+        print(json.dumps(kv_write_bandwidth(dev, reps=3)), flush=True)
+        return 0
     if args.profile_decode:
         import torch
         dev = torch.device("cuda", 0)
@@ -804,7 +835,7 @@ def main():
     achieved = per_launch_flops / (per_launch_ms * 1e-3) / 1e12
     roofline = {"bound": "tensor", "achieved": round(achieved, 2), "peak": peak_tf, "unit": "TFLOP/s",
                 "frac": round(achieved / peak_tf, 4), "traffic": load_traffic(),
-                "kernel": "chunk_attn_kernel<128,2>", "peak_source": f"{peak_src} bf16 dense (burst)",
+                "kernel": "chunk_attn_kernel<128,2,true> (one request per call: runs planned by the kernel itself)", "peak_source": f"{peak_src} bf16 dense (burst)",
                 "per_launch_flops": per_launch_flops, "per_launch_ms": round(per_launch_ms, 4),
                 "last_chunk_ms": round(float(km[:, -1].mean()), 4),
                 "last_chunk_tflops": round(chunk_flops((N_CHUNKS - 1) * CHUNK, CHUNK) / (km[:, -1].mean() * 1e-3) / 1e12, 2)}

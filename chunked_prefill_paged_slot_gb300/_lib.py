@@ -32,6 +32,7 @@ DEV_TOKENS_MISMATCH = 0x08
 DEV_SEQ_GT_TABLE = 0x10
 DEV_SPLITS_CLAMPED = 0x20
 DEV_WAIT_TIMEOUT = 0x40
+DEV_PLAN_OVERFLOW = 0x80
 
 
 class CpsaError(RuntimeError):

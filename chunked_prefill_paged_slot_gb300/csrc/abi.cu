@@ -2,6 +2,7 @@
 // include/cpsa.h): argument checks, TMA tensor maps, workspace carving and the
 // stream-ordered launch sequence. No device memory is allocated here.
 #include <math.h>
+#include <atomic>
 #include <mutex>
 
 #include <cudaTypedefs.h>
@@ -87,6 +88,34 @@ bool make_map4_halves(CUtensorMap *m, const void *base, int page_size, uint64_t 
 }
 
 int nq_for_group(int group) { return (group % 2 == 0) ? 2 : 1; }
+
+// Every attention call gets its own nonzero epoch: the merge counters it leaves
+// in the workspace carry it, so the next call tells them apart from its own.
+std::atomic<uint32_t> g_epoch{0};
+
+uint32_t next_epoch()
+{
+    uint32_t e;
+    do {
+        e = g_epoch.fetch_add(1u, std::memory_order_relaxed) + 1u;
+    } while (e == 0u);
+    return e;
+}
+
+// Whether a batch of one prefill request of num_tokens tokens can skip the plan
+// kernel: every chunk-kernel run must fit its pieces in kSelfPlanCap. A run of R
+// tiles holds at most (R - 2) / L + 2 pieces, L the shortest unit; that ratio is
+// largest with no history (L = 1, R = R0, every unit as short as it gets) and
+// stays below R0 + 3 for any history (the units grow as fast as the run).
+bool self_plan_fits(int64_t num_tokens, int units_per_qtile, int grid)
+{
+    const int64_t nqt = (num_tokens + kTileM - 1) / kTileM;
+    const int64_t w0 = (int64_t)units_per_qtile * nqt * (nqt + 1) / 2;
+    int64_t r0 = (w0 + grid - 1) / grid;
+    if (r0 < kMinRunTiles)
+        r0 = kMinRunTiles;
+    return r0 + 3 <= kSelfPlanCap;
+}
 
 int attn_impl(const void *q, const void *k_new, const void *v_new, const int64_t *slot_mapping, void *k_cache,
               void *v_cache, const int32_t *query_lens, const int32_t *seq_lens, const int32_t *block_table,
@@ -289,7 +318,7 @@ int attn_impl(const void *q, const void *k_new, const void *v_new, const int64_t
     int32_t *counts = reinterpret_cast<int32_t *>(ws + L.off_counts);
     int32_t *cu_q = reinterpret_cast<int32_t *>(ws + L.off_cuq);
     int32_t *run_first = reinterpret_cast<int32_t *>(ws + L.off_runs);
-    int32_t *flags = reinterpret_cast<int32_t *>(ws + L.off_flags);
+    unsigned long long *flags = reinterpret_cast<unsigned long long *>(ws + L.off_flags);
     PrefillItem *pitems = reinterpret_cast<PrefillItem *>(ws + L.off_pitems);
     DecodeItem *ditems = reinterpret_cast<DecodeItem *>(ws + L.off_ditems);
     CombineItem *citems = reinterpret_cast<CombineItem *>(ws + L.off_citems);
@@ -323,8 +352,15 @@ int attn_impl(const void *q, const void *k_new, const void *v_new, const int64_t
     pp.max_ditems = L.max_ditems;
     pp.max_citems = L.max_citems;
     pp.dev_err = dev_err;
+    // A single request is either one decode row or one prefill: the other
+    // kernel would find no items, so it is not launched. A single prefill that
+    // fits self-planning needs no plan kernel either: the chunk kernel's CTAs
+    // compute their runs themselves, and it is the call's first kernel.
+    const bool single_prefill = num_reqs == 1 && num_tokens >= 2;
+    const bool single_decode = num_reqs == 1 && num_tokens == 1;
+    const bool self_plan = single_prefill && self_plan_fits(num_tokens, num_kv_heads * (group / nq), pp.chunk_grid);
     mark(0, s);
-    if (launch_plan(pp, s, false) != cudaSuccess)
+    if (!self_plan && launch_plan(pp, s, false) != cudaSuccess)
         return CPSA_ERR_CUDA;
     mark(1, s);
 
@@ -384,12 +420,16 @@ int attn_impl(const void *q, const void *k_new, const void *v_new, const int64_t
     cp.pitems = pitems;
     cp.run_first = run_first;
     cp.flags = flags;
-    // A single request is either one decode row or one prefill: the other
-    // kernel would find no items, so it is not launched.
-    const bool single_prefill = num_reqs == 1 && num_tokens >= 2;
-    const bool single_decode = num_reqs == 1 && num_tokens == 1;
+    cp.epoch = next_epoch();
+    cp.self_plan = self_plan ? 1 : 0;
+    cp.num_tokens = (int)num_tokens;
+    // cuts need two pieces' partial rows per run (see the chunk kernel's self plan)
+    const bool partials_fit = cap >= (int64_t)2 * pp.chunk_grid * kTileM * nq;
+    cp.split_ok = max_kv_splits > 1 && partials_fit ? 1 : 0;
+    cp.split_clamped = max_kv_splits > 1 && !partials_fit ? 1 : 0;
     const int grid_c = single_decode ? 0 : pp.chunk_grid;   // one stream-K run per CTA
-    if (grid_c > 0 && launch_chunk_attn(cp, tq, tk, tv, tkn, tvn, head_dim, nq, grid_c, s, early) != cudaSuccess)
+    if (grid_c > 0 &&
+        launch_chunk_attn(cp, tq, tk, tv, tkn, tvn, head_dim, nq, grid_c, s, early && !self_plan) != cudaSuccess)
         return CPSA_ERR_CUDA;
     mark(2, s);
 

@@ -37,7 +37,18 @@ struct AttnCommon {
 struct ChunkParams : AttnCommon {
     const PrefillItem *pitems;
     const int32_t *run_first;   // CTA c processes pieces [run_first[c], run_first[c + 1])
-    int32_t *flags;             // per split unit, q head and softmax warp: pieces done (zeroed by the plan)
+    // Merge counters, per split unit, q head and softmax warp: the pieces of the
+    // unit done in this call, tagged with the call's epoch in the high 32 bits
+    // (a count left by an earlier call carries another epoch and reads as zero,
+    // so nothing has to clear the counters between calls).
+    unsigned long long *flags;
+    uint32_t epoch;             // nonzero, different for every call of the library
+    // A batch of one prefill request (self_plan != 0): no plan kernel ran; every
+    // CTA computes its own run's pieces from query_lens[0] / seq_lens[0].
+    int self_plan;
+    int num_tokens;             // for the self-planned batch's token check
+    int split_ok;               // self-planned batch: units may be cut (splits allowed and the partials fit)
+    int split_clamped;          // self-planned batch: splits were asked for but the partials do not fit
 };
 
 struct DecodeParams : AttnCommon {

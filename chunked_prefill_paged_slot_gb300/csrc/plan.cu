@@ -7,6 +7,8 @@
 //             sum(query_lens) == num_tokens,
 //   pieces    the stream-K cut of all prefill units' KV tiles into one run per
 //             chunk-kernel CTA (see plan.cuh), decode items, combine items,
+//             (the merge counters of split units need no zeroing: they carry
+//             the call's epoch, see the chunk kernel),
 // and stores the counts that the persistent kernels read.
 // Pass 1 sums tokens, prefill tiles (W) and decode partial rows and finds the
 // shortest and longest unit, which fix the run length, whether the partials fit
@@ -437,8 +439,6 @@ __global__ void __launch_bounds__(kPlanThreads, 1) plan_kernel(PlanParams p)
     __syncthreads();   // this block's piece writes are visible to the whole block
     const int n_pieces = (int)min((int64_t)carry_b[0], p.max_pitems);
     fill_run_first(p, n_pieces, grid, split_prefill, tiles, run, threadIdx.x, kPlanThreads);
-    const int n_flags = min(carry_b[5], kMaxSplitUnits) * p.nq * 4;
-    for (int i = threadIdx.x; i < n_flags; i += kPlanThreads) p.flags[i] = 0;
     if (threadIdx.x == 0) {
         p.cu_q[p.num_reqs] = carry_a[0];
         p.counts[kCntPrefill] = (int)min((int64_t)carry_b[0], p.max_pitems);
@@ -523,8 +523,6 @@ __global__ void __launch_bounds__(32, 1) plan_small_kernel(PlanParams p)
     __syncwarp();   // the warp's piece writes are visible to all its lanes
     const int n_pieces = (int)min((int64_t)off.pieces, p.max_pitems);
     fill_run_first(p, n_pieces, grid, sc.split_prefill, tile_sum, sc.run, lane, 32);
-    const int n_flags = min(off.sunits, kMaxSplitUnits) * p.nq * 4;
-    for (int i = lane; i < n_flags; i += 32) p.flags[i] = 0;
     if (lane == 0) {
         p.cu_q[p.num_reqs] = tok_total;
         p.counts[kCntPrefill] = n_pieces;

@@ -3,13 +3,15 @@
 //
 // One call of cpp_chunked_prefill_attn runs:
 //   plan      one CTA (one warp for up to 32 requests): scan of query_lens,
-//             validation, work lists, split choice, merge counters zeroed
+//             validation, work lists, split choice
 //   chunk     tensor-core kernel over prefill items (query_len >= 2); merges
 //             the units the stream-K cut split
 //   decode    split-KV kernel over decode items (query_len == 1)
 //   combine   merges the partial results of decode rows split along keys
 // The lists live in the caller's workspace; every kernel is persistent and reads
-// its item count from the workspace, so the host never needs the lengths.
+// its item count from the workspace, so the host never needs the lengths. A
+// batch of one prefill request of at most about 4k tokens runs the chunk kernel
+// alone: its CTAs compute their own runs (same units and cuts as the plan).
 #pragma once
 
 #include <cuda_runtime.h>
@@ -40,6 +42,9 @@ constexpr int kDecodeChunk = 64;            // keys per decode pipeline stage
 constexpr int kDecodeKeysPerSplit = 4096;   // keys per decode split (multiple of kDecodeChunk)
 constexpr int kMaxSplitUnits = kMaxChunkGrid;   // a split unit holds a run boundary: at most grid - 1
 constexpr int kMergeCounters = 2 * 4;          // per split unit: q heads (<= 2) x 4 softmax warps
+// A batch of one prefill request skips the plan kernel: every chunk-kernel CTA
+// computes its own run's pieces (at most this many, kept in shared memory).
+constexpr int kSelfPlanCap = 56;
 
 // A prefill piece: KV tiles [kt0, kt1) of the unit (request r, query tile at
 // row i0, kv head kvh, head pair hp); piece `piece` of `npieces` of that unit.
@@ -105,7 +110,7 @@ inline WsLayout ws_layout(int num_reqs, int64_t num_tokens, int Hq, int Hkv, int
     L.off_counts = o; o = ws_align(o + sizeof(int32_t) * kCntSlots);
     L.off_cuq = o;    o = ws_align(o + sizeof(int32_t) * (size_t)(B + 1));
     L.off_runs = o;   o = ws_align(o + sizeof(int32_t) * (size_t)(kMaxChunkGrid + 1));
-    L.off_flags = o;  o = ws_align(o + sizeof(int32_t) * (size_t)kMaxSplitUnits * kMergeCounters);
+    L.off_flags = o;  o = ws_align(o + sizeof(unsigned long long) * (size_t)kMaxSplitUnits * kMergeCounters);
     L.off_pitems = o; o = ws_align(o + sizeof(PrefillItem) * (size_t)L.max_pitems);
     L.off_ditems = o; o = ws_align(o + sizeof(DecodeItem) * (size_t)L.max_ditems);
     L.off_citems = o; o = ws_align(o + sizeof(CombineItem) * (size_t)L.max_citems);
@@ -141,7 +146,7 @@ struct PlanParams {
     int32_t *counts;
     int32_t *cu_q;
     int32_t *run_first;        // [chunk_grid + 1]: first piece of each CTA's run
-    int32_t *flags;            // [kMaxSplitUnits][nq][4]: merge counters, zeroed by the plan
+    unsigned long long *flags; // [kMaxSplitUnits][nq][4]: merge counters (epoch-tagged, see ChunkParams)
     PrefillItem *pitems;
     DecodeItem *ditems;
     CombineItem *citems;

@@ -70,7 +70,9 @@ struct ChunkCfg {
     static constexpr int kSlotOff = NQ * kTileBytes;
     static constexpr int kStageOff = kSlotOff + kSlots * kTileBytes;   // the cache writer's buffer
     static constexpr int kBarOff = kStageOff + kTileBytes;
-    static constexpr int kSmemBytes = kBarOff + 1024 + 1024;   // barriers + alignment slack
+    static constexpr int kItemOff = kBarOff + 256;             // self-planned pieces (after ChunkBars)
+    static constexpr int kBarBytes = 256 + kSelfPlanCap * 32;  // barriers + pieces
+    static constexpr int kSmemBytes = kBarOff + kBarBytes + 1024;   // + alignment slack
     static_assert(kSmemBytes <= 232448, "beyond the 227 KB of shared memory a CTA may have");
     static_assert(D != 128 || NQ * 4 * kMergeStageBytes <= kSlotOff + kSlots * kTileBytes,
                   "the staged merge uses the Q and K/V buffers");
@@ -92,6 +94,148 @@ struct ChunkBars {
     int abort;
     int it_begin, it_end;    // this CTA's run of pieces
 };
+static_assert(sizeof(ChunkBars) <= 256, "the self-planned pieces follow the barriers at +256");
+static_assert(sizeof(PrefillItem) == 32, "piece size");
+
+// Merge counters carry the call's epoch in their high 32 bits (see ChunkParams).
+__device__ __forceinline__ unsigned long long ld_acquire_gpu_u64(const unsigned long long *p)
+{
+    unsigned long long v;
+    asm volatile("ld.acquire.gpu.global.b64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
+    return v;
+}
+
+// Pieces of this call counted in a counter (0 when it still holds an earlier call's count).
+__device__ __forceinline__ int epoch_count(unsigned long long v, uint32_t epoch)
+{
+    return (uint32_t)(v >> 32) == epoch ? (int)(uint32_t)v : 0;
+}
+
+// Counts one more piece of this call and returns the count before it (a counter
+// left by an earlier call starts over at one). An exchange fails only when
+// another piece of the unit counted itself in between, so the loop ends within
+// as many rounds as the unit has pieces; the cap is a safeguard that flags an
+// error rather than spin.
+__device__ __forceinline__ int epoch_arrive(unsigned long long *cnt, uint32_t epoch, uint32_t *dev_err)
+{
+    unsigned long long old = *reinterpret_cast<volatile unsigned long long *>(cnt);
+    for (int i = 0; i < 4096; ++i) {
+        const bool cur = (uint32_t)(old >> 32) == epoch;
+        const unsigned long long nv = cur ? old + 1ull : (((unsigned long long)epoch << 32) | 1ull);
+        const unsigned long long prev = atomicCAS(cnt, old, nv);
+        if (prev == old)
+            return cur ? (int)(uint32_t)old : 0;
+        old = prev;
+    }
+    set_dev_error(dev_err, CPSA_DEV_WAIT_TIMEOUT);
+    return -1;
+}
+
+// The units of a self-planned batch that fall in this CTA's run (see
+// self_plan_run); I is the integer type of the tile positions: 32 bits whenever
+// the request's W tiles fit (64-bit division is a long software routine on the
+// GPU, and this walk sits on every launch's critical path), 64 bits otherwise.
+template <int NQ, typename I>
+__device__ __forceinline__ int self_plan_walk(const ChunkParams &p, PrefillItem *items, int lane, int nqt, int hb,
+                                              int nkv_last, int upq, int pairs, I run, bool cut)
+{
+    const I lo = (I)blockIdx.x * run, hi = lo + run;
+    const int prow_unit = kTileM * NQ;
+    const unsigned below = (1u << lane) - 1u;
+    const int G = nqt * upq;
+    int n = 0;
+    for (int g0 = 0; g0 < G; g0 += 32) {
+        const int g = g0 + lane;
+        const bool active = g < G;
+        const int a = g / upq, j = g - a * upq;
+        const int qt = nqt - 1 - a;
+        const int nkv = a == 0 ? nkv_last : hb + qt + 1;
+        // KV tiles of one unit column before the a-th query tile from the last
+        const I before = a == 0 ? (I)0 : (I)nkv_last + (I)(a - 1) * (I)(hb + nqt) - (I)((a - 1) * a / 2);
+        const I u0 = (I)upq * before + (I)j * (I)nkv, u1 = u0 + (I)nkv;
+        // with cuts a run takes every piece of a unit inside it; without, whole units
+        // go to the run that holds their first tile
+        const bool take = active && (cut ? (u1 > lo && u0 < hi) : (u0 >= lo && u0 < hi));
+        const unsigned m = __ballot_sync(0xffffffffu, take);
+        if (take) {
+            const int k = n + __popc(m & below);
+            if (k < kSelfPlanCap) {
+                const int kvh = j / pairs, hp = j - kvh * pairs;
+                const I c0 = u0 / run;
+                const int np = cut ? (int)((u1 - 1) / run - c0 + 1) : 1;
+                if (np == 1) {
+                    items[k] = PrefillItem{0, qt * kTileM, kvh | (hp << 16), 0, nkv, 1 << 16, -1, (int)blockIdx.x};
+                } else {
+                    const I x0 = u0 > lo ? u0 : lo, x1 = u1 < hi ? u1 : hi;
+                    items[k] = PrefillItem{0, qt * kTileM, kvh | (hp << 16), (int)(x0 - u0), (int)(x1 - u0),
+                                           ((int)blockIdx.x - (int)c0) | (np << 16), 2 * (int)c0 * prow_unit,
+                                           (int)c0};
+                }
+            }
+        }
+        n += __popc(m);
+        // units come in tile order: after one that starts at or past the run's end, none is in it
+        if (__shfl_sync(0xffffffffu, active ? (u0 >= hi ? 1 : 0) : 1, 31))
+            break;
+    }
+    return n;
+}
+
+// The pieces of this CTA's stream-K run for a batch of one prefill request,
+// computed by the CTA itself (one warp) instead of the plan kernel. Units,
+// their order (query tiles from the last, then kv heads, then head pairs), the
+// run length, the rule for cutting units and the piece fields are the plan's
+// (plan.cu: request_work, choose_split). Only the addresses of a split unit's
+// partial rows and merge counters differ: they follow from the run c0 that holds
+// the unit's first tile, rows [2 c0, 2 c0 + np) x (128 NQ) and counter c0,
+// instead of from its rank among split units (which needs the whole list). A
+// run holds at most one piece that continues a split unit (its first) and at
+// most one that starts one (its last), so a later split unit starts in run
+// c0' >= c0 + np - 1 and its rows begin at 2 c0' >= 2 c0 + 2 np - 2 >= 2 c0 + np
+// (np >= 2): no overlap, and 2 x grid x 128 NQ rows are enough (the host checks
+// that they fit before it allows cuts). A piece of run c belongs to it, so its
+// index within its unit is c - c0. Validation as in the plan, flags raised by
+// CTA 0. Writes up to kSelfPlanCap pieces; returns their number (warp-uniform).
+template <int NQ>
+__device__ __forceinline__ int self_plan_run(const ChunkParams &p, PrefillItem *items, int lane)
+{
+    const int q = __ldg(p.query_lens), s = __ldg(p.seq_lens);
+    uint32_t bad = 0;
+    if (q != p.num_tokens)
+        bad = CPSA_DEV_TOKENS_MISMATCH;
+    else if (q < 0 || s < q)
+        bad = CPSA_DEV_SEQ_LT_QUERY;
+    else if ((int64_t)s > (int64_t)p.max_blocks * p.page_size)
+        bad = CPSA_DEV_SEQ_GT_TABLE;
+    if (blockIdx.x == 0 && lane == 0) {
+        if (bad)
+            set_dev_error(p.dev_err, bad);
+        if (p.split_clamped)
+            set_dev_error(p.dev_err, CPSA_DEV_SPLITS_CLAMPED);
+    }
+    if (bad || q < 2)
+        return 0;
+    const int hist = s - q;
+    const int pairs = p.group / NQ;
+    const int upq = p.num_kv_heads * pairs;      // units per query tile
+    const int nqt = (q + kTileM - 1) / kTileM;
+    const int hb = (hist + kTileN - 1) / kTileN;
+    const int nkv_last = p.fused ? hb + nqt : (hist + q + kTileN - 1) / kTileN;
+    const long long W = (long long)upq * (nkv_last + (long long)(nqt - 1) * (hb + nqt) - (long long)(nqt - 1) * nqt / 2);
+    const int shortest = nqt == 1 ? nkv_last : hb + 1;
+    const long long grid = gridDim.x;
+    const long long run = max((W + grid - 1) / grid, (long long)kMinRunTiles);
+    const bool cut = p.split_ok && !(shortest >= run && nkv_last <= run + kCutCostTiles);
+    int n = W + run < 0x7fffffffll
+                ? self_plan_walk<NQ, int>(p, items, lane, nqt, hb, nkv_last, upq, pairs, (int)run, cut)
+                : self_plan_walk<NQ, long long>(p, items, lane, nqt, hb, nkv_last, upq, pairs, run, cut);
+    if (n > kSelfPlanCap) {
+        if (lane == 0)
+            set_dev_error(p.dev_err, CPSA_DEV_PLAN_OVERFLOW);
+        n = kSelfPlanCap;
+    }
+    return n;
+}
 
 // Cache stores of one staged K or V tile of new rows (128 rows, 128-byte
 // swizzled 64-column halves), rows [0, rows) to the slots sl of kv head kvh (lane
@@ -319,7 +463,9 @@ __device__ __noinline__ void merge_split_row_any(const ChunkParams &p, uint32_t 
     }
 }
 
-template <int D, int NQ>
+// SELF: a batch of one prefill request, planned by the kernel itself (pieces in
+// shared memory); else the plan kernel's lists in the workspace.
+template <int D, int NQ, bool SELF>
 __global__ void __launch_bounds__(352, 1)
 chunk_attn_kernel(const ChunkParams p, const __grid_constant__ CUtensorMap tm_q,
                   const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
@@ -365,7 +511,17 @@ chunk_attn_kernel(const ChunkParams p, const __grid_constant__ CUtensorMap tm_q,
     }
     // the set-up above touches no global memory; from here on the plan's output
     pdl_wait();
-    if (threadIdx.x == 0) {
+    PrefillItem *s_items = reinterpret_cast<PrefillItem *>(smem + C::kItemOff);
+    if (SELF) {
+        // a batch of one prefill request: this CTA computes its own run
+        if (warp == C::kWriteWarp) {
+            const int n = self_plan_run<NQ>(p, s_items, lane);
+            if (lane == 0) {
+                bars->it_begin = 0;
+                bars->it_end = n;
+            }
+        }
+    } else if (threadIdx.x == 0) {
         // this CTA's run of pieces, from the plan's table
         bars->it_begin = p.run_first[blockIdx.x];
         bars->it_end = p.run_first[blockIdx.x + 1];
@@ -376,6 +532,9 @@ chunk_attn_kernel(const ChunkParams p, const __grid_constant__ CUtensorMap tm_q,
     const uint32_t tmem = bars->tmem_base;
     volatile int *abort = &bars->abort;
     const int it_begin = bars->it_begin, it_end = bars->it_end;
+    const PrefillItem *items = SELF ? s_items : p.pitems;
+    // first row of a request in q / out (a self-planned batch has one request)
+    auto row0 = [&](int r) -> int { return SELF ? 0 : p.cu_q[r]; };
 
     if (warp == C::kLoadWarp) {
         // ------------------------------------------------------------ producer
@@ -384,10 +543,10 @@ chunk_attn_kernel(const ChunkParams p, const __grid_constant__ CUtensorMap tm_q,
         const uint32_t box_bytes = (uint32_t)PB * 128u;
         uint32_t q_uses = 0, slot_it = 0, tail_uses = 0;
         for (int it = it_begin; it < it_end && !*abort; ++it) {
-            const PrefillItem w = p.pitems[it];
+            const PrefillItem w = items[it];
             const int kvh = w.kvh_hp & 0xFFFF, hp = w.kvh_hp >> 16;
             const int h0 = kvh * p.group + hp * NQ;
-            const int cu = p.cu_q[w.r];
+            const int cu = row0(w.r);
             const int s_len = p.seq_lens[w.r];
             const int hist = s_len - p.query_lens[w.r];
             // tiles [0, nh) come from the cache, over keys [0, hist_end); the rest
@@ -503,7 +662,7 @@ chunk_attn_kernel(const ChunkParams p, const __grid_constant__ CUtensorMap tm_q,
             uint32_t stage_uses = 0;
             bool ok = true;
             for (int it = it_begin; it < it_end && ok && !*abort; ++it) {
-                const PrefillItem w = p.pitems[it];
+                const PrefillItem w = items[it];
                 const int kvh = w.kvh_hp & 0xFFFF, hp = w.kvh_hp >> 16;
                 const int q_len = p.query_lens[w.r];
                 const int hist = p.seq_lens[w.r] - q_len;
@@ -511,7 +670,7 @@ chunk_attn_kernel(const ChunkParams p, const __grid_constant__ CUtensorMap tm_q,
                 if (kd < w.kt0 || kd >= w.kt1)
                     continue;
                 const int rows = min(128, q_len - w.i0);
-                const int t0 = p.cu_q[w.r] + w.i0;
+                const int t0 = row0(w.r) + w.i0;
                 int64_t sl[4];
 #pragma unroll
                 for (int q = 0; q < 4; ++q) {
@@ -635,7 +794,7 @@ chunk_attn_kernel(const ChunkParams p, const __grid_constant__ CUtensorMap tm_q,
             return ok;
         };
         for (int it = it_begin; it < it_end && !aborted(); ++it) {
-            const PrefillItem w = p.pitems[it];
+            const PrefillItem w = items[it];
             const int n = w.kt1 - w.kt0;
             if (!wait(&bars->q_full, q_uses & 1))
                 break;
@@ -711,7 +870,7 @@ chunk_attn_kernel(const ChunkParams p, const __grid_constant__ CUtensorMap tm_q,
         const float sl2 = p.scale_log2;
         uint32_t s_uses = 0, o_base = 0;
         for (int it = it_begin; it < it_end && !*abort; ++it) {
-            const PrefillItem w = p.pitems[it];
+            const PrefillItem w = items[it];
             const int kvh = w.kvh_hp & 0xFFFF, hp = w.kvh_hp >> 16;
             const int h = kvh * p.group + hp * NQ + wg;
             const int q_len = p.query_lens[w.r];
@@ -826,7 +985,7 @@ chunk_attn_kernel(const ChunkParams p, const __grid_constant__ CUtensorMap tm_q,
             o_base += n;
             tc_fence_after_sync();
             const bool valid_row = i < q_len;
-            const int64_t t_row = (int64_t)p.cu_q[w.r] + i;
+            const int64_t t_row = (int64_t)row0(w.r) + i;
             const int npieces = w.piece_np >> 16;
             if (npieces > 1) {
                 // A piece of a split unit. Every warp (32 rows) decides on its own:
@@ -841,10 +1000,10 @@ chunk_attn_kernel(const ChunkParams p, const __grid_constant__ CUtensorMap tm_q,
                 // accesses are 512 contiguous bytes. The unit's partial rows keep
                 // the fp32 row pitch of the workspace (decode partials share it).
                 const int piece = w.piece_np & 0xFFFF;
-                int *cnt = p.flags + ((int64_t)w.aux * NQ + wg) * 4 + sub;
+                unsigned long long *cnt = p.flags + ((int64_t)w.aux * NQ + wg) * 4 + sub;
                 uint4 *ph = reinterpret_cast<uint4 *>(p.part_o) + (int64_t)w.pbase * (D / 4);
                 float2 *pml = reinterpret_cast<float2 *>(p.part_ml) + w.pbase;
-                int seen = lane == 0 && it + 1 == it_end ? ld_acquire_gpu(cnt) : 0;
+                int seen = lane == 0 && it + 1 == it_end ? epoch_count(ld_acquire_gpu_u64(cnt), p.epoch) : 0;
                 seen = __shfl_sync(0xffffffffu, seen, 0);
                 bool merge = seen == npieces - 1;
                 if (!merge) {
@@ -867,7 +1026,7 @@ chunk_attn_kernel(const ChunkParams p, const __grid_constant__ CUtensorMap tm_q,
                     __syncwarp();
                     if (lane == 0) {
                         fence_acq_rel_gpu();   // this warp's partial, then the count
-                        seen = atomicAdd(cnt, 1);
+                        seen = epoch_arrive(cnt, p.epoch, p.dev_err);
                         fence_acq_rel_gpu();   // the count, then the other partials
                     }
                     seen = __shfl_sync(0xffffffffu, seen, 0);
@@ -932,7 +1091,7 @@ cudaError_t launch_chunk_t(const ChunkParams &p, const CUtensorMap &tq, const CU
                            cudaStream_t s, bool early)
 {
     using C = ChunkCfg<D, NQ>;
-    auto k = chunk_attn_kernel<D, NQ>;
+    auto k = p.self_plan ? chunk_attn_kernel<D, NQ, true> : chunk_attn_kernel<D, NQ, false>;
     cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
     if (e != cudaSuccess)
         return e;

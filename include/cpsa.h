@@ -72,6 +72,7 @@ extern "C" {
 #define CPSA_DEV_SEQ_GT_TABLE 0x10u       /* seq_len > max_blocks_per_req * page_size: request skipped */
 #define CPSA_DEV_SPLITS_CLAMPED 0x20u     /* info: partials did not fit the workspace, one KV split used */
 #define CPSA_DEV_WAIT_TIMEOUT 0x40u       /* an on-chip wait hit its limit; outputs of this call invalid */
+#define CPSA_DEV_PLAN_OVERFLOW 0x80u      /* a self-planned chunk-kernel run held more pieces than it can keep */
 
 /*
  * Write the new tokens' K and V into their cache slots ([DS] section 3.1,
@@ -133,9 +134,14 @@ size_t cpp_attn_workspace_min_bytes(int num_reqs, int64_t num_tokens, int num_q_
  * row's last-bit rounding (not its value) can depend on the other requests; it
  * does not depend on timing.
  * max_kv_splits = 1 turns off both kinds of split.
+ * A batch of one prefill request (num_reqs == 1, num_tokens >= 2) of at most
+ * about 4k tokens (while every CTA's run fits 56 pieces) launches the chunk
+ * kernel alone: its CTAs compute their own runs, with the same units and cuts.
  * workspace: device memory of at least cpp_attn_workspace_min_bytes(...) with
  * the same (num_reqs, num_tokens, heads, head_dim, max_kv_splits); it is
- * scratch, overwritten by each call; calls that share it must be stream-ordered.
+ * scratch, overwritten by each call; calls that share it must be stream-ordered
+ * (each call tags the merge counters it leaves there with its own epoch, so no
+ * call needs the workspace cleared).
  */
 int cpp_chunked_prefill_attn(const void *q, const void *k_cache, const void *v_cache,
                              const int32_t *query_lens, const int32_t *seq_lens,
@@ -148,7 +154,7 @@ int cpp_chunked_prefill_attn(const void *q, const void *k_cache, const void *v_c
 /*
  * cpp_chunked_prefill_attn with timing marks: when `events` is not NULL it
  * points to 5 cudaEvent_t handles (any may be NULL) recorded on `stream`:
- * [0] before the plan kernel, [1] before the chunk kernel, [2] after it,
+ * [0] before the plan kernel (when one runs), [1] before the chunk kernel, [2] after it,
  * [3] after the decode kernel, [4] after the combine kernel (kernels that a
  * batch does not need are not launched; their marks follow the previous one).
  * For profiling harnesses; the computation is identical, its kernels launched
