@@ -838,6 +838,7 @@ def main():
                 "kernel": "chunk_attn_kernel<128,2,true> (one request per call: runs planned by the kernel itself)", "peak_source": f"{peak_src} bf16 dense (burst)",
                 "per_launch_flops": per_launch_flops, "per_launch_ms": round(per_launch_ms, 4),
                 "last_chunk_ms": round(float(km[:, -1].mean()), 4),
+                "per_chunk_ms": [round(float(x), 4) for x in km.mean(axis=0)],
                 "last_chunk_tflops": round(chunk_flops((N_CHUNKS - 1) * CHUNK, CHUNK) / (km[:, -1].mean() * 1e-3) / 1e12, 2)}
     # per chunk: split, [KV write,] plan, chunk attention (a single prefill
     # request launches neither the decode nor the combine kernel)

@@ -87,6 +87,46 @@ bool make_map4_halves(CUtensorMap *m, const void *base, int page_size, uint64_t 
     return r == CUDA_SUCCESS;
 }
 
+// View of a cache [pages][Hkv][P][D] for the grouped decode kernel, innermost
+// dimension first: 64 columns, P rows, (2 halves of head_dim 128,) Hkv heads,
+// pages. A box of `rows` rows of `heads` consecutive heads (both halves) lands as
+// [head][half][rows][128 B], 128-byte swizzled.
+bool make_map_group(CUtensorMap *m, const void *base, int head_dim, int page_size, int num_kv_heads,
+                    int64_t num_pages, uint32_t rows, uint32_t heads)
+{
+    auto enc = encode_fn();
+    if (!enc)
+        return false;
+    const uint64_t row_bytes = (uint64_t)head_dim * 2;
+    const uint64_t head_bytes = row_bytes * (uint64_t)page_size;
+    CUresult r;
+    if (head_dim == 128) {
+        cuuint64_t dims[5] = {64, (cuuint64_t)page_size, 2, (cuuint64_t)num_kv_heads, (cuuint64_t)num_pages};
+        cuuint64_t strides[4] = {row_bytes, 128, head_bytes, head_bytes * (uint64_t)num_kv_heads};
+        cuuint32_t box[5] = {64, rows, 2, heads, 1};
+        cuuint32_t estr[5] = {1, 1, 1, 1, 1};
+        r = enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 5, const_cast<void *>(base), dims, strides, box, estr,
+                CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    } else {
+        cuuint64_t dims[4] = {64, (cuuint64_t)page_size, (cuuint64_t)num_kv_heads, (cuuint64_t)num_pages};
+        cuuint64_t strides[3] = {row_bytes, head_bytes, head_bytes * (uint64_t)num_kv_heads};
+        cuuint32_t box[4] = {64, rows, heads, 1};
+        cuuint32_t estr[4] = {1, 1, 1, 1};
+        r = enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void *>(base), dims, strides, box, estr,
+                CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    }
+    return r == CUDA_SUCCESS;
+}
+
+// kv heads per decode item: groups of 8 (else 4) heads read every page's heads
+// together (the grouped decode kernel); 1 for other head counts.
+int decode_heads_per_item(int num_kv_heads)
+{
+    return num_kv_heads % 8 == 0 ? 8 : (num_kv_heads % 4 == 0 ? 4 : 1);
+}
+
 int nq_for_group(int group) { return (group % 2 == 0) ? 2 : 1; }
 
 // Every attention call gets its own nonzero epoch: the merge counters it leaves
@@ -338,6 +378,8 @@ int attn_impl(const void *q, const void *k_new, const void *v_new, const int64_t
     pp.group = group;
     pp.nq = nq;
     pp.max_splits = max_kv_splits;
+    const int dec_heads = decode_heads_per_item(num_kv_heads);
+    pp.dec_heads = dec_heads;
     pp.chunk_grid = sms < kMaxChunkGrid ? sms : kMaxChunkGrid;
     pp.fused = fused ? 1 : 0;
     pp.prow_capacity = cap;
@@ -404,9 +446,15 @@ int attn_impl(const void *q, const void *k_new, const void *v_new, const int64_t
                   !make_map(&tvn, v_new, D, (uint64_t)num_kv_heads, (uint64_t)num_tokens, D * 2,
                             D * 2 * num_kv_heads, 64, 1, 128)))
         return CPSA_ERR_CUDA;
-    // decode: one box per page-head block (at most 64 rows) covering all of head_dim
+    // decode: grouped, one box per page (16 rows, 8 at page 8) covering the item's
+    // heads and all of head_dim; else one box per page-head block (at most 64 rows)
     const uint32_t pb_dec = page_size < kDecodeChunk ? page_size : kDecodeChunk;
-    if (head_dim == 128) {
+    if (dec_heads > 1) {
+        const uint32_t rows = page_size < 16 ? (uint32_t)page_size : 16u;
+        if (!make_map_group(&tkd, k_cache, head_dim, page_size, num_kv_heads, num_pages, rows, dec_heads) ||
+            !make_map_group(&tvd, v_cache, head_dim, page_size, num_kv_heads, num_pages, rows, dec_heads))
+            return CPSA_ERR_CUDA;
+    } else if (head_dim == 128) {
         if (!make_map4_halves(&tkd, k_cache, page_size, rows_kv, pb_dec) ||
             !make_map4_halves(&tvd, v_cache, page_size, rows_kv, pb_dec))
             return CPSA_ERR_CUDA;
@@ -440,7 +488,9 @@ int attn_impl(const void *q, const void *k_new, const void *v_new, const int64_t
     dp.k_cache_ptr = k_cache;
     dp.v_cache_ptr = v_cache;
     int grid_d = single_prefill ? 0 : (int)(L.max_ditems < sms ? L.max_ditems : sms);
-    if (grid_d > 0 && launch_decode_attn(dp, tkd, tvd, head_dim, grid_d, s, early) != cudaSuccess)
+    if (grid_d > 0 &&
+        (dec_heads > 1 ? launch_decode_group(dp, tkd, tvd, head_dim, dec_heads, grid_d, s, early)
+                       : launch_decode_attn(dp, tkd, tvd, head_dim, grid_d, s, early)) != cudaSuccess)
         return CPSA_ERR_CUDA;
     mark(3, s);
 

@@ -437,6 +437,372 @@ cudaError_t launch_decode_t(const DecodeParams &p, const CUtensorMap &tk, const 
     return launch_pdl(early, k, dim3(grid), dim3(C::kThreads), C::kSmemBytes, s, p, tk, tv);
 }
 
+
+// ---------------------------------------------------------------------------
+// Grouped decode: one item covers a group of HG kv heads (4 or 8) of one decode
+// row, so its stages read every head of a page at once. The cache is
+// [pages][Hkv][P][D]: the heads of a page are contiguous, and a whole-page read
+// stream runs near the copy bandwidth (a copy-only probe of the Sarathi-sized
+// cache: 6.9-7.1 TB/s), where one head's 4 KB block per page at a time does not
+// (the per-head kernel above: about 5 TB/s even without its arithmetic).
+// CTA: HG consumer warps, warp h owning kv head group * HG + h over all keys of
+// the item (no merge between warps), then one producer warp.
+// Stage: 16 keys of all HG heads, K and V, one TMA box per page (two at page 8)
+// covering the heads and both 64-column halves of head_dim: a 5-D view of the
+// cache (columns, rows, halves, heads, pages), 128-byte swizzled, landing as
+// [box][head][half][rows][128 B]. One lane announces and issues all of a
+// stage's copies. Page numbers of 32 stages are looked up at a time, the next
+// window while the current one streams.
+template <int D, int HG>
+struct GDecCfg {
+    static constexpr int kHalves = D / 64;
+    static constexpr int kKeys = 16;                                  // keys per stage
+    static constexpr int kTileBytes = HG * kKeys * D * 2;             // K (or V) of one stage
+    static constexpr int kStageBytes = 2 * kTileBytes;
+    static constexpr int kStagesRaw = 196608 / kStageBytes;
+    static constexpr int kStages = kStagesRaw > 12 ? 12 : (kStagesRaw < 2 ? 2 : kStagesRaw);
+    static constexpr int kBarOff = kStages * kStageBytes;
+    static constexpr int kSmemBytes = kBarOff + 512 + 1024;
+    static constexpr int kThreads = 32 * (HG + 1);
+    static_assert(kSmemBytes <= 232448, "beyond the 227 KB of shared memory a CTA may have");
+};
+
+struct GDecBars {
+    uint64_t full[12], empty[12];
+    uint64_t patch;   // fused KV write: copies of the stage that gets the new row
+    int abort;
+};
+
+// Byte address of element (key, head, col) of a grouped stage tile, boxes of
+// 2^lgrb rows: [box][head][half][row][128 B], 16-byte chunks swizzled by the row.
+template <int D, int HG>
+__device__ __forceinline__ uint32_t gdec_addr(uint32_t base, int key, int head, int col, int lgrb)
+{
+    const int b = key >> lgrb, kr = key & ((1 << lgrb) - 1);
+    const int c = col >> 6, ch = (col & 63) >> 3;
+    return base + ((uint32_t)((b * HG + head) * (D / 64) + c) << (lgrb + 7)) + ((uint32_t)kr << 7) +
+           ((ch ^ (kr & 7)) << 4) + (col & 7) * 2;
+}
+
+template <int D, int HG, bool HI>
+__global__ void __launch_bounds__(GDecCfg<D, HG>::kThreads, 1)
+decode_group_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap tm_k,
+                    const __grid_constant__ CUtensorMap tm_v)
+{
+    using C = GDecCfg<D, HG>;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
+    GDecBars *bars = reinterpret_cast<GDecBars *>(smem + C::kBarOff);
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int G = p.group;
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < C::kStages; ++s) {
+            mbar_init(&bars->full[s], 1);
+            mbar_init(&bars->empty[s], HG);
+        }
+        mbar_init(&bars->patch, 1);
+        bars->abort = 0;
+        fence_barrier_init();
+    }
+    // set-up above touches no global memory: from here on the plan's output
+    pdl_trigger();
+    pdl_wait();
+    const int n_items = p.counts[kCntDecode];
+    __syncthreads();
+    volatile int *abort = &bars->abort;
+    const int RB = p.page_size < C::kKeys ? p.page_size : C::kKeys;   // rows per box: 8 or 16
+    const int lgrb = RB == 8 ? 3 : 4;
+    const int NBX = C::kKeys / RB;                                    // boxes per stage: 1 or 2
+
+    if (warp == HG) {
+        // ------------------------------------------------------------ producer
+        if (lane == 0) {
+            tma_prefetch_desc(&tm_k);
+            tma_prefetch_desc(&tm_v);
+        }
+        const uint32_t box_bytes = (uint32_t)HG * RB * D * 2;
+        uint32_t g = 0, patch_uses = 0;
+        bool stop = false;
+        for (int it = blockIdx.x; it < n_items && !stop && !*abort; it += gridDim.x) {
+            const DecodeItem w = p.ditems[it];
+            const int32_t *bt_row = p.block_table + (int64_t)w.r * p.max_blocks;
+            const int head0 = w.kvh * HG;
+            // the row's own key, when this item's range ends with it and the KV write is fused
+            const int knew = (p.fused && w.key1 == p.seq_lens[w.r]) ? w.key1 - 1 : -1;
+            // lane j holds the page numbers of stage 32 m + j of window m (box 0, and box 1
+            // at page 8); the next window's are loaded while the current one streams
+            auto lookup = [&](int m, int b) -> int {
+                const int key = w.key0 + (32 * m + lane) * C::kKeys + b * RB;
+                return (b < NBX && key < w.key1) ? __ldg(bt_row + key / p.page_size) : -1;
+            };
+            int cur0 = lookup(0, 0), cur1 = lookup(0, 1);
+            int nxt0 = lookup(1, 0), nxt1 = lookup(1, 1);
+            int j = 0;
+            for (int c0 = w.key0; c0 < w.key1; c0 += C::kKeys, ++g, ++j) {
+                if (j > 0 && (j & 31) == 0) {
+                    cur0 = nxt0;
+                    cur1 = nxt1;
+                    nxt0 = lookup((j >> 5) + 1, 0);
+                    nxt1 = lookup((j >> 5) + 1, 1);
+                }
+                const int pg0 = __shfl_sync(0xffffffffu, cur0, j & 31);
+                const int pg1 = __shfl_sync(0xffffffffu, cur1, j & 31);
+                const int stage = g % C::kStages;
+                if (g >= (uint32_t)C::kStages &&
+                    !mbar_wait(&bars->empty[stage], ((g / C::kStages) - 1) & 1, abort)) {
+                    stop = true;
+                    break;
+                }
+                uint8_t *kdst = smem + stage * C::kStageBytes;
+                uint8_t *vdst = kdst + C::kTileBytes;
+                const bool patch = knew >= c0 && knew < c0 + C::kKeys;
+                uint64_t *bar = patch ? &bars->patch : &bars->full[stage];
+                if (lane == 0) {
+                    // one lane announces the stage's bytes, then issues its copies
+                    bool v0 = false, v1 = false;
+                    if (c0 < w.key1) {
+                        v0 = pg0 >= 0 && pg0 < p.num_pages;
+                        if (!v0)
+                            set_dev_error(p.dev_err, CPSA_DEV_PAGE_OUT_OF_RANGE);
+                    }
+                    if (NBX == 2 && c0 + RB < w.key1) {
+                        v1 = pg1 >= 0 && pg1 < p.num_pages;
+                        if (!v1)
+                            set_dev_error(p.dev_err, CPSA_DEV_PAGE_OUT_OF_RANGE);
+                    }
+                    mbar_arrive_expect_tx(bar, (uint32_t)((v0 ? 2 : 0) + (v1 ? 2 : 0)) * box_bytes);
+#pragma unroll
+                    for (int b = 0; b < 2; ++b) {
+                        const bool vb = b == 0 ? v0 : v1;
+                        if (!vb)
+                            continue;
+                        const int pg = b == 0 ? pg0 : pg1;
+                        const int off = (c0 + b * RB) % p.page_size;
+                        if (C::kHalves == 2) {
+                            tma_load_5d(kdst + b * box_bytes, &tm_k, bar, 0, off, 0, head0, pg);
+                            tma_load_5d(vdst + b * box_bytes, &tm_v, bar, 0, off, 0, head0, pg);
+                        } else {
+                            tma_load_4d(kdst + b * box_bytes, &tm_k, bar, 0, off, head0, pg);
+                            tma_load_4d(vdst + b * box_bytes, &tm_v, bar, 0, off, head0, pg);
+                        }
+                    }
+                }
+                __syncwarp();
+                if (patch) {
+                    if (!mbar_wait(&bars->patch, patch_uses & 1u, abort)) {
+                        stop = true;
+                        break;
+                    }
+                    ++patch_uses;
+                    // the new token's K and V rows of the HG heads, 16-byte chunks over the
+                    // lanes: into the stage (over the cache's old bytes) and to the slot
+                    const int rr = knew - c0;
+                    const int64_t slot = __ldg(p.slot_mapping + w.t);
+                    constexpr int CPR = D / 8;
+                    for (int x = lane; x < 2 * HG * CPR; x += 32) {
+                        const int which = x / (HG * CPR), rem = x - which * (HG * CPR);
+                        const int h = rem / CPR, ch = rem - h * CPR;
+                        const int64_t src = ((int64_t)w.t * p.num_kv_heads + head0 + h) * CPR + ch;
+                        const uint4 val = __ldg(reinterpret_cast<const uint4 *>(which ? p.v_new : p.k_new) + src);
+                        uint8_t *tile = which ? vdst : kdst;
+                        *reinterpret_cast<uint4 *>(tile + (gdec_addr<D, HG>(0, rr, h, ch * 8, lgrb))) = val;
+                        if (slot >= 0 && slot < p.num_pages * (int64_t)p.page_size) {
+                            const int lg_p = __ffs(p.page_size) - 1;   // page_size is a power of two
+                            const int64_t spg = slot >> lg_p, po = slot & (p.page_size - 1);
+                            reinterpret_cast<uint4 *>(which ? p.v_cache_w : p.k_cache_w)
+                                [((spg * p.num_kv_heads + head0 + h) * p.page_size + po) * CPR + ch] = val;
+                        }
+                    }
+                    if (lane == 0 && slot >= p.num_pages * (int64_t)p.page_size)
+                        set_dev_error(p.dev_err, CPSA_DEV_SLOT_OUT_OF_RANGE);
+                    fence_proxy_async_smem();   // the patch before later copies into this stage
+                    __syncwarp();
+                    if (lane == 0)
+                        mbar_arrive(&bars->full[stage]);
+                }
+            }
+        }
+        return;
+    }
+
+    // ---------------------------------------------------------------- consumers
+    // Warp h: kv head w.kvh * HG + h and its G q heads (the M rows of
+    // mma.sync m16n8k16, rows >= G zero; rows lane/4 and, when HI, lane/4 + 8).
+    constexpr int R = HI ? 2 : 1;
+    const float sl2 = p.scale_log2;
+    const int qrow = lane >> 2;
+    const int qcol = (lane & 3) * 2;
+    const int h = warp;
+    uint32_t g = 0;
+    for (int it = blockIdx.x; it < n_items; it += gridDim.x) {
+        const DecodeItem w = p.ditems[it];
+        const int nch = (w.key1 - w.key0 + C::kKeys - 1) / C::kKeys;
+        const int kvh = w.kvh * HG + h;
+        uint32_t qa[D / 16][4];
+        {
+            const uint32_t *qsrc = reinterpret_cast<const uint32_t *>(
+                reinterpret_cast<const __nv_bfloat16 *>(p.q) + ((int64_t)w.t * p.num_q_heads + kvh * G) * D);
+#pragma unroll
+            for (int kk = 0; kk < D / 16; ++kk) {
+#pragma unroll
+                for (int rr = 0; rr < 2; ++rr) {
+                    const int row = qrow + 8 * rr;
+                    const bool live = (rr == 0 || HI) && row < G;
+                    qa[kk][rr] = live ? __ldg(qsrc + (row * D + kk * 16 + qcol) / 2) : 0u;
+                    qa[kk][2 + rr] = live ? __ldg(qsrc + (row * D + kk * 16 + 8 + qcol) / 2) : 0u;
+                }
+            }
+        }
+        float m_run[R], l_run[R];
+#pragma unroll
+        for (int rr = 0; rr < R; ++rr) {
+            m_run[rr] = -INFINITY;
+            l_run[rr] = 0.f;
+        }
+        float o[D / 8][4];
+#pragma unroll
+        for (int nt = 0; nt < D / 8; ++nt) o[nt][0] = o[nt][1] = o[nt][2] = o[nt][3] = 0.f;
+
+        for (int j = 0; j < nch; ++j) {
+            const uint32_t gg = g + j;
+            const int stage = gg % C::kStages;
+            if (!mbar_wait(&bars->full[stage], (gg / C::kStages) & 1, abort))
+                break;
+            const int c0 = w.key0 + j * C::kKeys;
+            const int nv = min(C::kKeys, w.key1 - c0);   // valid keys of this stage (>= 1)
+            uint8_t *kst = smem + stage * C::kStageBytes;
+            uint8_t *vst = kst + C::kTileBytes;
+            if (nv < C::kKeys) {
+                // value rows past the range may hold anything (NaN included): zero this
+                // head's (whole 128-byte half-rows, so the swizzle does not matter)
+                const int nchunks = (C::kKeys - nv) * C::kHalves * 8;
+                for (int x = lane; x < nchunks; x += 32) {
+                    const int row = nv + x / (C::kHalves * 8);
+                    const int half = (x >> 3) % C::kHalves;
+                    const int b = row >> lgrb, kr = row & ((1 << lgrb) - 1);
+                    *reinterpret_cast<uint4 *>(vst + (((b * HG + h) * C::kHalves + half) << (lgrb + 7)) + (kr << 7) +
+                                               (x & 7) * 16) = make_uint4(0, 0, 0, 0);
+                }
+                __syncwarp();
+            }
+            const uint32_t kb = smem_u32(kst), vb = smem_u32(vst);
+            const int mat = lane >> 3, mrow = lane & 7;
+            // S = q K^T over the stage's 16 keys: 2 n-tiles of 8
+            float s[2][4];
+#pragma unroll
+            for (int nt = 0; nt < 2; ++nt) s[nt][0] = s[nt][1] = s[nt][2] = s[nt][3] = 0.f;
+#pragma unroll
+            for (int kk = 0; kk < D / 16; ++kk) {
+                uint32_t b0, b1, b2, b3;
+                ldsm_x4(gdec_addr<D, HG>(kb, mrow + (mat >> 1) * 8, h, kk * 16 + (mat & 1) * 8, lgrb), b0, b1, b2, b3);
+                mma_bf16(s[0], qa[kk], b0, b1);
+                mma_bf16(s[1], qa[kk], b2, b3);
+            }
+            uint32_t pa[4];
+            pa[0] = pa[1] = pa[2] = pa[3] = 0u;
+#pragma unroll
+            for (int rr = 0; rr < R; ++rr) {
+                float mx = -INFINITY;
+#pragma unroll
+                for (int nt = 0; nt < 2; ++nt) {
+#pragma unroll
+                    for (int e = 0; e < 2; ++e) {
+                        if (nt * 8 + qcol + e >= nv) s[nt][2 * rr + e] = -INFINITY;
+                        mx = fmaxf(mx, s[nt][2 * rr + e]);
+                    }
+                }
+                mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
+                mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
+                const float m_new = fmaxf(m_run[rr], mx * sl2);
+                const float alpha = m_new == m_run[rr] ? 1.f : ex2_approx(m_run[rr] - m_new);
+                m_run[rr] = m_new;
+                const float mref = m_new == -INFINITY ? 0.f : m_new;
+                float psum = 0.f;
+#pragma unroll
+                for (int nt = 0; nt < 2; ++nt) {
+                    const float p0 = ex2_approx(fmaf(s[nt][2 * rr], sl2, -mref));
+                    const float p1 = ex2_approx(fmaf(s[nt][2 * rr + 1], sl2, -mref));
+                    psum += p0 + p1;
+                    pa[nt * 2 + rr] = pack_bf16x2(p0, p1);
+                }
+                l_run[rr] = l_run[rr] * alpha + psum;
+#pragma unroll
+                for (int nt = 0; nt < D / 8; ++nt) {
+                    o[nt][2 * rr] *= alpha;
+                    o[nt][2 * rr + 1] *= alpha;
+                }
+            }
+            // O += P V
+#pragma unroll
+            for (int np = 0; np < D / 16; ++np) {
+                uint32_t b0, b1, b2, b3;
+                ldsm_x4_t(gdec_addr<D, HG>(vb, mrow + (mat & 1) * 8, h, np * 16 + (mat >> 1) * 8, lgrb), b0, b1, b2,
+                          b3);
+                mma_bf16(o[2 * np], pa, b0, b1);
+                mma_bf16(o[2 * np + 1], pa, b2, b3);
+            }
+            if (nv < C::kKeys)
+                fence_proxy_async_smem();   // our zeroing writes before the next copy into this stage
+            __syncwarp();
+            if (lane == 0)
+                mbar_arrive(&bars->empty[stage]);
+        }
+        g += nch;
+        // this warp's rows are complete: the bf16 row, or the split's partial
+#pragma unroll
+        for (int rr = 0; rr < R; ++rr) {
+            float lq = l_run[rr];
+            lq += __shfl_xor_sync(0xffffffffu, lq, 1);
+            lq += __shfl_xor_sync(0xffffffffu, lq, 2);
+            const int row = qrow + 8 * rr;
+            if (row >= G)
+                continue;
+            const int hq = kvh * G + row;
+            if (w.nsplit > 1) {
+                const int64_t pr = (int64_t)w.pbase + (int64_t)hq * w.nsplit + w.split;
+#pragma unroll
+                for (int nt = 0; nt < D / 8; ++nt)
+                    *reinterpret_cast<float2 *>(p.part_o + pr * D + nt * 8 + qcol) =
+                        make_float2(o[nt][2 * rr], o[nt][2 * rr + 1]);
+                if ((lane & 3) == 0)
+                    reinterpret_cast<float2 *>(p.part_ml)[pr] = make_float2(m_run[rr], lq);
+            } else {
+                const float inv = lq > 0.f ? 1.f / lq : 0.f;
+                uint32_t *dst = reinterpret_cast<uint32_t *>(reinterpret_cast<__nv_bfloat16 *>(p.out) +
+                                                             ((int64_t)w.t * p.num_q_heads + hq) * D + qcol);
+#pragma unroll
+                for (int nt = 0; nt < D / 8; ++nt)
+                    dst[nt * 4] = pack_bf16x2(o[nt][2 * rr] * inv, o[nt][2 * rr + 1] * inv);
+            }
+        }
+    }
+    if (threadIdx.x == 0 && *abort)
+        set_dev_error(p.dev_err, CPSA_DEV_WAIT_TIMEOUT);
+}
+
+template <int D, int HG, bool HI>
+cudaError_t launch_decode_group_t(const DecodeParams &p, const CUtensorMap &tk, const CUtensorMap &tv, int grid,
+                                  cudaStream_t s, bool early)
+{
+    using C = GDecCfg<D, HG>;
+    auto k = decode_group_kernel<D, HG, HI>;
+    cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
+    if (e != cudaSuccess)
+        return e;
+    return launch_pdl(early, k, dim3(grid), dim3(C::kThreads), C::kSmemBytes, s, p, tk, tv);
+}
+
+template <int HG>
+cudaError_t launch_decode_group_hg(const DecodeParams &p, const CUtensorMap &tk, const CUtensorMap &tv, int head_dim,
+                                   int grid, cudaStream_t s, bool early)
+{
+    if (p.group > 8)
+        return head_dim == 128 ? launch_decode_group_t<128, HG, true>(p, tk, tv, grid, s, early)
+                               : launch_decode_group_t<64, HG, true>(p, tk, tv, grid, s, early);
+    return head_dim == 128 ? launch_decode_group_t<128, HG, false>(p, tk, tv, grid, s, early)
+                           : launch_decode_group_t<64, HG, false>(p, tk, tv, grid, s, early);
+}
+
 }  // namespace
 
 cudaError_t launch_decode_attn(const DecodeParams &p, const CUtensorMap &tk, const CUtensorMap &tv, int head_dim,
@@ -447,6 +813,13 @@ cudaError_t launch_decode_attn(const DecodeParams &p, const CUtensorMap &tk, con
                                : launch_decode_t<64, true>(p, tk, tv, grid, s, early);
     return head_dim == 128 ? launch_decode_t<128, false>(p, tk, tv, grid, s, early)
                            : launch_decode_t<64, false>(p, tk, tv, grid, s, early);
+}
+
+cudaError_t launch_decode_group(const DecodeParams &p, const CUtensorMap &tk, const CUtensorMap &tv, int head_dim,
+                                int heads_per_item, int grid, cudaStream_t s, bool early)
+{
+    return heads_per_item == 8 ? launch_decode_group_hg<8>(p, tk, tv, head_dim, grid, s, early)
+                               : launch_decode_group_hg<4>(p, tk, tv, head_dim, grid, s, early);
 }
 
 }  // namespace cpsa

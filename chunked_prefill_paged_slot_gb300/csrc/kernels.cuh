@@ -74,6 +74,10 @@ cudaError_t launch_chunk_attn(const ChunkParams &p, const CUtensorMap &tq, const
                               int nq, int grid, cudaStream_t s, bool early);
 cudaError_t launch_decode_attn(const DecodeParams &p, const CUtensorMap &tk, const CUtensorMap &tv, int head_dim,
                                int grid, cudaStream_t s, bool early);
+// the grouped decode kernel: items of heads_per_item (4 or 8) kv heads; tk / tv
+// are the grouped views of the caches (see abi.cu: make_map_group)
+cudaError_t launch_decode_group(const DecodeParams &p, const CUtensorMap &tk, const CUtensorMap &tv, int head_dim,
+                                int heads_per_item, int grid, cudaStream_t s, bool early);
 cudaError_t launch_combine(const CombineParams &p, int head_dim, int grid, cudaStream_t s, bool early);
 
 cudaError_t launch_kv_cache_write(const void *k, const void *v, const int64_t *slot_mapping,

@@ -126,7 +126,8 @@ __device__ Counts request_work(const PlanParams &p, int r, const Req &rq, int ti
     if (rq.q == 1) {
         const int ns = decode_splits(rq, max_splits);
         const int nch = ceil_div(rq.s, kDecodeChunk);
-        c.ditems = p.Hkv * ns;
+        const int ngroups = p.Hkv / p.dec_heads;   // decode items per split
+        c.ditems = ngroups * ns;
         if (ns > 1) {
             c.prows = p.Hq * ns;
             c.citems = 1;
@@ -134,7 +135,7 @@ __device__ Counts request_work(const PlanParams &p, int r, const Req &rq, int ti
         }
         if (emit) {
             for (int k = lane; k < c.ditems; k += 32) {
-                const int sp = k / p.Hkv, kvh = k % p.Hkv;
+                const int sp = k / ngroups, kvh = k % ngroups;
                 const int c0 = sp * nch / ns, c1 = (sp + 1) * nch / ns;
                 const int key1 = min(c1 * kDecodeChunk, rq.s);
                 p.ditems[off.ditems + k] = DecodeItem{r, kvh, c0 * kDecodeChunk, key1, sp, ns,

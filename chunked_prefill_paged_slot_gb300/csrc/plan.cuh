@@ -56,7 +56,8 @@ struct alignas(16) PrefillItem {
 };
 
 // A decode item: the single new token (global row t) of request r, all q heads
-// of kv head kvh, keys [key0, key1) of split `split`.
+// of kv head kvh (the grouped decode kernel: of kv heads kvh * dec_heads ..
+// kvh * dec_heads + dec_heads - 1), keys [key0, key1) of split `split`.
 struct DecodeItem {
     int32_t r, kvh, key0, key1, split, nsplit, pbase, t;
 };
@@ -140,6 +141,7 @@ struct PlanParams {
     int page_size;
     int Hq, Hkv, group, nq;    // nq: q heads per chunk-kernel CTA (1 or 2)
     int max_splits;
+    int dec_heads;             // kv heads per decode item: 1, or a group of 4 or 8 (the grouped decode kernel)
     int chunk_grid;            // CTAs of the chunk kernel (stream-K runs)
     int fused;                 // KV write fused: the chunk's own keys form tiles of their own
     int64_t prow_capacity;     // partial rows that fit

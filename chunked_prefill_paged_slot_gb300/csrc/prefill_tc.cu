@@ -105,6 +105,13 @@ __device__ __forceinline__ unsigned long long ld_acquire_gpu_u64(const unsigned 
     return v;
 }
 
+__device__ __forceinline__ unsigned long long ld_relaxed_gpu_u64(const unsigned long long *p)
+{
+    unsigned long long v;
+    asm volatile("ld.relaxed.gpu.global.b64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
+    return v;
+}
+
 // Pieces of this call counted in a counter (0 when it still holds an earlier call's count).
 __device__ __forceinline__ int epoch_count(unsigned long long v, uint32_t epoch)
 {
@@ -112,13 +119,15 @@ __device__ __forceinline__ int epoch_count(unsigned long long v, uint32_t epoch)
 }
 
 // Counts one more piece of this call and returns the count before it (a counter
-// left by an earlier call starts over at one). An exchange fails only when
-// another piece of the unit counted itself in between, so the loop ends within
-// as many rounds as the unit has pieces; the cap is a safeguard that flags an
-// error rather than spin.
-__device__ __forceinline__ int epoch_arrive(unsigned long long *cnt, uint32_t epoch, uint32_t *dev_err)
+// left by an earlier call starts over at one). `old` is the caller's earlier
+// read of the counter, the first guess of the exchange (read before the
+// partial's stores, its latency overlaps them). An exchange fails only when the
+// guess was stale or another piece counted itself in between, so the loop ends
+// within a few more rounds than the unit has pieces; the cap is a safeguard that
+// flags an error rather than spin.
+__device__ __forceinline__ int epoch_arrive(unsigned long long *cnt, uint32_t epoch, unsigned long long old,
+                                            uint32_t *dev_err)
 {
-    unsigned long long old = *reinterpret_cast<volatile unsigned long long *>(cnt);
     for (int i = 0; i < 4096; ++i) {
         const bool cur = (uint32_t)(old >> 32) == epoch;
         const unsigned long long nv = cur ? old + 1ull : (((unsigned long long)epoch << 32) | 1ull);
@@ -136,8 +145,8 @@ __device__ __forceinline__ int epoch_arrive(unsigned long long *cnt, uint32_t ep
 // the request's W tiles fit (64-bit division is a long software routine on the
 // GPU, and this walk sits on every launch's critical path), 64 bits otherwise.
 template <int NQ, typename I>
-__device__ __forceinline__ int self_plan_walk(const ChunkParams &p, PrefillItem *items, int lane, int nqt, int hb,
-                                              int nkv_last, int upq, int pairs, I run, bool cut)
+__device__ __forceinline__ int self_plan_walk(PrefillItem *items, int lane, int nqt, int hb, int nkv_last, int upq,
+                                              int pairs, I run, bool cut)
 {
     const I lo = (I)blockIdx.x * run, hi = lo + run;
     const int prow_unit = kTileM * NQ;
@@ -196,42 +205,52 @@ __device__ __forceinline__ int self_plan_walk(const ChunkParams &p, PrefillItem 
 // that they fit before it allows cuts). A piece of run c belongs to it, so its
 // index within its unit is c - c0. Validation as in the plan, flags raised by
 // CTA 0. Writes up to kSelfPlanCap pieces; returns their number (warp-uniform).
+// Everything the self plan reads from the kernel's parameters, passed by value:
+// the plan lives out of line (so that its registers do not weigh on the softmax
+// and MMA loops, which sit at the register cap), and a reference to the
+// parameter block would make every thread copy the block to local memory.
+struct SelfPlanArgs {
+    const int32_t *query_lens, *seq_lens;
+    uint32_t *dev_err;
+    int num_tokens, max_blocks, page_size, group, num_kv_heads, fused, split_ok, split_clamped;
+};
+
 template <int NQ>
-__device__ __forceinline__ int self_plan_run(const ChunkParams &p, PrefillItem *items, int lane)
+__device__ __noinline__ int self_plan_run(const SelfPlanArgs a, PrefillItem *items, int lane)
 {
-    const int q = __ldg(p.query_lens), s = __ldg(p.seq_lens);
+    const int q = __ldg(a.query_lens), s = __ldg(a.seq_lens);
     uint32_t bad = 0;
-    if (q != p.num_tokens)
+    if (q != a.num_tokens)
         bad = CPSA_DEV_TOKENS_MISMATCH;
     else if (q < 0 || s < q)
         bad = CPSA_DEV_SEQ_LT_QUERY;
-    else if ((int64_t)s > (int64_t)p.max_blocks * p.page_size)
+    else if ((int64_t)s > (int64_t)a.max_blocks * a.page_size)
         bad = CPSA_DEV_SEQ_GT_TABLE;
     if (blockIdx.x == 0 && lane == 0) {
         if (bad)
-            set_dev_error(p.dev_err, bad);
-        if (p.split_clamped)
-            set_dev_error(p.dev_err, CPSA_DEV_SPLITS_CLAMPED);
+            set_dev_error(a.dev_err, bad);
+        if (a.split_clamped)
+            set_dev_error(a.dev_err, CPSA_DEV_SPLITS_CLAMPED);
     }
     if (bad || q < 2)
         return 0;
     const int hist = s - q;
-    const int pairs = p.group / NQ;
-    const int upq = p.num_kv_heads * pairs;      // units per query tile
+    const int pairs = a.group / NQ;
+    const int upq = a.num_kv_heads * pairs;      // units per query tile
     const int nqt = (q + kTileM - 1) / kTileM;
     const int hb = (hist + kTileN - 1) / kTileN;
-    const int nkv_last = p.fused ? hb + nqt : (hist + q + kTileN - 1) / kTileN;
+    const int nkv_last = a.fused ? hb + nqt : (hist + q + kTileN - 1) / kTileN;
     const long long W = (long long)upq * (nkv_last + (long long)(nqt - 1) * (hb + nqt) - (long long)(nqt - 1) * nqt / 2);
     const int shortest = nqt == 1 ? nkv_last : hb + 1;
     const long long grid = gridDim.x;
     const long long run = max((W + grid - 1) / grid, (long long)kMinRunTiles);
-    const bool cut = p.split_ok && !(shortest >= run && nkv_last <= run + kCutCostTiles);
+    const bool cut = a.split_ok && !(shortest >= run && nkv_last <= run + kCutCostTiles);
     int n = W + run < 0x7fffffffll
-                ? self_plan_walk<NQ, int>(p, items, lane, nqt, hb, nkv_last, upq, pairs, (int)run, cut)
-                : self_plan_walk<NQ, long long>(p, items, lane, nqt, hb, nkv_last, upq, pairs, run, cut);
+                ? self_plan_walk<NQ, int>(items, lane, nqt, hb, nkv_last, upq, pairs, (int)run, cut)
+                : self_plan_walk<NQ, long long>(items, lane, nqt, hb, nkv_last, upq, pairs, run, cut);
     if (n > kSelfPlanCap) {
         if (lane == 0)
-            set_dev_error(p.dev_err, CPSA_DEV_PLAN_OVERFLOW);
+            set_dev_error(a.dev_err, CPSA_DEV_PLAN_OVERFLOW);
         n = kSelfPlanCap;
     }
     return n;
@@ -513,9 +532,15 @@ chunk_attn_kernel(const ChunkParams p, const __grid_constant__ CUtensorMap tm_q,
     pdl_wait();
     PrefillItem *s_items = reinterpret_cast<PrefillItem *>(smem + C::kItemOff);
     if (SELF) {
-        // a batch of one prefill request: this CTA computes its own run
+        // a batch of one prefill request: this CTA computes its own run; meanwhile
+        // the producer pulls the start of the request's block_table row into L2
+        // (up to 32 lines, within the row), which its first lookups read next
+        if (warp == C::kLoadWarp && lane * 32 < p.max_blocks)
+            asm volatile("prefetch.global.L2 [%0];" ::"l"(p.block_table + lane * 32));
         if (warp == C::kWriteWarp) {
-            const int n = self_plan_run<NQ>(p, s_items, lane);
+            const SelfPlanArgs a{p.query_lens, p.seq_lens, p.dev_err, p.num_tokens, p.max_blocks, p.page_size,
+                                 p.group, p.num_kv_heads, p.fused, p.split_ok, p.split_clamped};
+            const int n = self_plan_run<NQ>(a, s_items, lane);
             if (lane == 0) {
                 bars->it_begin = 0;
                 bars->it_end = n;
@@ -1003,7 +1028,20 @@ chunk_attn_kernel(const ChunkParams p, const __grid_constant__ CUtensorMap tm_q,
                 unsigned long long *cnt = p.flags + ((int64_t)w.aux * NQ + wg) * 4 + sub;
                 uint4 *ph = reinterpret_cast<uint4 *>(p.part_o) + (int64_t)w.pbase * (D / 4);
                 float2 *pml = reinterpret_cast<float2 *>(p.part_ml) + w.pbase;
-                int seen = lane == 0 && it + 1 == it_end ? epoch_count(ld_acquire_gpu_u64(cnt), p.epoch) : 0;
+                // lane 0 reads the counter now: at the run's last item to see whether the
+                // other pieces are all in (acquire: their partials are read next),
+                // otherwise only as the guess for counting in (relaxed: an acquire
+                // would hold this lane's partial stores back until it returns)
+                unsigned long long cur = 0;
+                int seen = 0;
+                if (lane == 0) {
+                    if (it + 1 == it_end) {
+                        cur = ld_acquire_gpu_u64(cnt);
+                        seen = epoch_count(cur, p.epoch);
+                    } else {
+                        cur = ld_relaxed_gpu_u64(cnt);
+                    }
+                }
                 seen = __shfl_sync(0xffffffffu, seen, 0);
                 bool merge = seen == npieces - 1;
                 if (!merge) {
@@ -1026,7 +1064,7 @@ chunk_attn_kernel(const ChunkParams p, const __grid_constant__ CUtensorMap tm_q,
                     __syncwarp();
                     if (lane == 0) {
                         fence_acq_rel_gpu();   // this warp's partial, then the count
-                        seen = epoch_arrive(cnt, p.epoch, p.dev_err);
+                        seen = epoch_arrive(cnt, p.epoch, cur, p.dev_err);
                         fence_acq_rel_gpu();   // the count, then the other partials
                     }
                     seen = __shfl_sync(0xffffffffu, seen, 0);
