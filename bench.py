@@ -840,9 +840,10 @@ def main():
                 "last_chunk_ms": round(float(km[:, -1].mean()), 4),
                 "per_chunk_ms": [round(float(x), 4) for x in km.mean(axis=0)],
                 "last_chunk_tflops": round(chunk_flops((N_CHUNKS - 1) * CHUNK, CHUNK) / (km[:, -1].mean() * 1e-3) / 1e12, 2)}
-    # per chunk: split, [KV write,] plan, chunk attention (a single prefill
-    # request launches neither the decode nor the combine kernel)
-    launches = args.steps * N_CHUNKS * (3 if wl.fused else 4)
+    # per chunk: split, [KV write,] chunk attention (a single prefill request of
+    # 512 tokens plans its runs inside the chunk kernel and launches neither the
+    # decode nor the combine kernel)
+    launches = args.steps * N_CHUNKS * (2 if wl.fused else 3)
 
     # the other variant of the step (two calls, or the fused call) on the same inputs
     other = {}
