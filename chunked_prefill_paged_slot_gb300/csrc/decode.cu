@@ -523,8 +523,15 @@ decode_group_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap tm
         const uint32_t box_bytes = (uint32_t)HG * RB * D * 2;
         uint32_t g = 0, patch_uses = 0;
         bool stop = false;
+        // the next item's descriptor is read one item ahead (its page lookups
+        // depend on it, and they start the item's stream)
+        DecodeItem w_next{};
+        if (blockIdx.x < n_items)
+            w_next = p.ditems[blockIdx.x];
         for (int it = blockIdx.x; it < n_items && !stop && !*abort; it += gridDim.x) {
-            const DecodeItem w = p.ditems[it];
+            const DecodeItem w = w_next;
+            if (it + (int)gridDim.x < n_items)
+                w_next = p.ditems[it + gridDim.x];
             const int32_t *bt_row = p.block_table + (int64_t)w.r * p.max_blocks;
             const int head0 = w.kvh * HG;
             // the row's own key, when this item's range ends with it and the KV write is fused

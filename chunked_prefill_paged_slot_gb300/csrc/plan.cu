@@ -83,10 +83,10 @@ __device__ int shortest_unit(const PlanParams &p, const Req &rq)
     return unit_tiles(p, rq, 0, min(kTileM, rq.q));
 }
 
-__device__ int decode_splits(const Req &rq, int max_splits)
+__device__ int decode_splits(const Req &rq, int max_splits, int dec_heads)
 {
     const int nch = ceil_div(rq.s, kDecodeChunk);
-    int ns = ceil_div(rq.s, kDecodeKeysPerSplit);
+    int ns = ceil_div(rq.s, dec_heads > 1 ? kDecodeKeysPerSplitGrouped : kDecodeKeysPerSplit);
     ns = min(ns, max_splits);
     ns = min(ns, nch);
     return max(ns, 1);
@@ -124,7 +124,7 @@ __device__ Counts request_work(const PlanParams &p, int r, const Req &rq, int ti
     if (!rq.valid || rq.q == 0)
         return c;
     if (rq.q == 1) {
-        const int ns = decode_splits(rq, max_splits);
+        const int ns = decode_splits(rq, max_splits, p.dec_heads);
         const int nch = ceil_div(rq.s, kDecodeChunk);
         const int ngroups = p.Hkv / p.dec_heads;   // decode items per split
         c.ditems = ngroups * ns;
@@ -352,7 +352,7 @@ __global__ void __launch_bounds__(kPlanThreads, 1) plan_kernel(PlanParams p)
             longest = max(longest, longest_unit(p, rq));
             shortest = min(shortest, shortest_unit(p, rq));
             if (rq.valid && rq.q == 1) {
-                const int ns = decode_splits(rq, p.max_splits);
+                const int ns = decode_splits(rq, p.max_splits, p.dec_heads);
                 if (ns > 1) dprows += (long long)p.Hq * ns;
             }
         }
@@ -475,7 +475,7 @@ __global__ void __launch_bounds__(32, 1) plan_small_kernel(PlanParams p)
     int shortest = mine ? shortest_unit(p, rq) : 0x7fffffff;
     int dprows = 0;
     if (mine && rq.valid && rq.q == 1) {
-        const int ns = decode_splits(rq, p.max_splits);
+        const int ns = decode_splits(rq, p.max_splits, p.dec_heads);
         if (ns > 1) dprows = p.Hq * ns;
     }
     // totals in 64 bits first: the 32-bit scans below are only used once they fit

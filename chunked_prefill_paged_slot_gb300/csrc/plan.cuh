@@ -27,7 +27,8 @@ namespace cpsa {
 // kernel; a unit cut by a run boundary becomes several pieces, merged inside the
 // chunk kernel by whichever piece finishes last (a counter per unit and q head;
 // no CTA waits for another). Every CTA gets the same amount of work.
-// Decode: a row splits into pieces of kDecodeKeysPerSplit keys (at most
+// Decode: a row splits into pieces of kDecodeKeysPerSplit keys (grouped items:
+// kDecodeKeysPerSplitGrouped) (at most
 // max_kv_splits), depending only on its own length.
 // KV tiles of a unit: tile kt holds keys [128 kt, 128 kt + 128). With the KV
 // write fused, the history (keys below h) keeps that grid, its last tile cut at
@@ -40,6 +41,10 @@ constexpr int kCutCostTiles = 6;            // a run's extra item and merge when
 constexpr int kMaxChunkGrid = 256;          // upper bound of the chunk kernel's grid (SMs)
 constexpr int kDecodeChunk = 64;            // keys per decode pipeline stage
 constexpr int kDecodeKeysPerSplit = 4096;   // keys per decode split (multiple of kDecodeChunk)
+// Grouped decode items carry all heads of a group, a quarter to an eighth of the
+// per-head items' count: they split every 1024 keys so that small decode batches
+// still occupy the GPU (still a function of the row's own length only).
+constexpr int kDecodeKeysPerSplitGrouped = 1024;
 constexpr int kMaxSplitUnits = kMaxChunkGrid;   // a split unit holds a run boundary: at most grid - 1
 constexpr int kMergeCounters = 2 * 4;          // per split unit: q heads (<= 2) x 4 softmax warps
 // A batch of one prefill request skips the plan kernel: every chunk-kernel CTA
