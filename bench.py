@@ -727,6 +727,10 @@ def main():
                     help="only the mixed decode step with 128 decode rows (about 2.5 GB of cache), timed with "
                          "CUDA events; an ncu --set full capture of this case once ended in a GPU fault (see the "
                          "design notes on measurement) and is not to be repeated")
+    ap.add_argument("--eager", action="store_true",
+                    help="time the step as stream launches (default: one step, all 64 chunks and the side-stream "
+                         "splits, captured once in a CUDA graph and replayed; the stream-launch step is then "
+                         "timed beside it as eager_step)")
     ap.add_argument("--profile-kv-write", action="store_true",
                     help="only the KV-write bandwidth measurement (T = 512 at page 128, T = 166528 at page 16)")
     args = ap.parse_args()
@@ -774,6 +778,21 @@ def main():
         gpu_uuid = gpu_uuid if gpu_uuid.startswith("GPU-") else "GPU-" + gpu_uuid
     except Exception:
         pass
+    eager_step = lambda: wl.step(stream)
+    run_step = eager_step
+    if not args.eager:
+        # the same step, captured once: the library's calls launch from the capture
+        graph = torch.cuda.CUDAGraph()
+        capture = torch.cuda.Stream(device=dev)   # a capture needs a stream of its own
+        with torch.cuda.graph(graph, stream=capture):
+            wl.step(capture)
+        torch.cuda.synchronize()
+        run_step = graph.replay
+        for _ in range(max(3, args.warmup)):
+            run_step()
+        torch.cuda.synchronize()
+        if cpsa.cpp_read_device_error(wl.err) != 0:
+            raise SystemExit("device error flags set during graph warm-up")
     clocks = ClockSampler(gpu_uuid)
     ev0 = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
     ev1 = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
@@ -786,7 +805,7 @@ def main():
         flush.zero_()
         ev0[s].record(stream)
         te = time.perf_counter()
-        wl.step(stream)
+        run_step()
         enqueue_s.append(time.perf_counter() - te)
         ev1[s].record(stream)
         torch.cuda.synchronize()
@@ -845,6 +864,22 @@ def main():
     # decode nor the combine kernel)
     launches = args.steps * N_CHUNKS * (2 if wl.fused else 3)
 
+    # the same step as stream launches, beside the graph replays
+    eager = {}
+    if rank == 0 and not args.eager and not args.no_compare:
+        ems = []
+        o0, o1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        for _ in range(10):
+            flush.zero_()
+            o0.record(stream)
+            eager_step()
+            o1.record(stream)
+            torch.cuda.synchronize()
+            ems.append(o0.elapsed_time(o1))
+        e_ms = float(np.mean(ems))
+        eager = {"ms_per_step": round(e_ms, 4), "value": round(STEP_FLOPS / (e_ms * 1e-3) / 1e12, 3),
+                 "device_flags": cpsa.cpp_read_device_error(wl.err)}
+
     # the other variant of the step (two calls, or the fused call) on the same inputs
     other = {}
     if rank == 0 and not args.no_compare:
@@ -873,6 +908,7 @@ def main():
             "data": "synthetic (seeded N(0,1) bf16 q/k/v, permuted page pool)",
             "config": {"workload": WORKLOAD, "global_batch": world, "seq_len": SEQ, "chunk": CHUNK,
                        "kv_write": "fused into the attention call" if wl.fused else "separate call",
+                       "launch": "stream launches" if args.eager else "one CUDA graph per step (replayed)",
                        "parallelism": "replicas" if world > 1 else "single-gpu",
                        "l2": "flushed between steps (256 MB write)", "max_kv_splits": wl.max_kv_splits,
                        "step_flops": STEP_FLOPS},
@@ -883,6 +919,8 @@ def main():
             "step_roofline": step_roofline(ms_per_step, peak_tf, peak_bw),
             "wall_s": round(wall, 3), "host_enqueue_ms_per_step": round(1e3 * float(np.mean(enqueue_s)), 3),
             "device_flags": flags}
+    if eager:
+        line["eager_step"] = eager
     if other:
         line["fused_step" if not wl.fused else "two_call_step"] = other
     if not args.no_secondary and rank == 0:
@@ -943,6 +981,9 @@ def summary_of(line):
     if "tile_alignment_h8192" in su:
         out["tile_alignment_h8192_ms"] = su["tile_alignment_h8192"]
     out["headline_tflops"] = line.get("value")
+    out["headline_launch"] = line.get("config", {}).get("launch")
+    if "eager_step" in line:
+        out["eager_step_tflops"] = line["eager_step"]["value"]
     out["roofline_frac"] = line.get("roofline", {}).get("frac")
     return out
 

@@ -3,6 +3,7 @@
 // commit) and bounded waits that give up with an error flag instead of hanging.
 #pragma once
 
+#include <atomic>
 #include <utility>
 
 #include <cuda.h>
@@ -310,6 +311,36 @@ inline cudaError_t launch_pdl(bool early, void (*kernel)(KArgs...), dim3 grid, d
     cfg.attrs = attr;
     cfg.numAttrs = early ? 1 : 0;
     return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
+}
+
+// Dynamic shared memory beyond 48 KB needs a function attribute. It is set the
+// first time a kernel launches on a device (one bit per device ordinal in
+// `done`, a static of the kernel's own launcher) rather than at every launch:
+// the call costs host time and is not a stream operation one wants inside a
+// graph capture. A context rebuilt after cudaDeviceReset forgets the attribute:
+// a launch that then fails is retried once with the attribute set again.
+template <typename Launch>
+inline cudaError_t launch_with_smem(std::atomic<uint64_t> &done, const void *kernel, int smem_bytes, Launch launch)
+{
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess)
+        return cudaErrorInvalidDevice;
+    const uint64_t bit = (dev >= 0 && dev < 64) ? (1ull << dev) : 0ull;
+    for (int attempt = 0; attempt < 2; ++attempt) {
+        if (!bit || !(done.load(std::memory_order_acquire) & bit)) {
+            cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_bytes);
+            if (e != cudaSuccess)
+                return e;
+            if (bit)
+                done.fetch_or(bit, std::memory_order_acq_rel);
+        }
+        cudaError_t e = launch();
+        if (e == cudaSuccess || attempt == 1 || !bit)
+            return e;
+        (void)cudaGetLastError();   // the launch was refused (nothing ran): set the attribute and retry
+        done.fetch_and(~bit, std::memory_order_acq_rel);
+    }
+    return cudaErrorUnknown;
 }
 
 // One lane of a converged warp, chosen by elect.sync. A tcgen05.mma or commit is

@@ -430,11 +430,11 @@ cudaError_t launch_decode_t(const DecodeParams &p, const CUtensorMap &tk, const 
                             cudaStream_t s, bool early)
 {
     using C = DecCfg<D, HI>;
+    static std::atomic<uint64_t> done{0};
     auto k = decode_attn_kernel<D, HI>;
-    cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
-    if (e != cudaSuccess)
-        return e;
-    return launch_pdl(early, k, dim3(grid), dim3(C::kThreads), C::kSmemBytes, s, p, tk, tv);
+    return launch_with_smem(done, reinterpret_cast<const void *>(k), C::kSmemBytes, [&] {
+        return launch_pdl(early, k, dim3(grid), dim3(C::kThreads), C::kSmemBytes, s, p, tk, tv);
+    });
 }
 
 
@@ -792,11 +792,11 @@ cudaError_t launch_decode_group_t(const DecodeParams &p, const CUtensorMap &tk, 
                                   cudaStream_t s, bool early)
 {
     using C = GDecCfg<D, HG>;
+    static std::atomic<uint64_t> done{0};
     auto k = decode_group_kernel<D, HG, HI>;
-    cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
-    if (e != cudaSuccess)
-        return e;
-    return launch_pdl(early, k, dim3(grid), dim3(C::kThreads), C::kSmemBytes, s, p, tk, tv);
+    return launch_with_smem(done, reinterpret_cast<const void *>(k), C::kSmemBytes, [&] {
+        return launch_pdl(early, k, dim3(grid), dim3(C::kThreads), C::kSmemBytes, s, p, tk, tv);
+    });
 }
 
 template <int HG>

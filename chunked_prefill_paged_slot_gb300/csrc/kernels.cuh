@@ -38,9 +38,10 @@ struct ChunkParams : AttnCommon {
     const PrefillItem *pitems;
     const int32_t *run_first;   // CTA c processes pieces [run_first[c], run_first[c + 1])
     // Merge counters, per split unit, q head and softmax warp: the pieces of the
-    // unit done in this call, tagged with the call's epoch in the high 32 bits
-    // (a count left by an earlier call carries another epoch and reads as zero,
-    // so nothing has to clear the counters between calls).
+    // unit done in this call, tagged with the call's epoch in the high 32 bits.
+    // The warp that merges a unit clears its counter; a count that an earlier
+    // call left (it ended early) carries another epoch and reads as zero, so
+    // nothing has to clear the counters between calls.
     unsigned long long *flags;
     uint32_t epoch;             // nonzero, different for every call of the library
     // A batch of one prefill request (self_plan != 0): no plan kernel ran; every

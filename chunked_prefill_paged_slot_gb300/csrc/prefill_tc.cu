@@ -97,7 +97,9 @@ struct ChunkBars {
 static_assert(sizeof(ChunkBars) <= 256, "the self-planned pieces follow the barriers at +256");
 static_assert(sizeof(PrefillItem) == 32, "piece size");
 
-// Merge counters carry the call's epoch in their high 32 bits (see ChunkParams).
+// Merge counters carry the call's epoch in their high 32 bits (see ChunkParams)
+// and are cleared by the warp that merges, so a counter holds another call's
+// count only after a call that ended early (a device error).
 __device__ __forceinline__ unsigned long long ld_acquire_gpu_u64(const unsigned long long *p)
 {
     unsigned long long v;
@@ -1087,6 +1089,12 @@ chunk_attn_kernel(const ChunkParams p, const __grid_constant__ CUtensorMap tm_q,
                         merge_split_row_any<D, NQ>(p, tO, pml, ph, piece, npieces, wg, row, m_use, l, valid_row,
                                                    out_off);
                     }
+                    // Every other piece has counted in, so no one else touches the
+                    // counter in this call: the merging warp clears it. A later call
+                    // then finds it clear even under the same epoch (a call captured
+                    // in a CUDA graph replays its epoch).
+                    if (lane == 0)
+                        *reinterpret_cast<volatile unsigned long long *>(cnt) = 0ull;
                 }
             } else {
                 const float inv_l = l > 0.f ? 1.f / l : 0.f;
@@ -1129,11 +1137,13 @@ cudaError_t launch_chunk_t(const ChunkParams &p, const CUtensorMap &tq, const CU
                            cudaStream_t s, bool early)
 {
     using C = ChunkCfg<D, NQ>;
+    static std::atomic<uint64_t> done_self{0}, done_plan{0};
     auto k = p.self_plan ? chunk_attn_kernel<D, NQ, true> : chunk_attn_kernel<D, NQ, false>;
-    cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
-    if (e != cudaSuccess)
-        return e;
-    return launch_pdl(early, k, dim3(grid), dim3(C::kThreads), C::kSmemBytes, s, p, tq, tk, tv, tkn, tvn);
+    return launch_with_smem(p.self_plan ? done_self : done_plan, reinterpret_cast<const void *>(k), C::kSmemBytes,
+                            [&] {
+                                return launch_pdl(early, k, dim3(grid), dim3(C::kThreads), C::kSmemBytes, s, p, tq,
+                                                  tk, tv, tkn, tvn);
+                            });
 }
 
 }  // namespace

@@ -139,9 +139,15 @@ size_t cpp_attn_workspace_min_bytes(int num_reqs, int64_t num_tokens, int num_q_
  * kernel alone: its CTAs compute their own runs, with the same units and cuts.
  * workspace: device memory of at least cpp_attn_workspace_min_bytes(...) with
  * the same (num_reqs, num_tokens, heads, head_dim, max_kv_splits); it is
- * scratch, overwritten by each call; calls that share it must be stream-ordered
- * (each call tags the merge counters it leaves there with its own epoch, so no
- * call needs the workspace cleared).
+ * scratch, overwritten by each call; calls that share it must be stream-ordered.
+ * No call needs the workspace cleared: the merge counters a call uses are
+ * cleared by the call itself as each split unit is merged, and are tagged with
+ * the call's epoch (a per-call number) so that counts left by a call that ended
+ * with a device error read as zero in the next call.
+ * CUDA graphs: the call may be captured on `stream` and replayed; a replay
+ * keeps the sizes, pointers and epoch of the capture and reads the current
+ * contents of the buffers. After a replay that reported a device error, clear
+ * the workspace (or call once outside the graph) before the next replay.
  */
 int cpp_chunked_prefill_attn(const void *q, const void *k_cache, const void *v_cache,
                              const int32_t *query_lens, const int32_t *seq_lens,
