@@ -475,9 +475,19 @@ int attn_impl(const void *q, const void *k_new, const void *v_new, const int64_t
     const bool partials_fit = cap >= (int64_t)2 * pp.chunk_grid * kTileM * nq;
     cp.split_ok = max_kv_splits > 1 && partials_fit ? 1 : 0;
     cp.split_clamped = max_kv_splits > 1 && !partials_fit ? 1 : 0;
+    // out, [T][Hq][D], in boxes of 64 columns x 1 head x 32 rows: the chunk
+    // kernel's TMA-store epilogue (head_dim 128 without the KV write, whose cache
+    // writer holds the staging buffer); without the map the rows are stored directly
+    CUtensorMap to = tq;
+    cp.out_tma = !fused && head_dim == 128 && aligned16(out) &&
+                         make_map(&to, out, D, (uint64_t)num_q_heads, (uint64_t)num_tokens, D * 2,
+                                  D * 2 * num_q_heads, 64, 1, 32)
+                     ? 1
+                     : 0;
     const int grid_c = single_decode ? 0 : pp.chunk_grid;   // one stream-K run per CTA
     if (grid_c > 0 &&
-        launch_chunk_attn(cp, tq, tk, tv, tkn, tvn, head_dim, nq, grid_c, s, early && !self_plan) != cudaSuccess)
+        launch_chunk_attn(cp, tq, tk, tv, tkn, tvn, to, head_dim, nq, grid_c, s, early && !self_plan) !=
+            cudaSuccess)
         return CPSA_ERR_CUDA;
     mark(2, s);
 

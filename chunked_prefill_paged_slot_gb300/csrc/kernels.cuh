@@ -50,6 +50,7 @@ struct ChunkParams : AttnCommon {
     int num_tokens;             // for the self-planned batch's token check
     int split_ok;               // self-planned batch: units may be cut (splits allowed and the partials fit)
     int split_clamped;          // self-planned batch: splits were asked for but the partials do not fit
+    int out_tma;                // head_dim 128 without the KV write: whole units' rows leave by TMA stores
 };
 
 struct DecodeParams : AttnCommon {
@@ -70,9 +71,10 @@ struct CombineParams {
 
 // early: launch with programmatic dependent launch (see launch_pdl)
 // tkn / tvn: maps over k_new / v_new (used when p.fused)
+// to: map over out, boxes of 64 columns x 1 head x 32 rows (used when p.out_tma)
 cudaError_t launch_chunk_attn(const ChunkParams &p, const CUtensorMap &tq, const CUtensorMap &tk,
-                              const CUtensorMap &tv, const CUtensorMap &tkn, const CUtensorMap &tvn, int head_dim,
-                              int nq, int grid, cudaStream_t s, bool early);
+                              const CUtensorMap &tv, const CUtensorMap &tkn, const CUtensorMap &tvn,
+                              const CUtensorMap &to, int head_dim, int nq, int grid, cudaStream_t s, bool early);
 cudaError_t launch_decode_attn(const DecodeParams &p, const CUtensorMap &tk, const CUtensorMap &tv, int head_dim,
                                int grid, cudaStream_t s, bool early);
 // the grouped decode kernel: items of heads_per_item (4 or 8) kv heads; tk / tv

@@ -490,7 +490,8 @@ template <int D, int NQ, bool SELF>
 __global__ void __launch_bounds__(352, 1)
 chunk_attn_kernel(const ChunkParams p, const __grid_constant__ CUtensorMap tm_q,
                   const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
-                  const __grid_constant__ CUtensorMap tm_kn, const __grid_constant__ CUtensorMap tm_vn)
+                  const __grid_constant__ CUtensorMap tm_kn, const __grid_constant__ CUtensorMap tm_vn,
+                  const __grid_constant__ CUtensorMap tm_o)
 {
     using C = ChunkCfg<D, NQ>;
     extern __shared__ uint8_t smem_raw[];
@@ -521,6 +522,8 @@ chunk_attn_kernel(const ChunkParams p, const __grid_constant__ CUtensorMap tm_q,
         tma_prefetch_desc(&tm_q);
         tma_prefetch_desc(&tm_k);
         tma_prefetch_desc(&tm_v);
+        if (!SELF && D == 128 && p.out_tma && !p.fused)
+            tma_prefetch_desc(&tm_o);
         if (p.fused) {
             tma_prefetch_desc(&tm_kn);
             tma_prefetch_desc(&tm_vn);
@@ -1096,6 +1099,62 @@ chunk_attn_kernel(const ChunkParams p, const __grid_constant__ CUtensorMap tm_q,
                     if (lane == 0)
                         *reinterpret_cast<volatile unsigned long long *>(cnt) = 0ull;
                 }
+            } else if constexpr (!SELF && D == 128) {
+                // A whole unit of a planned batch. Without the KV write (whose cache
+                // writer holds the buffer) each warp stages its 32 rows, 64 columns
+                // at a time, in its own 4 KB of the writer's buffer and a TMA store
+                // writes them out, so the warp moves on to the next unit while the
+                // rows go to memory; a warp with rows past the request's end (the
+                // last query tile), or any warp of a call with the KV write, stores
+                // its valid rows directly. (Planned batches hold many units per
+                // run; the self-planned kernel, with few, stores directly: staging
+                // measured slower there.)
+                const float inv_l = l > 0.f ? 1.f / l : 0.f;
+                const bool staged = p.out_tma && !p.fused && __all_sync(0xffffffffu, valid_row);
+                uint8_t *stg = smem + C::kStageOff + (wg * 4 + sub) * 4096;
+#pragma unroll
+                for (int c2 = 0; c2 < D / 64; ++c2) {
+                    if (staged) {
+                        if (lane == 0)
+                            bulk_wait_group_read0();   // the warp's previous store has read the buffer
+                        __syncwarp();
+                    }
+#pragma unroll
+                    for (int cc = 0; cc < 2; ++cc) {
+                        const int c = 2 * c2 + cc;
+                        uint32_t r[32];
+                        tmem_ld32(tO + c * 32, r);
+                        tmem_wait_ld();
+                        uint4 v[4];
+#pragma unroll
+                        for (int x = 0; x < 4; ++x)
+                            v[x] = make_uint4(pack_bf16x2(__uint_as_float(r[8 * x + 0]) * inv_l, __uint_as_float(r[8 * x + 1]) * inv_l),
+                                              pack_bf16x2(__uint_as_float(r[8 * x + 2]) * inv_l, __uint_as_float(r[8 * x + 3]) * inv_l),
+                                              pack_bf16x2(__uint_as_float(r[8 * x + 4]) * inv_l, __uint_as_float(r[8 * x + 5]) * inv_l),
+                                              pack_bf16x2(__uint_as_float(r[8 * x + 6]) * inv_l, __uint_as_float(r[8 * x + 7]) * inv_l));
+                        if (staged) {
+                            // row `lane` at lane * 128 bytes, 16-byte chunk j at (j ^ (lane & 7)):
+                            // the map's 128-byte swizzle
+#pragma unroll
+                            for (int x = 0; x < 4; ++x)
+                                *reinterpret_cast<uint4 *>(stg + lane * 128 + (((cc * 4 + x) ^ (lane & 7)) << 4)) = v[x];
+                        } else if (valid_row) {
+                            uint4 *dst = reinterpret_cast<uint4 *>(
+                                reinterpret_cast<__nv_bfloat16 *>(p.out) + (t_row * p.num_q_heads + h) * D + c * 32);
+#pragma unroll
+                            for (int x = 0; x < 4; ++x)
+                                dst[x] = v[x];
+                        }
+                    }
+                    if (staged) {
+                        fence_proxy_async_smem();
+                        __syncwarp();
+                        if (lane == 0) {
+                            tma_store_3d(&tm_o, stg, c2 * 64, h, (int)(t_row - lane));
+                            bulk_commit_group();
+                        }
+                    }
+                }
             } else {
                 const float inv_l = l > 0.f ? 1.f / l : 0.f;
 #pragma unroll
@@ -1118,6 +1177,9 @@ chunk_attn_kernel(const ChunkParams p, const __grid_constant__ CUtensorMap tm_q,
         }
     }
 
+    // the softmax warps' output stores are complete before the CTA ends
+    if (!SELF && D == 128 && warp / 4 < NQ && lane == 0 && p.out_tma && !p.fused)
+        bulk_wait_group0();
     if (threadIdx.x == 0 && bars->abort)
         set_dev_error(p.dev_err, CPSA_DEV_WAIT_TIMEOUT);
     // The next kernels are released only as CTAs finish: launched at the start
@@ -1133,8 +1195,8 @@ chunk_attn_kernel(const ChunkParams p, const __grid_constant__ CUtensorMap tm_q,
 
 template <int D, int NQ>
 cudaError_t launch_chunk_t(const ChunkParams &p, const CUtensorMap &tq, const CUtensorMap &tk,
-                           const CUtensorMap &tv, const CUtensorMap &tkn, const CUtensorMap &tvn, int grid,
-                           cudaStream_t s, bool early)
+                           const CUtensorMap &tv, const CUtensorMap &tkn, const CUtensorMap &tvn,
+                           const CUtensorMap &to, int grid, cudaStream_t s, bool early)
 {
     using C = ChunkCfg<D, NQ>;
     static std::atomic<uint64_t> done_self{0}, done_plan{0};
@@ -1142,21 +1204,21 @@ cudaError_t launch_chunk_t(const ChunkParams &p, const CUtensorMap &tq, const CU
     return launch_with_smem(p.self_plan ? done_self : done_plan, reinterpret_cast<const void *>(k), C::kSmemBytes,
                             [&] {
                                 return launch_pdl(early, k, dim3(grid), dim3(C::kThreads), C::kSmemBytes, s, p, tq,
-                                                  tk, tv, tkn, tvn);
+                                                  tk, tv, tkn, tvn, to);
                             });
 }
 
 }  // namespace
 
 cudaError_t launch_chunk_attn(const ChunkParams &p, const CUtensorMap &tq, const CUtensorMap &tk,
-                              const CUtensorMap &tv, const CUtensorMap &tkn, const CUtensorMap &tvn, int head_dim,
-                              int nq, int grid, cudaStream_t s, bool early)
+                              const CUtensorMap &tv, const CUtensorMap &tkn, const CUtensorMap &tvn,
+                              const CUtensorMap &to, int head_dim, int nq, int grid, cudaStream_t s, bool early)
 {
     if (head_dim == 128)
-        return nq == 2 ? launch_chunk_t<128, 2>(p, tq, tk, tv, tkn, tvn, grid, s, early)
-                       : launch_chunk_t<128, 1>(p, tq, tk, tv, tkn, tvn, grid, s, early);
-    return nq == 2 ? launch_chunk_t<64, 2>(p, tq, tk, tv, tkn, tvn, grid, s, early)
-                   : launch_chunk_t<64, 1>(p, tq, tk, tv, tkn, tvn, grid, s, early);
+        return nq == 2 ? launch_chunk_t<128, 2>(p, tq, tk, tv, tkn, tvn, to, grid, s, early)
+                       : launch_chunk_t<128, 1>(p, tq, tk, tv, tkn, tvn, to, grid, s, early);
+    return nq == 2 ? launch_chunk_t<64, 2>(p, tq, tk, tv, tkn, tvn, to, grid, s, early)
+                   : launch_chunk_t<64, 1>(p, tq, tk, tv, tkn, tvn, to, grid, s, early);
 }
 
 }  // namespace cpsa
