@@ -926,26 +926,28 @@ chunk_attn_kernel(const ChunkParams p, const __grid_constant__ CUtensorMap tm_q,
                 tc_fence_after_sync();
                 // the S row straight from TMEM: four loads, one wait
                 uint32_t sr[4][32];
+                float rm[4];
 #pragma unroll
-                for (int c = 0; c < 4; ++c) tmem_ld32(tS + c * 32, sr[c]);
+                for (int c = 0; c < 4; ++c) tmem_ld32_max(tS + c * 32, sr[c], rm[c]);
                 tmem_wait_ld();
 #define SV(x) __uint_as_float(sr[(x) >> 5][(x) & 31])
                 // causal / tail mask: only tiles that reach past some row's last key
                 const bool masked = __any_sync(0xffffffffu, key0 + 127 > lim);
+                float mx = fmaxf(fmaxf(rm[0], rm[1]), fmaxf(rm[2], rm[3]));
                 if (masked) {
 #pragma unroll
                     for (int x = 0; x < 128; ++x)
                         if (key0 + x > lim) sr[x >> 5][x & 31] = 0xff800000u;   // -inf
+                    // row max as 4 independent fmax3 chains joined at the end (short latency)
+                    float mc[4];
+#pragma unroll
+                    for (int c = 0; c < 4; ++c) mc[c] = fmaxf(SV(c), SV(c + 4));
+#pragma unroll
+                    for (int x = 8; x < 128; x += 8)
+#pragma unroll
+                        for (int c = 0; c < 4; ++c) mc[c] = fmax3(mc[c], SV(x + c), SV(x + 4 + c));
+                    mx = fmaxf(fmaxf(mc[0], mc[1]), fmaxf(mc[2], mc[3]));
                 }
-                // row max as 4 independent fmax3 chains joined at the end (short latency)
-                float mc[4];
-#pragma unroll
-                for (int c = 0; c < 4; ++c) mc[c] = fmaxf(SV(c), SV(c + 4));
-#pragma unroll
-                for (int x = 8; x < 128; x += 8)
-#pragma unroll
-                    for (int c = 0; c < 4; ++c) mc[c] = fmax3(mc[c], SV(x + c), SV(x + 4 + c));
-                const float mx = fmaxf(fmaxf(mc[0], mc[1]), fmaxf(mc[2], mc[3]));
                 const float m_tile = mx * sl2;
                 const bool need = m_tile > m_use + 8.f;
                 float alpha = 1.f;
