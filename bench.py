@@ -9,13 +9,17 @@ run on a side stream joined back before the step ends (a one-request batch is
 never split, so no attention call waits for one). The KV
 write runs fused into the attention call (cpp_chunked_prefill_attn_write_kv);
 `--two-call` times the separate write and attention calls instead, and the
-line's `two_call_step` reports that variant on the same inputs.
+line's `two_call_step` reports that variant on the same inputs. The step is
+captured once in a CUDA graph and the graph is replayed for every timed step
+(every kernel runs again on the resident inputs); `--eager` times stream
+launches, and the line's `eager_step` reports them beside the graph.
 
 Prints one JSON line (rank 0). `value` is attention TFLOP/s of the whole step
 (algorithmic FLOPs: 4*d*Hq*sum_i (h + i + 1), unmasked pairs only) with inputs
 resident in HBM; `e2e` is the same metric through the C ABI with host buffers
 (pinned host->device copies of each chunk's q/k/v/slots and the device->host
-read of its output inside the timed region); `roofline` is the chunk kernel's
+read of its output inside the timed region, in the same launch mode, copies
+included in the graph); `roofline` is the chunk kernel's
 own event-timed throughput against the measured bf16 peak; `cpu_baseline` is
 the fp64 oracle on a bounded sample of the same workload on the host cores.
 `--impl reference` times that oracle alone on the workload's own metric.
@@ -821,21 +825,40 @@ def main():
     ms_per_step = total_ms / args.steps
     value = job_tflops(world, STEP_FLOPS, args.steps, total_ms)
 
-    # end-to-end through host buffers
+    # end-to-end through host buffers: the same launch mode as the headline (the
+    # whole host-buffer step, copies included, captured once and replayed), and
+    # the stream-launch variant beside it
     h2d, d2h = wl.make_host()
     for _ in range(2):
         wl.step_e2e(stream)
     torch.cuda.synchronize()
-    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    e2e_ms = []
-    for s in range(max(1, args.steps // 2)):
-        flush.zero_()
-        e0.record(stream)
-        wl.step_e2e(stream)
-        e1.record(stream)
+
+    def time_e2e(fn, reps):
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        ms = []
+        for _ in range(reps):
+            flush.zero_()
+            e0.record(stream)
+            fn()
+            e1.record(stream)
+            torch.cuda.synchronize()
+            ms.append(e0.elapsed_time(e1))
+        return float(np.mean(ms))
+
+    e2e_eager_ms = time_e2e(lambda: wl.step_e2e(stream), max(1, args.steps // 2))
+    e2e_run = None
+    if not args.eager:
+        e2e_graph = torch.cuda.CUDAGraph()
+        capture2 = torch.cuda.Stream(device=dev)
+        with torch.cuda.graph(e2e_graph, stream=capture2):
+            wl.step_e2e(capture2)
         torch.cuda.synchronize()
-        e2e_ms.append(e0.elapsed_time(e1))
-    e2e_step_ms = max_over_ranks(float(np.mean(e2e_ms)), dist, dev)
+        for _ in range(2):
+            e2e_graph.replay()
+        torch.cuda.synchronize()
+        e2e_run = e2e_graph.replay
+    e2e_step_ms = e2e_eager_ms if e2e_run is None else time_e2e(e2e_run, max(1, args.steps // 2))
+    e2e_step_ms = max_over_ranks(e2e_step_ms, dist, dev)
     e2e_val = job_tflops(world, STEP_FLOPS, 1, e2e_step_ms)
 
     # roofline of the dominant kernel (the tensor-core chunk kernel): separate steps
@@ -913,7 +936,9 @@ def main():
                        "l2": "flushed between steps (256 MB write)", "max_kv_splits": wl.max_kv_splits,
                        "step_flops": STEP_FLOPS},
             "e2e": {"value": round(e2e_val, 3), "unit": "TFLOP/s", "h2d_bytes_per_step": h2d,
-                    "d2h_bytes_per_step": d2h, "ms_per_step": round(e2e_step_ms, 4)},
+                    "d2h_bytes_per_step": d2h, "ms_per_step": round(e2e_step_ms, 4),
+                    "launch": "stream launches" if args.eager else "one CUDA graph per step (copies included)",
+                    "stream_launch_ms_per_step": round(e2e_eager_ms, 4)},
             "roofline": roofline, "gpu_launches": launches, "clocks": clk,
             "tokens_per_s": round(world * SEQ / (ms_per_step * 1e-3), 1),
             "step_roofline": step_roofline(ms_per_step, peak_tf, peak_bw),

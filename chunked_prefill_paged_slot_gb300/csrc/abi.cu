@@ -484,9 +484,13 @@ int attn_impl(const void *q, const void *k_new, const void *v_new, const int64_t
                                   D * 2 * num_q_heads, 64, 1, 32)
                      ? 1
                      : 0;
+    // V below page 128: one box per page of one kv head, both column halves
+    CUtensorMap tv4 = tv;
+    if (head_dim == 128 && page_size < 128 && !make_map4_halves(&tv4, v_cache, page_size, rows_kv, page_size))
+        return CPSA_ERR_CUDA;
     const int grid_c = single_decode ? 0 : pp.chunk_grid;   // one stream-K run per CTA
     if (grid_c > 0 &&
-        launch_chunk_attn(cp, tq, tk, tv, tkn, tvn, to, head_dim, nq, grid_c, s, early && !self_plan) !=
+        launch_chunk_attn(cp, tq, tk, tv, tkn, tvn, to, tv4, head_dim, nq, grid_c, s, early && !self_plan) !=
             cudaSuccess)
         return CPSA_ERR_CUDA;
     mark(2, s);

@@ -72,9 +72,12 @@ struct CombineParams {
 // early: launch with programmatic dependent launch (see launch_pdl)
 // tkn / tvn: maps over k_new / v_new (used when p.fused)
 // to: map over out, boxes of 64 columns x 1 head x 32 rows (used when p.out_tma)
+// tv4: 4-D map over v_cache, one box per page with both column halves (used for
+//      head_dim 128 below page 128)
 cudaError_t launch_chunk_attn(const ChunkParams &p, const CUtensorMap &tq, const CUtensorMap &tk,
                               const CUtensorMap &tv, const CUtensorMap &tkn, const CUtensorMap &tvn,
-                              const CUtensorMap &to, int head_dim, int nq, int grid, cudaStream_t s, bool early);
+                              const CUtensorMap &to, const CUtensorMap &tv4, int head_dim, int nq, int grid,
+                              cudaStream_t s, bool early);
 cudaError_t launch_decode_attn(const DecodeParams &p, const CUtensorMap &tk, const CUtensorMap &tv, int head_dim,
                                int grid, cudaStream_t s, bool early);
 // the grouped decode kernel: items of heads_per_item (4 or 8) kv heads; tk / tv

@@ -13,15 +13,20 @@
 //
 // CTA layout (352 threads, one CTA per SM, persistent over prefill items):
 //   warp 8       TMA producer: Q tiles once per item, then K_j, V_j into a ring
-//                of shared-memory slots; block_table lookups; zeroes the value
-//                rows past the tile's last key (they may hold anything).
+//                of shared-memory slots (one box per page and 64-column half;
+//                below page 128 a cache V tile takes one box per page holding
+//                both halves, page-major in the slot); block_table lookups;
+//                zeroes the value rows past the tile's last key (they may hold
+//                anything).
 //   warp 9       tcgen05 issuer (one elected lane per instruction, the warp
 //                converged): S_n = Q_n K_j^T into TMEM, then O_n += P_n V_j with
 //                P_n read from TMEM; TMEM alloc/dealloc.
 //   warps 0..7   softmax, one warpgroup per q head n; thread = query row:
-//                S row from TMEM, causal mask on the diagonal/tail tiles, online
+//                S row from TMEM (the reducing load gives the row max of an
+//                unmasked tile), causal mask on the diagonal/tail tiles, online
 //                max/sum in fp32 (base-2 exponent, scale folded in), P as bf16
-//                back into TMEM over S; final O / l epilogue, or for a piece of
+//                back into TMEM over S; final O / l epilogue (planned batches
+//                without the KV write: staged in shared memory, TMA stores), or for a piece of
 //                a unit cut by the stream-K split, its partial (O / l in bf16,
 //                m and l in fp32) or the merge of all the unit's pieces
 //                (whichever piece finishes last merges; at the end of a run
@@ -491,7 +496,7 @@ __global__ void __launch_bounds__(352, 1)
 chunk_attn_kernel(const ChunkParams p, const __grid_constant__ CUtensorMap tm_q,
                   const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
                   const __grid_constant__ CUtensorMap tm_kn, const __grid_constant__ CUtensorMap tm_vn,
-                  const __grid_constant__ CUtensorMap tm_o)
+                  const __grid_constant__ CUtensorMap tm_o, const __grid_constant__ CUtensorMap tm_v4)
 {
     using C = ChunkCfg<D, NQ>;
     extern __shared__ uint8_t smem_raw[];
@@ -524,6 +529,8 @@ chunk_attn_kernel(const ChunkParams p, const __grid_constant__ CUtensorMap tm_q,
         tma_prefetch_desc(&tm_v);
         if (!SELF && D == 128 && p.out_tma && !p.fused)
             tma_prefetch_desc(&tm_o);
+        if (D == 128 && p.page_size < 128)
+            tma_prefetch_desc(&tm_v4);
         if (p.fused) {
             tma_prefetch_desc(&tm_kn);
             tma_prefetch_desc(&tm_vn);
@@ -571,6 +578,7 @@ chunk_attn_kernel(const ChunkParams p, const __grid_constant__ CUtensorMap tm_q,
         const int PB = p.page_size < 128 ? p.page_size : 128;   // rows per TMA box
         const int NB = 128 / PB;                                 // boxes per tile
         const uint32_t box_bytes = (uint32_t)PB * 128u;
+        const bool v_pages = D == 128 && PB < 128;   // V tiles of the cache in page-major boxes
         uint32_t q_uses = 0, slot_it = 0, tail_uses = 0;
         for (int it = it_begin; it < it_end && !*abort; ++it) {
             const PrefillItem w = items[it];
@@ -650,6 +658,16 @@ chunk_attn_kernel(const ChunkParams p, const __grid_constant__ CUtensorMap tm_q,
                         } else if (issuer) {
                             mbar_arrive(bar);
                         }
+                    } else if (valid && kv == 1 && v_pages) {
+                        // V below page 128: one box per page holding both column halves,
+                        // [page][half][PB rows][128 B] (the half-1 lanes only arrive)
+                        if (half == 0) {
+                            mbar_arrive_expect_tx(bar, 2 * box_bytes);
+                            tma_load_4d(dst + box * 2 * box_bytes, &tm_v4, bar, 0, off, 0,
+                                        page * p.num_kv_heads + kvh);
+                        } else {
+                            mbar_arrive(bar);
+                        }
                     } else if (valid) {
                         mbar_arrive_expect_tx(bar, box_bytes);
                         tma_load_3d(dst + half * C::kHalfBytes + box * box_bytes, kv == 0 ? &tm_k : &tm_v, bar,
@@ -667,11 +685,22 @@ chunk_attn_kernel(const ChunkParams p, const __grid_constant__ CUtensorMap tm_q,
                         ++tail_uses;
                         const int first = key_end - key0;   // 1 .. 127
                         const int nchunks = (128 - first) * 8;   // 16-byte chunks per half
-                        for (int c = 0; c < C::kHalves; ++c)
-                            for (int x = lane; x < nchunks; x += 32) {
-                                uint4 *row = reinterpret_cast<uint4 *>(dst + c * C::kHalfBytes + first * 128);
-                                row[x] = make_uint4(0, 0, 0, 0);
+                        if (v_pages && !from_new) {
+                            // [page][half][PB rows][128 B]: row r, half c at
+                            // (r / PB) * 2 * box_bytes + c * box_bytes + (r % PB) * 128
+                            for (int x = lane; x < 2 * nchunks; x += 32) {
+                                const int r = first + (x >> 4), c = (x >> 3) & 1;
+                                uint4 *q = reinterpret_cast<uint4 *>(dst + (r / PB) * 2 * box_bytes + c * box_bytes +
+                                                                     (r % PB) * 128);
+                                q[x & 7] = make_uint4(0, 0, 0, 0);
                             }
+                        } else {
+                            for (int c = 0; c < C::kHalves; ++c)
+                                for (int x = lane; x < nchunks; x += 32) {
+                                    uint4 *row = reinterpret_cast<uint4 *>(dst + c * C::kHalfBytes + first * 128);
+                                    row[x] = make_uint4(0, 0, 0, 0);
+                                }
+                        }
                         fence_proxy_async_smem();
                         __syncwarp();
                         if (issuer)
@@ -807,11 +836,22 @@ chunk_attn_kernel(const ChunkParams p, const __grid_constant__ CUtensorMap tm_q,
                     umma_ss(tmem + C::s_col(n), a, b, idesc_qk, kk > 0);
             }
         };
-        auto issue_pv = [&](int n, int slot, bool acc) {
+        // V below page 128 (cache tiles) lands page-major, [page][half][P rows][128 B]:
+        // keys 16 kk .. 16 kk + 15 start at page 16 kk / P, row 16 kk % P; the
+        // column halves are P * 128 bytes apart, 8-key groups 1024 bytes (two pages
+        // at page 8). Otherwise [half][128 rows][128 B].
+        const int pg = p.page_size < 128 ? p.page_size : 128;
+        const int lg_pg = __ffs(pg) - 1;
+        const bool v_pages = D == 128 && pg < 128;
+        auto issue_pv = [&](int n, int slot, bool acc, bool pm) {
 #pragma unroll
             for (int kk = 0; kk < 128 / 16; ++kk) {
-                const uint64_t b = smem_desc_sw128(slot_addr + slot * C::kTileBytes + kk * 16 * 128,
-                                                   C::kHalfBytes, 1024);
+                const int r0 = kk * 16;
+                const uint32_t off = pm ? (uint32_t)(((r0 >> lg_pg) << (lg_pg + 8)) + (r0 & (pg - 1)) * 128)
+                                        : (uint32_t)(r0 * 128);
+                const uint64_t b = smem_desc_sw128(slot_addr + slot * C::kTileBytes + off,
+                                                   pm ? (uint32_t)pg * 128u : (uint32_t)C::kHalfBytes,
+                                                   pm && pg < 16 ? (uint32_t)pg * 256u : 1024u);
                 if (elect_one_sync())
                     umma_ts(tmem + C::o_col(n), tmem + C::s_col(n) + kk * 8, b, idesc_pv, (acc || kk > 0));
             }
@@ -826,6 +866,8 @@ chunk_attn_kernel(const ChunkParams p, const __grid_constant__ CUtensorMap tm_q,
         for (int it = it_begin; it < it_end && !aborted(); ++it) {
             const PrefillItem w = items[it];
             const int n = w.kt1 - w.kt0;
+            // tiles from nh on hold the chunk's own keys, loaded from k/v (fused KV write)
+            const int nh = v_pages && p.fused ? (p.seq_lens[w.r] - p.query_lens[w.r] + 127) / 128 : 0x7fffffff;
             if (!wait(&bars->q_full, q_uses & 1))
                 break;
             ++q_uses;
@@ -848,7 +890,8 @@ chunk_attn_kernel(const ChunkParams p, const __grid_constant__ CUtensorMap tm_q,
                     break;
                 ++p_uses[0];
                 tc_fence_after_sync();
-                issue_pv(0, sV, t > 0);
+                const bool pm = v_pages && w.kt0 + t < nh;
+                issue_pv(0, sV, t > 0, pm);
                 commit(&bars->o_done[0]);
                 const bool more = t + 1 < n;
                 if (more) {
@@ -862,7 +905,7 @@ chunk_attn_kernel(const ChunkParams p, const __grid_constant__ CUtensorMap tm_q,
                         break;
                     ++p_uses[1];
                     tc_fence_after_sync();
-                    issue_pv(1, sV, t > 0);
+                    issue_pv(1, sV, t > 0, pm);
                     commit(&bars->o_done[1]);
                 }
                 commit(&bars->slot_empty[sV]);
@@ -1198,7 +1241,7 @@ chunk_attn_kernel(const ChunkParams p, const __grid_constant__ CUtensorMap tm_q,
 template <int D, int NQ>
 cudaError_t launch_chunk_t(const ChunkParams &p, const CUtensorMap &tq, const CUtensorMap &tk,
                            const CUtensorMap &tv, const CUtensorMap &tkn, const CUtensorMap &tvn,
-                           const CUtensorMap &to, int grid, cudaStream_t s, bool early)
+                           const CUtensorMap &to, const CUtensorMap &tv4, int grid, cudaStream_t s, bool early)
 {
     using C = ChunkCfg<D, NQ>;
     static std::atomic<uint64_t> done_self{0}, done_plan{0};
@@ -1206,7 +1249,7 @@ cudaError_t launch_chunk_t(const ChunkParams &p, const CUtensorMap &tq, const CU
     return launch_with_smem(p.self_plan ? done_self : done_plan, reinterpret_cast<const void *>(k), C::kSmemBytes,
                             [&] {
                                 return launch_pdl(early, k, dim3(grid), dim3(C::kThreads), C::kSmemBytes, s, p, tq,
-                                                  tk, tv, tkn, tvn, to);
+                                                  tk, tv, tkn, tvn, to, tv4);
                             });
 }
 
@@ -1214,13 +1257,14 @@ cudaError_t launch_chunk_t(const ChunkParams &p, const CUtensorMap &tq, const CU
 
 cudaError_t launch_chunk_attn(const ChunkParams &p, const CUtensorMap &tq, const CUtensorMap &tk,
                               const CUtensorMap &tv, const CUtensorMap &tkn, const CUtensorMap &tvn,
-                              const CUtensorMap &to, int head_dim, int nq, int grid, cudaStream_t s, bool early)
+                              const CUtensorMap &to, const CUtensorMap &tv4, int head_dim, int nq, int grid,
+                              cudaStream_t s, bool early)
 {
     if (head_dim == 128)
-        return nq == 2 ? launch_chunk_t<128, 2>(p, tq, tk, tv, tkn, tvn, to, grid, s, early)
-                       : launch_chunk_t<128, 1>(p, tq, tk, tv, tkn, tvn, to, grid, s, early);
-    return nq == 2 ? launch_chunk_t<64, 2>(p, tq, tk, tv, tkn, tvn, to, grid, s, early)
-                   : launch_chunk_t<64, 1>(p, tq, tk, tv, tkn, tvn, to, grid, s, early);
+        return nq == 2 ? launch_chunk_t<128, 2>(p, tq, tk, tv, tkn, tvn, to, tv4, grid, s, early)
+                       : launch_chunk_t<128, 1>(p, tq, tk, tv, tkn, tvn, to, tv4, grid, s, early);
+    return nq == 2 ? launch_chunk_t<64, 2>(p, tq, tk, tv, tkn, tvn, to, tv4, grid, s, early)
+                   : launch_chunk_t<64, 1>(p, tq, tk, tv, tkn, tvn, to, tv4, grid, s, early);
 }
 
 }  // namespace cpsa
