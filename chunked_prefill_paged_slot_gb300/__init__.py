@@ -17,6 +17,7 @@ this package is its Python binding plus host-side orchestration:
 from ._lib import (  # noqa: F401
     CpsaError, load, cpp_kv_cache_write, cpp_attn_workspace_bytes, cpp_attn_workspace_min_bytes,
     cpp_chunked_prefill_attn, cpp_chunked_prefill_attn_events, cpp_chunked_prefill_attn_noalloc,
+    cpp_noalloc_scratch_address,
     cpp_chunked_prefill_attn_write_kv,
     cpp_split_microbatch, cpp_read_device_error, cpp_get_device_error, cpp_plan_chunk_sizes,
     cpp_fit_latency_quadratic, cpp_fit_latency_two_var, cpp_selftest_exp2, cpp_selftest_wait_timeout,

@@ -65,6 +65,8 @@ def load():
                                                       _c_int, _c_p, _c_p, _c_size, _c_p, _c_p]
     lib.cpp_chunked_prefill_attn_write_kv_events.restype = _c_int
     lib.cpp_chunked_prefill_attn_write_kv_events.argtypes = lib.cpp_chunked_prefill_attn_write_kv.argtypes + [_c_p]
+    lib.cpp_noalloc_scratch_address.restype = _c_int
+    lib.cpp_noalloc_scratch_address.argtypes = [ctypes.POINTER(_c_p)]
     lib.cpp_chunked_prefill_attn_noalloc.restype = _c_int
     lib.cpp_chunked_prefill_attn_noalloc.argtypes = [_c_p, _c_p, _c_p, _c_p, _c_p, _c_p, _c_int, _c_i64, _c_int,
                                                      _c_int, _c_int, _c_int, _c_int, _c_i64, _c_f, _c_int, _c_p,
@@ -237,6 +239,13 @@ def cpp_chunked_prefill_attn_write_kv(q, k, v, slot_mapping, k_cache, v_cache, q
         evs = (_c_p * 5)(*[_c_p(e.cuda_event) if e is not None else _c_p(0) for e in events])
         st = load().cpp_chunked_prefill_attn_write_kv_events(*args, evs)
     _check(st, "cpp_chunked_prefill_attn_write_kv")
+
+
+def cpp_noalloc_scratch_address():
+    """Device address (int) of the no-alloc scratch area in the current CUDA context."""
+    addr = _c_p()
+    _check(load().cpp_noalloc_scratch_address(ctypes.byref(addr)), "cpp_noalloc_scratch_address")
+    return int(addr.value or 0)
 
 
 def cpp_chunked_prefill_attn_noalloc(q, k_cache, v_cache, query_lens, seq_lens, block_table, out, dev_err,

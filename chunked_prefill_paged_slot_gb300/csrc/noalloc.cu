@@ -121,3 +121,14 @@ extern "C" int cpp_chunked_prefill_attn_noalloc(const void *q, const void *k_cac
                                     max_blocks_per_req, num_q_heads, num_kv_heads, head_dim, page_size, num_pages,
                                     scale, max_kv_splits, out, scratch, kScratchBytes, dev_err, stream);
 }
+
+extern "C" int cpp_noalloc_scratch_address(void **addr)
+{
+    if (!addr)
+        return CPSA_ERR_CUDA;
+    void *p = nullptr;
+    const int st = scratch_address(&p);
+    if (st == CPSA_OK)
+        *addr = p;
+    return st;
+}

@@ -265,6 +265,17 @@ int cpp_chunked_prefill_attn_noalloc(const void *q, const void *k_cache, const v
                                      int max_kv_splits, void *out, uint32_t *dev_err, void *stream);
 
 /*
+ * The device address of cpp_chunked_prefill_attn_noalloc's scratch area in the
+ * calling thread's current CUDA context (the device's primary context when no
+ * context is current), written to *addr: the same lookup, and the same
+ * per-context cache, as the first attention call in that context (so it also
+ * reserves the area, and can serve as the warm-up call). Launches nothing.
+ * Returns CPSA_OK, CPSA_ERR_NO_DEVICE, CPSA_ERR_SCRATCH_UNAVAILABLE or
+ * CPSA_ERR_CUDA; *addr is left unchanged on an error.
+ */
+int cpp_noalloc_scratch_address(void **addr);
+
+/*
  * Balanced micro-batch split point ([DS] section 3.1, "advanced method").
  *
  * total = sum(query_lens); best = total / 2 (integer); over request boundaries

@@ -8,8 +8,10 @@ different batches (the second finding the first one's data in the scratch
 area), and checks each result bit for bit against cpp_chunked_prefill_attn with
 a caller workspace (the split partials fit in both, so both make the same
 choices), and both against the fp64 oracle within the attention tolerance of
-the other tests. The file sorts last so that a run stopping at the first
-failure has run everything else.
+the other tests. A context created through the driver API must get its own
+lookup of the scratch area's address (a __device__ array has one address per
+context), never the primary context's cached one. The file sorts last so that a
+run stopping at the first failure has run everything else.
 """
 import numpy as np
 import pytest
@@ -95,3 +97,33 @@ def test_noalloc_rejects_a_batch_beyond_the_scratch_area(cuda_lib):
                                               ctypes.c_void_p(torch.cuda.current_stream().cuda_stream))
     assert st == -8     # CPSA_ERR_SCRATCH_TOO_SMALL, nothing launched
     assert lib.cpp_status_string(st).startswith(b"batch needs more")
+
+
+def test_scratch_address_is_looked_up_per_context(cuda_lib):
+    """A second context on the same device, created and made current through
+    the driver API, gets the address of its own copy of the scratch area; the
+    primary context keeps its cached one. No kernel runs in the second context."""
+    import ctypes
+    import torch
+    torch.zeros(1, device="cuda")                     # the primary context is current
+    a_primary = cuda_lib.cpp_noalloc_scratch_address()
+    assert a_primary != 0
+    assert cuda_lib.cpp_noalloc_scratch_address() == a_primary
+    try:
+        cu = ctypes.CDLL("libcuda.so.1")
+        create, pop, destroy = cu.cuCtxCreate_v2, cu.cuCtxPopCurrent_v2, cu.cuCtxDestroy_v2
+    except (OSError, AttributeError):
+        pytest.skip("the driver API's context calls are not reachable")
+    dev = ctypes.c_int()
+    assert cu.cuDeviceGet(ctypes.byref(dev), torch.cuda.current_device()) == 0
+    ctx = ctypes.c_void_p()
+    assert create(ctypes.byref(ctx), 0, dev) == 0      # pushed: current on this thread
+    try:
+        a_other = cuda_lib.cpp_noalloc_scratch_address()
+    finally:
+        top = ctypes.c_void_p()
+        assert pop(ctypes.byref(top)) == 0 and top.value == ctx.value
+        assert destroy(ctx) == 0
+    # both arrays are live in one unified address space, so they cannot coincide
+    assert a_other != 0 and a_other != a_primary, (hex(a_other), hex(a_primary))
+    assert cuda_lib.cpp_noalloc_scratch_address() == a_primary
