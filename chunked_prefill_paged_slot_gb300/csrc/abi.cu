@@ -476,10 +476,11 @@ int attn_impl(const void *q, const void *k_new, const void *v_new, const int64_t
     cp.split_ok = max_kv_splits > 1 && partials_fit ? 1 : 0;
     cp.split_clamped = max_kv_splits > 1 && !partials_fit ? 1 : 0;
     // out, [T][Hq][D], in boxes of 64 columns x 1 head x 32 rows: the chunk
-    // kernel's TMA-store epilogue (head_dim 128 without the KV write, whose cache
-    // writer holds the staging buffer); without the map the rows are stored directly
+    // kernel's TMA stores of whole units' rows (head_dim 128 without the KV
+    // write, whose cache writer holds the staging buffer) and of merged rows at
+    // the end of a run; without the map the rows are stored directly
     CUtensorMap to = tq;
-    cp.out_tma = !fused && head_dim == 128 && aligned16(out) &&
+    cp.out_tma = head_dim == 128 && aligned16(out) &&
                          make_map(&to, out, D, (uint64_t)num_q_heads, (uint64_t)num_tokens, D * 2,
                                   D * 2 * num_q_heads, 64, 1, 32)
                      ? 1

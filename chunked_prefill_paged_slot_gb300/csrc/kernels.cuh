@@ -50,7 +50,8 @@ struct ChunkParams : AttnCommon {
     int num_tokens;             // for the self-planned batch's token check
     int split_ok;               // self-planned batch: units may be cut (splits allowed and the partials fit)
     int split_clamped;          // self-planned batch: splits were asked for but the partials do not fit
-    int out_tma;                // head_dim 128 without the KV write: whole units' rows leave by TMA stores
+    int out_tma;                // head_dim 128, `out` mapped for TMA stores (whole units' rows without the KV
+                                // write, merged rows at the end of a run)
 };
 
 struct DecodeParams : AttnCommon {

@@ -95,6 +95,7 @@ struct ChunkBars {
     uint64_t s_full[2], p_full[2], o_done[2];
     uint64_t slot_full[8], slot_empty[8];
     uint64_t stage;        // fused KV write: the writer's buffer is loaded
+    uint64_t writer_done;  // the cache writer has finished with its buffer (its last store has read it)
     uint32_t tmem_base;
     int abort;
     int it_begin, it_end;    // this CTA's run of pieces
@@ -373,14 +374,22 @@ __device__ __forceinline__ float merge_weights(const float2 *pml, int piece, int
 // through this warp's kMergeStageBytes of them (cp.async), so the L2 latency is
 // paid once. Kept out of line so that its registers do not weigh on the softmax
 // loop.
+//
+// The weighted sum runs on packed f32x2 pairs (one fma.rn.f32x2 per pair and
+// piece, the rounding of one fmaf per element, in the same order). With ostage
+// (this warp's 4 KB of the cache writer's buffer, free at the end of a run) and
+// every row valid, the merged rows leave by TMA stores through the `out` map,
+// 64 columns at a time; otherwise each lane stores its row.
 template <int D, int NQ>
 __device__ __noinline__ void merge_split_row(const ChunkParams &p, uint32_t tO, const float2 *pml, const uint4 *ph,
                                              int piece, int npieces, int wg, int row, int lane, float m_use, float l,
-                                             bool valid_row, int64_t out_off, uint4 *stage)
+                                             bool valid_row, int64_t out_off, uint4 *stage, uint8_t *ostage,
+                                             const CUtensorMap *tm_o, int h, int t_row0)
 {
     float wq[kMergeMaxOthers + 1];
     const float inv_L = merge_weights<NQ>(pml, piece, npieces, wg, row, m_use, l, wq);
     const float inv_own = l > 0.f ? 1.f / l : 0.f;
+    const bool staged_out = ostage != nullptr && __all_sync(0xffffffffu, valid_row);
     if (stage != nullptr) {
 #pragma unroll
         for (int q = 0; q <= kMergeMaxOthers; ++q) {
@@ -393,41 +402,76 @@ __device__ __noinline__ void merge_split_row(const ChunkParams &p, uint32_t tO, 
         }
         cp_async_wait_all();
     }
+    // bf16 pair (low half first) as an f32x2 pair
+    auto widen = [](uint32_t w) -> uint64_t { return f2_pack(__uint_as_float(w << 16), __uint_as_float(w & 0xffff0000u)); };
+    const uint64_t own2 = f2_pack(inv_own, inv_own), invL2 = f2_pack(inv_L, inv_L);
 #pragma unroll 1
     for (int c = 0; c < D / 32; ++c) {
         uint32_t r[32];
         tmem_ld32(tO + c * 32, r);
         tmem_wait_ld();
-        float acc[32];
+        uint64_t acc[16];
 #pragma unroll
-        for (int x = 0; x < 32; ++x) acc[x] = 0.f;
+        for (int x = 0; x < 16; ++x) acc[x] = 0ull;
 #pragma unroll
         for (int q = 0; q <= kMergeMaxOthers; ++q) {
             if (q >= npieces)
                 continue;
-            float v[32];
+            const uint64_t w2 = f2_pack(wq[q], wq[q]);
             if (q == piece) {
+                // this piece's O / l rounded to bf16 like the stored partials
 #pragma unroll
-                for (int x = 0; x < 32; ++x) v[x] = bf16_round(__uint_as_float(r[x]) * inv_own);
+                for (int x = 0; x < 16; ++x) {
+                    float a, b;
+                    f2_unpack(f2_mul(f2_pack(__uint_as_float(r[2 * x]), __uint_as_float(r[2 * x + 1])), own2), a, b);
+                    acc[x] = f2_fma(widen(pack_bf16x2(a, b)), w2, acc[x]);
+                }
             } else {
                 const int qi = q - (q > piece ? 1 : 0);
 #pragma unroll
-                for (int x = 0; x < 4; ++x)
-                    bf16x8_unpack(stage != nullptr ? stage[(qi * (D / 8) + c * 4 + x) * 32 + lane]
-                                                   : __ldcg(ph + ((int64_t)(q * NQ + wg) * (D / 8) + c * 4 + x) * 128 + row),
-                                  v + 8 * x);
+                for (int x = 0; x < 4; ++x) {
+                    const uint4 u = stage != nullptr
+                                        ? stage[(qi * (D / 8) + c * 4 + x) * 32 + lane]
+                                        : __ldcg(ph + ((int64_t)(q * NQ + wg) * (D / 8) + c * 4 + x) * 128 + row);
+                    acc[4 * x + 0] = f2_fma(widen(u.x), w2, acc[4 * x + 0]);
+                    acc[4 * x + 1] = f2_fma(widen(u.y), w2, acc[4 * x + 1]);
+                    acc[4 * x + 2] = f2_fma(widen(u.z), w2, acc[4 * x + 2]);
+                    acc[4 * x + 3] = f2_fma(widen(u.w), w2, acc[4 * x + 3]);
+                }
+            }
+        }
+        uint32_t pk[16];
+#pragma unroll
+        for (int x = 0; x < 16; ++x) {
+            float a, b;
+            f2_unpack(f2_mul(acc[x], invL2), a, b);
+            pk[x] = pack_bf16x2(a, b);
+        }
+        if (staged_out) {
+            // 64 columns per store: blocks c = 2 c2 and 2 c2 + 1, row `lane` at lane * 128
+            // bytes, 16-byte chunk j at (j ^ (lane & 7)) (the map's 128-byte swizzle)
+            if ((c & 1) == 0) {
+                if (lane == 0)
+                    bulk_wait_group_read0();   // the previous store has read the buffer
+                __syncwarp();
             }
 #pragma unroll
-            for (int x = 0; x < 32; ++x) acc[x] = fmaf(wq[q], v[x], acc[x]);
-        }
-        if (valid_row) {
+            for (int x = 0; x < 4; ++x)
+                *reinterpret_cast<uint4 *>(ostage + lane * 128 + ((((c & 1) * 4 + x) ^ (lane & 7)) << 4)) =
+                    make_uint4(pk[4 * x], pk[4 * x + 1], pk[4 * x + 2], pk[4 * x + 3]);
+            if ((c & 1) == 1) {
+                fence_proxy_async_smem();
+                __syncwarp();
+                if (lane == 0) {
+                    tma_store_3d(tm_o, ostage, (c >> 1) * 64, h, t_row0);
+                    bulk_commit_group();
+                }
+            }
+        } else if (valid_row) {
             uint4 *dst = reinterpret_cast<uint4 *>(reinterpret_cast<__nv_bfloat16 *>(p.out) + out_off + c * 32);
 #pragma unroll
             for (int x = 0; x < 4; ++x)
-                dst[x] = make_uint4(pack_bf16x2(acc[8 * x + 0] * inv_L, acc[8 * x + 1] * inv_L),
-                                    pack_bf16x2(acc[8 * x + 2] * inv_L, acc[8 * x + 3] * inv_L),
-                                    pack_bf16x2(acc[8 * x + 4] * inv_L, acc[8 * x + 5] * inv_L),
-                                    pack_bf16x2(acc[8 * x + 6] * inv_L, acc[8 * x + 7] * inv_L));
+                dst[x] = make_uint4(pk[4 * x], pk[4 * x + 1], pk[4 * x + 2], pk[4 * x + 3]);
         }
     }
 }
@@ -520,6 +564,7 @@ chunk_attn_kernel(const ChunkParams p, const __grid_constant__ CUtensorMap tm_q,
             mbar_init(&bars->slot_empty[s], 1);
         }
         mbar_init(&bars->stage, 1);
+        mbar_init(&bars->writer_done, 1);
         bars->abort = 0;
         fence_barrier_init();
     }
@@ -527,7 +572,7 @@ chunk_attn_kernel(const ChunkParams p, const __grid_constant__ CUtensorMap tm_q,
         tma_prefetch_desc(&tm_q);
         tma_prefetch_desc(&tm_k);
         tma_prefetch_desc(&tm_v);
-        if (!SELF && D == 128 && p.out_tma && !p.fused)
+        if (D == 128 && p.out_tma)
             tma_prefetch_desc(&tm_o);
         if (D == 128 && p.page_size < 128)
             tma_prefetch_desc(&tm_v4);
@@ -807,6 +852,8 @@ chunk_attn_kernel(const ChunkParams p, const __grid_constant__ CUtensorMap tm_q,
             if (lane == 0)
                 bulk_wait_group0();   // the cache stores are complete before the CTA ends
         }
+        if (lane == 0)
+            mbar_arrive(&bars->writer_done);
     } else if (warp == C::kMmaWarp) {
         // ------------------------------------------------------------ MMA issuer
         // The whole warp walks the loop; every MMA and commit is issued by one
@@ -1129,10 +1176,15 @@ chunk_attn_kernel(const ChunkParams p, const __grid_constant__ CUtensorMap tm_q,
                         if (D == 128 && it + 1 == it_end)
                             staged = NQ == 1 || __all_sync(0xffffffffu, mbar_wait(&bars->o_done[NQ - 1 - wg],
                                                                                   (o_base - 1) & 1, abort));
+                        // the merged rows through the writer's buffer once the writer is done with it
+                        const bool ostaged = staged && p.out_tma &&
+                                             (!p.fused || __all_sync(0xffffffffu, mbar_wait(&bars->writer_done, 0, abort)));
                         merge_split_row<D, NQ>(p, tO, pml, ph, piece, npieces, wg, row, lane, m_use, l, valid_row,
                                                out_off,
                                                staged ? reinterpret_cast<uint4 *>(smem + (wg * 4 + sub) * kMergeStageBytes)
-                                                      : nullptr);
+                                                      : nullptr,
+                                               ostaged ? smem + C::kStageOff + (wg * 4 + sub) * 4096 : nullptr, &tm_o, h,
+                                               (int)(t_row - lane));
                     } else {
                         merge_split_row_any<D, NQ>(p, tO, pml, ph, piece, npieces, wg, row, m_use, l, valid_row,
                                                    out_off);
@@ -1223,7 +1275,7 @@ chunk_attn_kernel(const ChunkParams p, const __grid_constant__ CUtensorMap tm_q,
     }
 
     // the softmax warps' output stores are complete before the CTA ends
-    if (!SELF && D == 128 && warp / 4 < NQ && lane == 0 && p.out_tma && !p.fused)
+    if (D == 128 && warp / 4 < NQ && lane == 0 && p.out_tma)
         bulk_wait_group0();
     if (threadIdx.x == 0 && bars->abort)
         set_dev_error(p.dev_err, CPSA_DEV_WAIT_TIMEOUT);
