@@ -42,7 +42,7 @@ if ROOT not in sys.path:
 
 SEQ, CHUNK, HQ, HKV, D, PAGE = 32768, 512, 32, 8, 128, 128
 N_CHUNKS = SEQ // CHUNK
-E2E_BATCH = 8   # chunks per host<->device copy in the end-to-end measurement
+E2E_BATCH = 4   # chunks per host<->device copy in the end-to-end measurement
 WORKLOAD = "llama3-8b-attn-layer 32768-token prefill in 64 chunks of 512 (32/8 heads, d128, bf16, page 128)"
 METRIC = "chunked-prefill attention TFLOP/s"
 
