@@ -862,16 +862,30 @@ def main():
     e2e_val = job_tflops(world, STEP_FLOPS, 1, e2e_step_ms)
 
     # roofline of the dominant kernel (the tensor-core chunk kernel): separate steps
-    # with events around every chunk-kernel launch (events between kernels keep
-    # the next kernel from launching early, so the headline steps carry none)
-    kernel_ms = []
-    for s in range(5):
-        flush.zero_()
-        wl.step(stream, with_marks=True)
+    # with events around every chunk-kernel launch (the headline steps carry none),
+    # in the headline's launch mode (the marked step captured in a graph of its own,
+    # the events becoming event nodes around each kernel) and as stream launches
+    def marked_steps(run):
+        kernel_ms = []
+        for _ in range(5):
+            flush.zero_()
+            run()
+            torch.cuda.synchronize()
+            kernel_ms.append(wl.chunk_kernel_ms())
+        return np.asarray(kernel_ms)                 # [steps, chunks]
+
+    km_stream = marked_steps(lambda: wl.step(stream, with_marks=True))
+    km = km_stream
+    if not args.eager:
+        marked_graph = torch.cuda.CUDAGraph()
+        capture3 = torch.cuda.Stream(device=dev)
+        with torch.cuda.graph(marked_graph, stream=capture3):
+            wl.step(capture3, with_marks=True)
         torch.cuda.synchronize()
-        kernel_ms.append(wl.chunk_kernel_ms())
+        marked_graph.replay()
+        torch.cuda.synchronize()
+        km = marked_steps(marked_graph.replay)
     peak_tf, peak_bw, peak_src = load_peaks()
-    km = np.asarray(kernel_ms)                       # [steps, chunks]
     per_launch_ms = float(km.mean())
     per_launch_flops = STEP_FLOPS / N_CHUNKS
     achieved = per_launch_flops / (per_launch_ms * 1e-3) / 1e12
@@ -879,6 +893,8 @@ def main():
                 "frac": round(achieved / peak_tf, 4), "traffic": load_traffic(),
                 "kernel": "chunk_attn_kernel<128,2,true> (one request per call: runs planned by the kernel itself)", "peak_source": f"{peak_src} bf16 dense (burst)",
                 "per_launch_flops": per_launch_flops, "per_launch_ms": round(per_launch_ms, 4),
+                "launch": "stream launches" if args.eager else "graph replay (event nodes around each launch)",
+                "per_launch_ms_stream_launches": round(float(km_stream.mean()), 4),
                 "last_chunk_ms": round(float(km[:, -1].mean()), 4),
                 "per_chunk_ms": [round(float(x), 4) for x in km.mean(axis=0)],
                 "last_chunk_tflops": round(chunk_flops((N_CHUNKS - 1) * CHUNK, CHUNK) / (km[:, -1].mean() * 1e-3) / 1e12, 2)}

@@ -319,8 +319,15 @@ int attn_impl(const void *q, const void *k_new, const void *v_new, const int64_t
     if (events)
         for (int i = 0; i < 5; ++i)
             ev[i] = static_cast<cudaEvent_t>(events[i]);
+    // under stream capture a mark becomes an event node of the graph (recorded at
+    // every replay); the external flag is for capture only
     auto mark = [&](int i, cudaStream_t st) {
-        if (ev[i])
+        if (!ev[i])
+            return;
+        cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+        if (cudaStreamIsCapturing(st, &cs) == cudaSuccess && cs == cudaStreamCaptureStatusActive)
+            cudaEventRecordWithFlags(ev[i], st, cudaEventRecordExternal);
+        else
             cudaEventRecord(ev[i], st);
     };
     // programmatic dependent launch between the call's own kernels, except when

@@ -164,7 +164,10 @@ int cpp_chunked_prefill_attn(const void *q, const void *k_cache, const void *v_c
  * [3] after the decode kernel, [4] after the combine kernel (kernels that a
  * batch does not need are not launched; their marks follow the previous one).
  * For profiling harnesses; the computation is identical, its kernels launched
- * in plain stream order.
+ * in plain stream order. Under stream capture the marks are recorded as
+ * external events (cudaEventRecordExternal), so a call captured in a CUDA graph
+ * records them as event nodes at every replay and their timings can be read
+ * afterwards.
  */
 int cpp_chunked_prefill_attn_events(const void *q, const void *k_cache, const void *v_cache,
                                     const int32_t *query_lens, const int32_t *seq_lens,

@@ -107,3 +107,37 @@ def test_graph_replay_new_inputs(cuda_lib, case, fused):
             bufs.load(torch, cuda_lib, batches[0], fused)
             bufs.call(cuda_lib, fused, splits)
             _check(torch, cuda_lib, bufs, batches[0], f"{case} eager between replays")
+
+
+def test_graph_replay_records_timing_marks(cuda_lib):
+    """The timing-marks entry point captured in a graph: its marks become event
+    nodes, readable after every replay, while the output still meets the oracle
+    on the replay's own inputs."""
+    import torch
+    specs = [W.BatchSpec(hist=[9000], qlen=[512], num_q_heads=32, num_kv_heads=8, head_dim=128, page_size=16,
+                         seed=3300 + i) for i in range(2)]
+    batches = [W.make_batch(s) for s in specs]
+    bufs = _Bufs(torch, cuda_lib, batches[0], 8)
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(5)]
+
+    def call():
+        cuda_lib.cpp_chunked_prefill_attn_events(bufs.q, bufs.kc, bufs.vc, bufs.ql, bufs.sl, bufs.bt, bufs.out,
+                                                 bufs.ws, bufs.err, ev, max_kv_splits=8)
+
+    bufs.load(torch, cuda_lib, batches[0], False)
+    call()
+    torch.cuda.synchronize()
+    t_stream = ev[1].elapsed_time(ev[2])
+    # the chunk kernel of 512 queries over 9512 keys runs for tens of microseconds:
+    # marks recorded back to back (not around the kernel) would read far less
+    assert 0.01 < t_stream < 1000.0, t_stream
+    _check(torch, cuda_lib, bufs, batches[0], "marks, stream launch")
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        call()
+    bufs.load(torch, cuda_lib, batches[1], False)
+    g.replay()
+    torch.cuda.synchronize()
+    t_graph = ev[1].elapsed_time(ev[2])
+    assert 0.01 < t_graph < 1000.0, t_graph
+    _check(torch, cuda_lib, bufs, batches[1], "marks, graph replay")
