@@ -452,7 +452,9 @@ def serving_loop(dev, chunk_caps=(), tile_align=0, budget=2048, n_req=32, decode
     (decode rows first, then started prompts, then new ones) and allocates pages;
     each step runs the KV write and the attention kernels on it. Llama-3-8B
     shapes (32/8 heads, d128), page 16, prompts U[512, 4096], `decode_tokens`
-    decode rows per request. Device time per step from CUDA events."""
+    decode rows per request. Device time per step from CUDA events around each
+    call (host work inside the call included), and the whole loop again as one
+    graph per step replayed back to back (the kernels' own time)."""
     import torch
     import chunked_prefill_paged_slot_gb300 as cpsa
     rng = np.random.Generator(np.random.PCG64(seed))
@@ -475,7 +477,7 @@ def serving_loop(dev, chunk_caps=(), tile_align=0, budget=2048, n_req=32, decode
     err = torch.zeros(1, dtype=torch.int32, device=dev)
     ws = torch.empty(cpsa.cpp_attn_workspace_bytes(256, budget, HQ, HKV, D, 8), dtype=torch.uint8, device=dev)
     stream = torch.cuda.current_stream(dev)
-    evs, prefill_tok, decode_tok, flops, steps = [], 0, 0, 0.0, 0
+    evs, calls, prefill_tok, decode_tok, flops, steps = [], [], 0, 0, 0.0, 0
     t0 = time.perf_counter()
     while True:
         waiting, running, _, _ = sched.stats()
@@ -487,17 +489,20 @@ def serving_loop(dev, chunk_caps=(), tile_align=0, budget=2048, n_req=32, decode
             raise RuntimeError("serving loop made no progress")
         ql, sl = b["query_lens"], b["seq_lens"]
         meta = [torch.from_numpy(x).to(dev, non_blocking=True) for x in (ql, sl, b["block_table"], b["slot_mapping"])]
+        def call(T=T, meta=meta, s=stream):
+            if fused:
+                cpsa.cpp_chunked_prefill_attn_write_kv(qp[:T], kp[:T], vp[:T], meta[3], kc, vc, meta[0], meta[1],
+                                                       meta[2], out[:T], ws, err, max_kv_splits=8, stream=s)
+            else:
+                cpsa.cpp_kv_cache_write(kp[:T], vp[:T], meta[3], kc, vc, err, stream=s)
+                cpsa.cpp_chunked_prefill_attn(qp[:T], kc, vc, meta[0], meta[1], meta[2], out[:T], ws, err,
+                                              max_kv_splits=8, stream=s)
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         e0.record(stream)
-        if fused:
-            cpsa.cpp_chunked_prefill_attn_write_kv(qp[:T], kp[:T], vp[:T], meta[3], kc, vc, meta[0], meta[1],
-                                                   meta[2], out[:T], ws, err, max_kv_splits=8, stream=stream)
-        else:
-            cpsa.cpp_kv_cache_write(kp[:T], vp[:T], meta[3], kc, vc, err, stream=stream)
-            cpsa.cpp_chunked_prefill_attn(qp[:T], kc, vc, meta[0], meta[1], meta[2], out[:T], ws, err,
-                                          max_kv_splits=8, stream=stream)
+        call()
         e1.record(stream)
         evs.append((e0, e1))
+        calls.append(call)
         dec = ql == 1
         decode_tok += int(dec.sum())
         prefill_tok += int(ql[~dec].sum())
@@ -509,6 +514,25 @@ def serving_loop(dev, chunk_caps=(), tile_align=0, budget=2048, n_req=32, decode
     torch.cuda.synchronize()
     wall = time.perf_counter() - t0
     ms = [a.elapsed_time(b_) for a, b_ in evs]
+    # the same steps again, each captured in a graph of its own and replayed back
+    # to back: the kernels' time without the host work between and inside the calls
+    # (each step rewrites the same cache slots with the same rows)
+    graphs = []
+    cap = torch.cuda.Stream(device=dev)
+    for call in calls:
+        gr = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(gr, stream=cap):
+            call(s=cap)
+        graphs.append(gr)
+    torch.cuda.synchronize()
+    g0, g1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    g0.record(stream)
+    for gr in graphs:
+        gr.replay()
+    g1.record(stream)
+    torch.cuda.synchronize()
+    graph_ms = g0.elapsed_time(g1)
+    del graphs
     flags = cpsa.cpp_read_device_error(err)
     sched.close()
     del kc, vc, qp, kp, vp, ws
@@ -517,7 +541,9 @@ def serving_loop(dev, chunk_caps=(), tile_align=0, budget=2048, n_req=32, decode
             "device_ms": round(float(sum(ms)), 3), "mean_step_ms": round(float(np.mean(ms)), 4),
             "max_step_ms": round(float(np.max(ms)), 4), "wall_s": round(wall, 3),
             "tokens_per_s_device": round((prefill_tok + decode_tok) / (sum(ms) * 1e-3), 1),
-            "attention_tflops_device": round(flops / (sum(ms) * 1e-3) / 1e12, 2), "device_flags": flags}
+            "attention_tflops_device": round(flops / (sum(ms) * 1e-3) / 1e12, 2),
+            "graph_replay_ms": round(graph_ms, 3),
+            "attention_tflops_graph_replay": round(flops / (graph_ms * 1e-3) / 1e12, 2), "device_flags": flags}
 
 
 def step_roofline(ms_per_step, peak_tf, peak_gbs):
@@ -1019,6 +1045,10 @@ def summary_of(line):
     if "two_vs_one" in mb:
         out["microbatch_two_vs_one"] = round(mb["two_vs_one"], 4)
         out["microbatch_prefill_tflops_one_stream"] = round(mb["prefill_tflops_one_stream"], 1)
+    sl = su.get("serving_loop", {}).get("budget_only", {})
+    if "graph_replay_ms" in sl:
+        out["serving_loop_ms_per_call_events"] = sl["device_ms"]
+        out["serving_loop_ms_graph_replay"] = sl["graph_replay_ms"]
     if "tile_alignment_h8192" in su:
         out["tile_alignment_h8192_ms"] = su["tile_alignment_h8192"]
     out["headline_tflops"] = line.get("value")
