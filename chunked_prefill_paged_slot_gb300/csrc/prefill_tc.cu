@@ -476,6 +476,62 @@ __device__ __noinline__ void merge_split_row(const ChunkParams &p, uint32_t tO, 
     }
 }
 
+// The rows of a whole unit in the self-planned kernel without the KV write: as
+// in the planned kernel's epilogue, each warp stages its 32 rows, 64 columns at
+// a time, in its own 4 KB (stg) of the cache writer's idle buffer and a TMA
+// store writes them out; a warp with rows past the request's end stores its
+// valid rows directly. Out of line: compiled into the self-planned kernel's
+// loop, the same code measured slower on one-request chunks with the KV write
+// fused, which never take it.
+template <int D>
+__device__ __noinline__ void store_unit_rows_staged(uint32_t tO, float l, bool valid_row, uint8_t *stg,
+                                                    const CUtensorMap *tm_o, __nv_bfloat16 *out, int64_t t_row,
+                                                    int h, int num_q_heads, int lane)
+{
+    const float inv_l = l > 0.f ? 1.f / l : 0.f;
+    const bool staged = __all_sync(0xffffffffu, valid_row);
+#pragma unroll
+    for (int c2 = 0; c2 < D / 64; ++c2) {
+        if (staged) {
+            if (lane == 0)
+                bulk_wait_group_read0();   // the warp's previous store has read the buffer
+            __syncwarp();
+        }
+#pragma unroll
+        for (int cc = 0; cc < 2; ++cc) {
+            const int c = 2 * c2 + cc;
+            uint32_t r[32];
+            tmem_ld32(tO + c * 32, r);
+            tmem_wait_ld();
+            uint4 v[4];
+#pragma unroll
+            for (int x = 0; x < 4; ++x)
+                v[x] = make_uint4(pack_bf16x2(__uint_as_float(r[8 * x + 0]) * inv_l, __uint_as_float(r[8 * x + 1]) * inv_l),
+                                  pack_bf16x2(__uint_as_float(r[8 * x + 2]) * inv_l, __uint_as_float(r[8 * x + 3]) * inv_l),
+                                  pack_bf16x2(__uint_as_float(r[8 * x + 4]) * inv_l, __uint_as_float(r[8 * x + 5]) * inv_l),
+                                  pack_bf16x2(__uint_as_float(r[8 * x + 6]) * inv_l, __uint_as_float(r[8 * x + 7]) * inv_l));
+            if (staged) {
+#pragma unroll
+                for (int x = 0; x < 4; ++x)
+                    *reinterpret_cast<uint4 *>(stg + lane * 128 + (((cc * 4 + x) ^ (lane & 7)) << 4)) = v[x];
+            } else if (valid_row) {
+                uint4 *dst = reinterpret_cast<uint4 *>(out + (t_row * num_q_heads + h) * D + c * 32);
+#pragma unroll
+                for (int x = 0; x < 4; ++x)
+                    dst[x] = v[x];
+            }
+        }
+        if (staged) {
+            fence_proxy_async_smem();
+            __syncwarp();
+            if (lane == 0) {
+                tma_store_3d(tm_o, stg, c2 * 64, h, (int)(t_row - lane));
+                bulk_commit_group();
+            }
+        }
+    }
+}
+
 // The same merge for units of more than kMergeMaxOthers + 1 pieces (long KV
 // ranges against short runs), every partial straight from L2; the same weights,
 // order and rounding as merge_split_row.
@@ -1252,6 +1308,9 @@ chunk_attn_kernel(const ChunkParams p, const __grid_constant__ CUtensorMap tm_q,
                         }
                     }
                 }
+            } else if (SELF && D == 128 && p.out_tma && !p.fused) {
+                store_unit_rows_staged<D>(tO, l, valid_row, smem + C::kStageOff + (wg * 4 + sub) * 4096, &tm_o,
+                                          reinterpret_cast<__nv_bfloat16 *>(p.out), t_row, h, p.num_q_heads, lane);
             } else {
                 const float inv_l = l > 0.f ? 1.f / l : 0.f;
 #pragma unroll
