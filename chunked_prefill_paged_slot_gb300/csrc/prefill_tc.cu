@@ -905,11 +905,15 @@ chunk_attn_kernel(const ChunkParams p, const __grid_constant__ CUtensorMap tm_q,
                     __syncwarp();
                 }
             }
-            if (lane == 0)
-                bulk_wait_group0();   // the cache stores are complete before the CTA ends
-        }
-        if (lane == 0)
+            // every store has read the buffer (each job waits for that): release it
+            // to the epilogue, then let the stores complete before the CTA ends
+            if (lane == 0) {
+                mbar_arrive(&bars->writer_done);
+                bulk_wait_group0();
+            }
+        } else if (lane == 0) {
             mbar_arrive(&bars->writer_done);
+        }
     } else if (warp == C::kMmaWarp) {
         // ------------------------------------------------------------ MMA issuer
         // The whole warp walks the loop; every MMA and commit is issued by one
@@ -1263,7 +1267,10 @@ chunk_attn_kernel(const ChunkParams p, const __grid_constant__ CUtensorMap tm_q,
                 // run; the self-planned kernel, with few, stores directly: staging
                 // measured slower there.)
                 const float inv_l = l > 0.f ? 1.f / l : 0.f;
-                const bool staged = p.out_tma && !p.fused && __all_sync(0xffffffffu, valid_row);
+                // with the KV write, once the cache writer has released its buffer
+                const bool writer_idle =
+                    !p.fused || __shfl_sync(0xffffffffu, lane == 0 && mbar_test_wait(&bars->writer_done, 0), 0);
+                const bool staged = p.out_tma && writer_idle && __all_sync(0xffffffffu, valid_row);
                 uint8_t *stg = smem + C::kStageOff + (wg * 4 + sub) * 4096;
 #pragma unroll
                 for (int c2 = 0; c2 < D / 64; ++c2) {
@@ -1308,7 +1315,8 @@ chunk_attn_kernel(const ChunkParams p, const __grid_constant__ CUtensorMap tm_q,
                         }
                     }
                 }
-            } else if (SELF && D == 128 && p.out_tma && !p.fused) {
+            } else if (SELF && D == 128 && p.out_tma &&
+                       (!p.fused || __shfl_sync(0xffffffffu, lane == 0 && mbar_test_wait(&bars->writer_done, 0), 0))) {
                 store_unit_rows_staged<D>(tO, l, valid_row, smem + C::kStageOff + (wg * 4 + sub) * 4096, &tm_o,
                                           reinterpret_cast<__nv_bfloat16 *>(p.out), t_row, h, p.num_q_heads, lane);
             } else {
