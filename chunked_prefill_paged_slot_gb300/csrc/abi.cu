@@ -149,12 +149,16 @@ uint32_t next_epoch()
 // stays below R0 + 3 for any history (the units grow as fast as the run).
 bool self_plan_fits(int64_t num_tokens, int units_per_qtile, int grid)
 {
+    // the most pieces a run can hold is in the no-history case (the shortest
+    // units): a run of r0 positions meets at most r0 / (1 + kUnitCostTiles) + 2 units
+    // (each unit takes at least one tile and its fixed cost, plus the ones it starts
+    // and ends inside); one more for safety
     const int64_t nqt = (num_tokens + kTileM - 1) / kTileM;
-    const int64_t w0 = (int64_t)units_per_qtile * nqt * (nqt + 1) / 2;
+    const int64_t w0 = (int64_t)units_per_qtile * (nqt * (nqt + 1) / 2 + nqt * kUnitCostTiles);
     int64_t r0 = (w0 + grid - 1) / grid;
     if (r0 < kMinRunTiles)
         r0 = kMinRunTiles;
-    return r0 + 3 <= kSelfPlanCap;
+    return r0 / (1 + kUnitCostTiles) + 3 <= kSelfPlanCap;
 }
 
 int attn_impl(const void *q, const void *k_new, const void *v_new, const int64_t *slot_mapping, void *k_cache,

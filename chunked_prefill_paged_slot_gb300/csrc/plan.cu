@@ -52,7 +52,8 @@ __device__ __forceinline__ int unit_tiles(const PlanParams &p, const Req &rq, in
     return p.fused ? ceil_div(rq.hist, kTileN) + qt + 1 : ceil_div(rq.hist + qt * kTileM + rows, kTileN);
 }
 
-// KV tiles of all prefill units of one request (0 for decode / invalid / empty).
+// Stream-K positions of all prefill units of one request: their KV tiles plus
+// kUnitCostTiles per unit (0 for decode / invalid / empty).
 __device__ int prefill_tiles(const PlanParams &p, const Req &rq)
 {
     if (!rq.valid || rq.q < 2)
@@ -60,27 +61,27 @@ __device__ int prefill_tiles(const PlanParams &p, const Req &rq)
     const int units_per_qtile = p.Hkv * (p.group / p.nq);
     int tiles = 0;
     for (int qt = 0; qt * kTileM < rq.q; ++qt)
-        tiles += unit_tiles(p, rq, qt, min(kTileM, rq.q - qt * kTileM)) * units_per_qtile;
+        tiles += (unit_tiles(p, rq, qt, min(kTileM, rq.q - qt * kTileM)) + kUnitCostTiles) * units_per_qtile;
     return tiles;
 }
 
-// KV tiles of the request's longest unit (its last query tile), 0 for decode /
+// Positions of the request's longest unit (its last query tile), 0 for decode /
 // invalid / empty requests.
 __device__ int longest_unit(const PlanParams &p, const Req &rq)
 {
     if (!rq.valid || rq.q < 2)
         return 0;
     const int nqt = ceil_div(rq.q, kTileM);
-    return unit_tiles(p, rq, nqt - 1, rq.q - (nqt - 1) * kTileM);
+    return unit_tiles(p, rq, nqt - 1, rq.q - (nqt - 1) * kTileM) + kUnitCostTiles;
 }
 
-// KV tiles of the request's shortest unit (its first query tile), INT_MAX for
+// Positions of the request's shortest unit (its first query tile), INT_MAX for
 // decode / invalid / empty requests.
 __device__ int shortest_unit(const PlanParams &p, const Req &rq)
 {
     if (!rq.valid || rq.q < 2)
         return 0x7fffffff;
-    return unit_tiles(p, rq, 0, min(kTileM, rq.q));
+    return unit_tiles(p, rq, 0, min(kTileM, rq.q)) + kUnitCostTiles;
 }
 
 __device__ int decode_splits(const Req &rq, int max_splits, int dec_heads)
@@ -166,8 +167,10 @@ __device__ Counts request_work(const PlanParams &p, int r, const Req &rq, int ti
         const int nkv = a == 0 ? nkv_last : hb + qt + 1;
         // tiles of the units of query tiles nqt - 1 .. qt + 1: nkv_last, then hb + nqt - a' for a' = 1 .. a - 1
         const int before = a == 0 ? 0 : nkv_last + (a - 1) * (hb + nqt) - (a - 1) * a / 2;
-        const int u0 = tile_off + upq * before + j * nkv, u1 = u0 + nkv;
-        const int first = u0 / run;
+        // the unit's positions [u0, u1): kUnitCostTiles of fixed cost, then its tiles from t0
+        const int u0 = tile_off + upq * (before + a * kUnitCostTiles) + j * (nkv + kUnitCostTiles);
+        const int t0 = u0 + kUnitCostTiles, u1 = t0 + nkv;
+        const int first = t0 / run;
         const int np = active ? (cut ? (u1 - 1) / run - first + 1 : 1) : 0;
         const bool split = np > 1;
         // one scan for two sums: pieces (low word) and pieces of split units (high word)
@@ -184,23 +187,24 @@ __device__ Counts request_work(const PlanParams &p, int r, const Req &rq, int ti
             const int kvh = j / pairs, hp = j - kvh * pairs;
             const int i0 = qt * kTileM;
             const int pi = off.pieces + c.pieces + (int)(ex & 0xffffffffll);
-            // with cuts, every run starts a piece: the piece starting at tile
-            // c * run is the first of CTA c's run
+            // with cuts, every run starts a piece: the piece holding position c *
+            // run (or the first one after it when that position is a unit's fixed
+            // cost) is the first of CTA c's run
             if (!split) {
                 p.pitems[pi] = PrefillItem{r, i0, kvh | (hp << 16), 0, nkv, (1 << 16), -1, first};
-                if (cut && u0 == first * run)
+                if (cut && u0 <= first * run)
                     p.run_first[first] = pi;
             } else {
                 // a split unit's partials: kTileM rows x nq heads x np pieces (see the chunk kernel's merge)
                 const int pbase = off.prows + c.prows + prow_unit * (int)(ex >> 32);
                 const int sunit = off.sunits + c.sunits + __popc(split_lanes & lanes_below);
-                int x = u0;
+                int x = t0;
                 for (int pc = 0; pc < np; ++pc) {
                     const int owner = first + pc;
                     const int end = min(u1, (owner + 1) * run);
                     p.pitems[pi + pc] =
-                        PrefillItem{r, i0, kvh | (hp << 16), x - u0, end - u0, pc | (np << 16), pbase, sunit};
-                    if (x == owner * run)
+                        PrefillItem{r, i0, kvh | (hp << 16), x - t0, end - t0, pc | (np << 16), pbase, sunit};
+                    if (pc > 0 || u0 <= owner * run)
                         p.run_first[owner] = pi + pc;
                     x = end;
                 }

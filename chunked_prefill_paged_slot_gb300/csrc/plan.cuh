@@ -26,7 +26,11 @@ namespace cpsa {
 // of max(ceil(W / grid), kMinRunTiles) tiles, one run per CTA of the chunk
 // kernel; a unit cut by a run boundary becomes several pieces, merged inside the
 // chunk kernel by whichever piece finishes last (a counter per unit and q head;
-// no CTA waits for another). Every CTA gets the same amount of work.
+// no CTA waits for another). Every CTA gets the same amount of work, counting
+// for every unit kUnitCostTiles positions ahead of its tiles: the fixed cost of
+// starting and finishing an item (loading its Q, storing its rows), which a run
+// of many short units pays many times. Those positions hold no tile: a unit's
+// first piece belongs to the run that holds its first tile.
 // Decode: a row splits into pieces of kDecodeKeysPerSplit keys (grouped items:
 // kDecodeKeysPerSplitGrouped) (at most
 // max_kv_splits), depending only on its own length.
@@ -37,6 +41,11 @@ namespace cpsa {
 // [h + 128 j, h + 128 j + 128), and the unit of query tile i has ceil(h / 128) +
 // i + 1 tiles (the same count whenever h is a multiple of 128).
 constexpr int kMinRunTiles = 4;             // shortest run of KV tiles per CTA
+#ifndef CPSA_UNIT_COST_TILES
+#define CPSA_UNIT_COST_TILES 2
+#endif
+constexpr int kUnitCostTiles = CPSA_UNIT_COST_TILES;   // a unit's fixed cost, in KV tiles (< kMinRunTiles)
+static_assert(kUnitCostTiles >= 0 && kUnitCostTiles < kMinRunTiles, "a run must hold more than one unit's start");
 constexpr int kCutCostTiles = 6;            // a run's extra item and merge when a unit is cut, in KV tiles
 constexpr int kMaxChunkGrid = 256;          // upper bound of the chunk kernel's grid (SMs)
 constexpr int kDecodeChunk = 64;            // keys per decode pipeline stage

@@ -169,30 +169,33 @@ __device__ __forceinline__ int self_plan_walk(PrefillItem *items, int lane, int 
         const int nkv = a == 0 ? nkv_last : hb + qt + 1;
         // KV tiles of one unit column before the a-th query tile from the last
         const I before = a == 0 ? (I)0 : (I)nkv_last + (I)(a - 1) * (I)(hb + nqt) - (I)((a - 1) * a / 2);
-        const I u0 = (I)upq * before + (I)j * (I)nkv, u1 = u0 + (I)nkv;
+        // the unit's positions: kUnitCostTiles of fixed cost from u0, its tiles [t0, u1)
+        const I u0 = (I)upq * (before + (I)a * kUnitCostTiles) + (I)j * (I)(nkv + kUnitCostTiles);
+        const I t0 = u0 + kUnitCostTiles, u1 = t0 + (I)nkv;
         // with cuts a run takes every piece of a unit inside it; without, whole units
         // go to the run that holds their first tile
-        const bool take = active && (cut ? (u1 > lo && u0 < hi) : (u0 >= lo && u0 < hi));
+        const bool take = active && (cut ? (u1 > lo && t0 < hi) : (t0 >= lo && t0 < hi));
         const unsigned m = __ballot_sync(0xffffffffu, take);
         if (take) {
             const int k = n + __popc(m & below);
             if (k < kSelfPlanCap) {
                 const int kvh = j / pairs, hp = j - kvh * pairs;
-                const I c0 = u0 / run;
+                const I c0 = t0 / run;
                 const int np = cut ? (int)((u1 - 1) / run - c0 + 1) : 1;
                 if (np == 1) {
                     items[k] = PrefillItem{0, qt * kTileM, kvh | (hp << 16), 0, nkv, 1 << 16, -1, (int)blockIdx.x};
                 } else {
-                    const I x0 = u0 > lo ? u0 : lo, x1 = u1 < hi ? u1 : hi;
-                    items[k] = PrefillItem{0, qt * kTileM, kvh | (hp << 16), (int)(x0 - u0), (int)(x1 - u0),
+                    const I x0 = t0 > lo ? t0 : lo, x1 = u1 < hi ? u1 : hi;
+                    items[k] = PrefillItem{0, qt * kTileM, kvh | (hp << 16), (int)(x0 - t0), (int)(x1 - t0),
                                            ((int)blockIdx.x - (int)c0) | (np << 16), 2 * (int)c0 * prow_unit,
                                            (int)c0};
                 }
             }
         }
         n += __popc(m);
-        // units come in tile order: after one that starts at or past the run's end, none is in it
-        if (__shfl_sync(0xffffffffu, active ? (u0 >= hi ? 1 : 0) : 1, 31))
+        // units come in tile order: after one whose tiles start at or past the run's
+        // end, none is in it
+        if (__shfl_sync(0xffffffffu, active ? (t0 >= hi ? 1 : 0) : 1, 31))
             break;
     }
     return n;
@@ -248,11 +251,12 @@ __device__ __noinline__ int self_plan_run(const SelfPlanArgs a, PrefillItem *ite
     const int nqt = (q + kTileM - 1) / kTileM;
     const int hb = (hist + kTileN - 1) / kTileN;
     const int nkv_last = a.fused ? hb + nqt : (hist + q + kTileN - 1) / kTileN;
-    const long long W = (long long)upq * (nkv_last + (long long)(nqt - 1) * (hb + nqt) - (long long)(nqt - 1) * nqt / 2);
-    const int shortest = nqt == 1 ? nkv_last : hb + 1;
+    const long long W = (long long)upq * (nkv_last + (long long)(nqt - 1) * (hb + nqt) - (long long)(nqt - 1) * nqt / 2 +
+                                          (long long)nqt * kUnitCostTiles);
+    const int shortest = (nqt == 1 ? nkv_last : hb + 1) + kUnitCostTiles;
     const long long grid = gridDim.x;
     const long long run = max((W + grid - 1) / grid, (long long)kMinRunTiles);
-    const bool cut = a.split_ok && !(shortest >= run && nkv_last <= run + kCutCostTiles);
+    const bool cut = a.split_ok && !(shortest >= run && nkv_last + kUnitCostTiles <= run + kCutCostTiles);
     int n = W + run < 0x7fffffffll
                 ? self_plan_walk<NQ, int>(items, lane, nqt, hb, nkv_last, upq, pairs, (int)run, cut)
                 : self_plan_walk<NQ, long long>(items, lane, nqt, hb, nkv_last, upq, pairs, run, cut);

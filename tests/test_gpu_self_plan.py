@@ -3,8 +3,9 @@ skips the plan kernel, and every chunk-kernel CTA computes its own stream-K run
 (units, run length and cut rule of the plan; split units' partial rows and merge
 counters addressed by the run they start in; epoch-tagged merge counters that
 no kernel clears between calls). Each case is checked against the fp64 oracle.
-Batches of one request up to 3968 tokens (32 q / 8 kv heads on 152 SMs) take
-this path; 4096 tokens takes the plan kernel and is checked beside it."""
+Batches of one request up to 6656 tokens (32 q / 8 kv heads on 152 SMs, each
+unit weighted by its fixed cost of two tiles) take this path; 6784 tokens takes
+the plan kernel and is checked beside it."""
 import numpy as np
 import pytest
 
@@ -47,9 +48,10 @@ def test_single_prefill_heads(cuda_lib, d, hq, hkv):
         compare(got, _oracle_rows(b), what=f"d={d} {hq}/{hkv}")
 
 
-@pytest.mark.parametrize("q", [3968, 4096])
+@pytest.mark.parametrize("q", [3968, 6656, 6784])
 def test_size_on_either_side_of_the_self_plan_bound(cuda_lib, q):
-    """3968 tokens: self-planned; 4096: the plan kernel. Sampled rows, every tile edge."""
+    """6656 tokens: self-planned (the most pieces a run may hold); 6784: the plan
+    kernel; 3968 as well. Sampled rows, every tile edge."""
     spec = W.BatchSpec(hist=[300], qlen=[q], num_q_heads=32, num_kv_heads=8, head_dim=128, page_size=16,
                        seed=1300 + q)
     b = W.make_batch(spec)
