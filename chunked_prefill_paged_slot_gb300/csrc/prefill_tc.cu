@@ -496,33 +496,37 @@ __device__ __noinline__ void store_unit_rows_staged(uint32_t tO, float l, bool v
     const bool staged = __all_sync(0xffffffffu, valid_row);
 #pragma unroll
     for (int c2 = 0; c2 < D / 64; ++c2) {
+        // 64 columns into registers first: the wait for the previous store's read
+        // (the other half's, just issued) overlaps the TMEM loads
+        uint4 v[2][4];
+#pragma unroll
+        for (int cc = 0; cc < 2; ++cc) {
+            uint32_t r[32];
+            tmem_ld32(tO + (2 * c2 + cc) * 32, r);
+            tmem_wait_ld();
+#pragma unroll
+            for (int x = 0; x < 4; ++x)
+                v[cc][x] = make_uint4(pack_bf16x2(__uint_as_float(r[8 * x + 0]) * inv_l, __uint_as_float(r[8 * x + 1]) * inv_l),
+                                      pack_bf16x2(__uint_as_float(r[8 * x + 2]) * inv_l, __uint_as_float(r[8 * x + 3]) * inv_l),
+                                      pack_bf16x2(__uint_as_float(r[8 * x + 4]) * inv_l, __uint_as_float(r[8 * x + 5]) * inv_l),
+                                      pack_bf16x2(__uint_as_float(r[8 * x + 6]) * inv_l, __uint_as_float(r[8 * x + 7]) * inv_l));
+        }
         if (staged) {
             if (lane == 0)
                 bulk_wait_group_read0();   // the warp's previous store has read the buffer
             __syncwarp();
-        }
 #pragma unroll
-        for (int cc = 0; cc < 2; ++cc) {
-            const int c = 2 * c2 + cc;
-            uint32_t r[32];
-            tmem_ld32(tO + c * 32, r);
-            tmem_wait_ld();
-            uint4 v[4];
-#pragma unroll
-            for (int x = 0; x < 4; ++x)
-                v[x] = make_uint4(pack_bf16x2(__uint_as_float(r[8 * x + 0]) * inv_l, __uint_as_float(r[8 * x + 1]) * inv_l),
-                                  pack_bf16x2(__uint_as_float(r[8 * x + 2]) * inv_l, __uint_as_float(r[8 * x + 3]) * inv_l),
-                                  pack_bf16x2(__uint_as_float(r[8 * x + 4]) * inv_l, __uint_as_float(r[8 * x + 5]) * inv_l),
-                                  pack_bf16x2(__uint_as_float(r[8 * x + 6]) * inv_l, __uint_as_float(r[8 * x + 7]) * inv_l));
-            if (staged) {
+            for (int cc = 0; cc < 2; ++cc)
 #pragma unroll
                 for (int x = 0; x < 4; ++x)
-                    *reinterpret_cast<uint4 *>(stg + lane * 128 + (((cc * 4 + x) ^ (lane & 7)) << 4)) = v[x];
-            } else if (valid_row) {
-                uint4 *dst = reinterpret_cast<uint4 *>(out + (t_row * num_q_heads + h) * D + c * 32);
+                    *reinterpret_cast<uint4 *>(stg + lane * 128 + (((cc * 4 + x) ^ (lane & 7)) << 4)) = v[cc][x];
+        } else if (valid_row) {
+#pragma unroll
+            for (int cc = 0; cc < 2; ++cc) {
+                uint4 *dst = reinterpret_cast<uint4 *>(out + (t_row * num_q_heads + h) * D + (2 * c2 + cc) * 32);
 #pragma unroll
                 for (int x = 0; x < 4; ++x)
-                    dst[x] = v[x];
+                    dst[x] = v[cc][x];
             }
         }
         if (staged) {
@@ -1278,36 +1282,40 @@ chunk_attn_kernel(const ChunkParams p, const __grid_constant__ CUtensorMap tm_q,
                 uint8_t *stg = smem + C::kStageOff + (wg * 4 + sub) * 4096;
 #pragma unroll
                 for (int c2 = 0; c2 < D / 64; ++c2) {
+                    // 64 columns into registers first: the wait for the previous
+                    // store's read (the other half's, just issued) overlaps the TMEM loads
+                    uint4 v[2][4];
+#pragma unroll
+                    for (int cc = 0; cc < 2; ++cc) {
+                        uint32_t r[32];
+                        tmem_ld32(tO + (2 * c2 + cc) * 32, r);
+                        tmem_wait_ld();
+#pragma unroll
+                        for (int x = 0; x < 4; ++x)
+                            v[cc][x] = make_uint4(pack_bf16x2(__uint_as_float(r[8 * x + 0]) * inv_l, __uint_as_float(r[8 * x + 1]) * inv_l),
+                                                  pack_bf16x2(__uint_as_float(r[8 * x + 2]) * inv_l, __uint_as_float(r[8 * x + 3]) * inv_l),
+                                                  pack_bf16x2(__uint_as_float(r[8 * x + 4]) * inv_l, __uint_as_float(r[8 * x + 5]) * inv_l),
+                                                  pack_bf16x2(__uint_as_float(r[8 * x + 6]) * inv_l, __uint_as_float(r[8 * x + 7]) * inv_l));
+                    }
                     if (staged) {
                         if (lane == 0)
                             bulk_wait_group_read0();   // the warp's previous store has read the buffer
                         __syncwarp();
-                    }
+                        // row `lane` at lane * 128 bytes, 16-byte chunk j at (j ^ (lane & 7)):
+                        // the map's 128-byte swizzle
 #pragma unroll
-                    for (int cc = 0; cc < 2; ++cc) {
-                        const int c = 2 * c2 + cc;
-                        uint32_t r[32];
-                        tmem_ld32(tO + c * 32, r);
-                        tmem_wait_ld();
-                        uint4 v[4];
-#pragma unroll
-                        for (int x = 0; x < 4; ++x)
-                            v[x] = make_uint4(pack_bf16x2(__uint_as_float(r[8 * x + 0]) * inv_l, __uint_as_float(r[8 * x + 1]) * inv_l),
-                                              pack_bf16x2(__uint_as_float(r[8 * x + 2]) * inv_l, __uint_as_float(r[8 * x + 3]) * inv_l),
-                                              pack_bf16x2(__uint_as_float(r[8 * x + 4]) * inv_l, __uint_as_float(r[8 * x + 5]) * inv_l),
-                                              pack_bf16x2(__uint_as_float(r[8 * x + 6]) * inv_l, __uint_as_float(r[8 * x + 7]) * inv_l));
-                        if (staged) {
-                            // row `lane` at lane * 128 bytes, 16-byte chunk j at (j ^ (lane & 7)):
-                            // the map's 128-byte swizzle
+                        for (int cc = 0; cc < 2; ++cc)
 #pragma unroll
                             for (int x = 0; x < 4; ++x)
-                                *reinterpret_cast<uint4 *>(stg + lane * 128 + (((cc * 4 + x) ^ (lane & 7)) << 4)) = v[x];
-                        } else if (valid_row) {
-                            uint4 *dst = reinterpret_cast<uint4 *>(
-                                reinterpret_cast<__nv_bfloat16 *>(p.out) + (t_row * p.num_q_heads + h) * D + c * 32);
+                                *reinterpret_cast<uint4 *>(stg + lane * 128 + (((cc * 4 + x) ^ (lane & 7)) << 4)) = v[cc][x];
+                    } else if (valid_row) {
+#pragma unroll
+                        for (int cc = 0; cc < 2; ++cc) {
+                            uint4 *dst = reinterpret_cast<uint4 *>(reinterpret_cast<__nv_bfloat16 *>(p.out) +
+                                                                   (t_row * p.num_q_heads + h) * D + (2 * c2 + cc) * 32);
 #pragma unroll
                             for (int x = 0; x < 4; ++x)
-                                dst[x] = v[x];
+                                dst[x] = v[cc][x];
                         }
                     }
                     if (staged) {
