@@ -10,8 +10,9 @@
 //   combine   merges the partial results of decode rows split along keys
 // The lists live in the caller's workspace; every kernel is persistent and reads
 // its item count from the workspace, so the host never needs the lengths. A
-// batch of one prefill request of at most about 4k tokens runs the chunk kernel
-// alone: its CTAs compute their own runs (same units and cuts as the plan).
+// batch of one prefill request of at most about 6.6k tokens (32/8 heads, 152
+// SMs) runs the chunk kernel alone: its CTAs compute their own runs (same units
+// and cuts as the plan).
 #pragma once
 
 #include <cuda_runtime.h>

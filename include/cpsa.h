@@ -135,8 +135,9 @@ size_t cpp_attn_workspace_min_bytes(int num_reqs, int64_t num_tokens, int num_q_
  * does not depend on timing.
  * max_kv_splits = 1 turns off both kinds of split.
  * A batch of one prefill request (num_reqs == 1, num_tokens >= 2) of at most
- * about 4k tokens (while every CTA's run fits 56 pieces) launches the chunk
- * kernel alone: its CTAs compute their own runs, with the same units and cuts.
+ * about 6.6k tokens at 32/8 heads (while every CTA's run fits 56 pieces)
+ * launches the chunk kernel alone: its CTAs compute their own runs, with the
+ * same units and cuts.
  * workspace: device memory of at least cpp_attn_workspace_min_bytes(...) with
  * the same (num_reqs, num_tokens, heads, head_dim, max_kv_splits); it is
  * scratch, overwritten by each call; calls that share it must be stream-ordered.
