@@ -65,12 +65,15 @@ class AttentionStep:
         return self.last_split
 
     def run_two_stream(self, q, k, v, slot_mapping, k_cache, v_cache, query_lens, seq_lens, block_table, out,
-                       scale: float = 0.0, stream=None):
-        """Split the batch and run the two micro-batches on two streams (one stream when refused)."""
+                       scale: float = 0.0, stream=None, split=None):
+        """Split the batch and run the two micro-batches on two streams (one stream when refused).
+        split: (batch_split, token_split, use_two) of this batch when already known (from split()
+        on the same query_lens: it depends on the lengths alone), else computed here, which reads
+        the split kernel's result back to the host."""
         if self.streams is None:
             raise _lib.CpsaError("AttentionStep was built without two_stream=True")
         main = stream if stream is not None else torch.cuda.current_stream()
-        b, t, use = self.split(query_lens, stream=main)
+        b, t, use = self.split(query_lens, stream=main) if split is None else split
         if not use:
             self.run(q, k, v, slot_mapping, k_cache, v_cache, query_lens, seq_lens, block_table, out,
                      scale=scale, stream=main)

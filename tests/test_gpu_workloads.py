@@ -221,6 +221,13 @@ def test_two_streams_match_oracle(cuda_lib, fused):
             atol=1e-2, rtol_f=2e-3, what="two streams vs one")
     n_dec = 128
     assert torch.equal(out1[:n_dec].view(torch.int16), out2[:n_dec].view(torch.int16))
+    # the same run with the split passed in (computed once per batch): identical bits
+    out3 = torch.full_like(d["q"], float("nan"))
+    assert step.run_two_stream(d["q"], d["k"], d["v"], d["slot_mapping"], d["k_cache"], d["v_cache"],
+                               d["query_lens"], d["seq_lens"], d["block_table"], out3, split=step.last_split)
+    torch.cuda.synchronize()
+    assert step.read_errors() == 0
+    assert torch.equal(out3.view(torch.int16), out2.view(torch.int16))
 
 
 def test_gpu_chunk_invariance(cuda_lib):
