@@ -696,32 +696,51 @@ def suite(dev):
     d = W.device_batch(spec, device=dev)
     B, T = len(spec.qlen), sum(spec.qlen)
     step = cpsa.AttentionStep(B, T, HQ, HKV, D, max_kv_splits=8, two_stream=True, device=dev)
+    step_f = cpsa.AttentionStep(B, T, HQ, HKV, D, max_kv_splits=8, two_stream=True, device=dev,
+                                fused_kv_write=True)
     o = torch.empty_like(d["q"])
     args = (d["q"], d["k"], d["v"], d["slot_mapping"], d["k_cache"], d["v_cache"], d["query_lens"],
             d["seq_lens"], d["block_table"], o)
-    def wall(fn, reps=5):
-        ts = []
+
+    def timed(fn, reps=5):
+        """Median of (device ms between CUDA events on the calling stream, host wall
+        ms around the same call, both synchronised). Both micro-batches' streams
+        join the calling stream before its end event. The inputs (1.4 GB of q
+        alone) exceed L2, so nothing is flushed between repetitions."""
+        cur = torch.cuda.current_stream()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        dv, hw = [], []
         for r in range(reps + 2):
             torch.cuda.synchronize()
             t0 = time.perf_counter()
+            e0.record(cur)
             fn()
+            e1.record(cur)
             torch.cuda.synchronize()
             if r >= 2:
-                ts.append(1e3 * (time.perf_counter() - t0))
-        return float(np.median(ts))
-    one = wall(lambda: step.run(*args))
+                hw.append(1e3 * (time.perf_counter() - t0))
+                dv.append(e0.elapsed_time(e1))
+        return float(np.median(dv)), float(np.median(hw))
+    one, one_wall = timed(lambda: step.run(*args))
+    one_f, one_f_wall = timed(lambda: step_f.run(*args))
     # the split depends on the batch's lengths alone: the split kernel runs once
     # per batch, its result read back before the timed steps
     split = step.split(d["query_lens"])
-    two = wall(lambda: step.run_two_stream(*args, split=split))
-    two_with_split = wall(lambda: step.run_two_stream(*args))
+    two, two_wall = timed(lambda: step.run_two_stream(*args, split=split))
+    two_f, _ = timed(lambda: step_f.run_two_stream(*args, split=split))
+    two_with_split, _ = timed(lambda: step.run_two_stream(*args))
     pf = sum(4.0 * D * HQ * (q * h + q * (q + 1) // 2) for q, h in zip(spec.qlen, spec.hist) if q > 1)
+    tf = lambda ms: pf / (ms * 1e-3) / 1e12
     out["microbatch_two_streams"] = {
-        "workload": "128 decode rows (context U[2600,5200]) + 64 prompts of 2600 tokens, page 16",
-        "split": list(step.last_split), "one_stream_ms": one, "two_streams_ms": two,
-        "two_vs_one": two / one, "two_streams_with_split_readback_ms": two_with_split, "prefill_tflops_one_stream": pf / (one * 1e-3) / 1e12,
-        "tokens_per_s_one_stream": T / (one * 1e-3), "device_flags": step.read_errors()}
-    del d, step, o
+        "workload": "128 decode rows (context U[2600,5200]) + 64 prompts of 2600 tokens, page 16; "
+                    "device time between CUDA events on the calling stream (host wall time beside it)",
+        "split": list(step.last_split), "one_stream_ms": one, "two_streams_ms": two, "two_vs_one": two / one,
+        "two_streams_with_split_readback_ms": two_with_split, "prefill_tflops_one_stream": tf(one),
+        "fused_kv_write": {"one_stream_ms": one_f, "two_streams_ms": two_f, "two_vs_one": two_f / one_f,
+                           "prefill_tflops_one_stream": tf(one_f)},
+        "host_wall_ms": {"one_stream": one_wall, "two_streams": two_wall, "one_stream_fused": one_f_wall},
+        "tokens_per_s_one_stream": T / (one * 1e-3), "device_flags": step.read_errors() | step_f.read_errors()}
+    del d, step, step_f, o
     torch.cuda.empty_cache()
     return out
 
@@ -1050,6 +1069,8 @@ def summary_of(line):
     if "two_vs_one" in mb:
         out["microbatch_two_vs_one"] = round(mb["two_vs_one"], 4)
         out["microbatch_prefill_tflops_one_stream"] = round(mb["prefill_tflops_one_stream"], 1)
+        out["microbatch_prefill_tflops_one_stream_fused_kv_write"] = round(
+            mb["fused_kv_write"]["prefill_tflops_one_stream"], 1)
     sl = su.get("serving_loop", {}).get("budget_only", {})
     if "graph_replay_ms" in sl:
         out["serving_loop_ms_per_call_events"] = sl["device_ms"]
