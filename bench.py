@@ -691,7 +691,16 @@ def suite(dev):
         "progressive_2048_1024_512": serving_loop(dev, chunk_caps=(2048, 1024, 512)),
         "budget_tile_128": serving_loop(dev, tile_align=128),
         "budget_only_fused_kv_write": serving_loop(dev, fused=True)}
-    # --- micro-batch workload: one stream vs the balanced split on two streams
+    out["microbatch_two_streams"] = microbatch(dev)
+    return out
+
+
+def microbatch(dev, reps=5):
+    """The micro-batch workload on one stream and on two (the balanced split), as
+    two calls and with the KV write fused."""
+    import torch
+    import chunked_prefill_paged_slot_gb300 as cpsa
+    import workloads as W
     spec = W.spec_microbatch()
     d = W.device_batch(spec, device=dev)
     B, T = len(spec.qlen), sum(spec.qlen)
@@ -702,7 +711,7 @@ def suite(dev):
     args = (d["q"], d["k"], d["v"], d["slot_mapping"], d["k_cache"], d["v_cache"], d["query_lens"],
             d["seq_lens"], d["block_table"], o)
 
-    def timed(fn, reps=5):
+    def timed(fn):
         """Median of (device ms between CUDA events on the calling stream, host wall
         ms around the same call, both synchronised). Both micro-batches' streams
         join the calling stream before its end event. The inputs (1.4 GB of q
@@ -731,7 +740,7 @@ def suite(dev):
     two_with_split, _ = timed(lambda: step.run_two_stream(*args))
     pf = sum(4.0 * D * HQ * (q * h + q * (q + 1) // 2) for q, h in zip(spec.qlen, spec.hist) if q > 1)
     tf = lambda ms: pf / (ms * 1e-3) / 1e12
-    out["microbatch_two_streams"] = {
+    res = {
         "workload": "128 decode rows (context U[2600,5200]) + 64 prompts of 2600 tokens, page 16; "
                     "device time between CUDA events on the calling stream (host wall time beside it)",
         "split": list(step.last_split), "one_stream_ms": one, "two_streams_ms": two, "two_vs_one": two / one,
@@ -742,7 +751,7 @@ def suite(dev):
         "tokens_per_s_one_stream": T / (one * 1e-3), "device_flags": step.read_errors() | step_f.read_errors()}
     del d, step, step_f, o
     torch.cuda.empty_cache()
-    return out
+    return res
 
 
 # ----------------------------------------------------------------------------- replicas
@@ -787,7 +796,16 @@ def main():
                          "timed beside it as eager_step)")
     ap.add_argument("--profile-kv-write", action="store_true",
                     help="only the KV-write bandwidth measurement (T = 512 at page 128, T = 166528 at page 16)")
+    ap.add_argument("--profile-microbatch", action="store_true",
+                    help="only the micro-batch workload (one and two streams, two calls and fused), each variant "
+                         "run three times (one timed), for a launch list of its kernels")
     args = ap.parse_args()
+    if args.profile_microbatch:
+        import torch
+        dev = torch.device("cuda", 0)
+        torch.cuda.set_device(dev)
+        print(json.dumps(microbatch(dev, reps=1)), flush=True)
+        return 0
     if args.profile_kv_write:
         import torch
         dev = torch.device("cuda", 0)

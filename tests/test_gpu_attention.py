@@ -208,6 +208,26 @@ def test_short_histories_keep_units_whole(cuda_lib, fused):
         compare(got, ref, what=f"whole units {hist}")
 
 
+@pytest.mark.parametrize("fused", [False, True])
+def test_few_long_requests_take_the_block_plan(cuda_lib, fused):
+    """At most 32 requests but more than 8192 tokens also take the block-wide plan
+    kernel (a warp per request): three prompts and a decode row, 8301 tokens,
+    sampled rows of every request (its first and last rows, tile edges) against
+    the oracle."""
+    spec = W.BatchSpec(hist=[0, 1000, 3000, 500], qlen=[3000, 2600, 1, 2700], num_q_heads=32, num_kv_heads=8,
+                       head_dim=128, page_size=16, seed=540 + int(fused))
+    b = W.make_batch(spec)
+    got, flags, _, _ = (run_gpu_batch_fused if fused else run_gpu_batch)(cuda_lib, b)
+    assert flags == 0, f"device flags {flags:#x}"
+    starts = np.concatenate([[0], np.cumsum(spec.qlen)])
+    rng = np.random.default_rng(541)
+    rows = [0, 127, 128, 2999, 3000, 3127, 3128, 5599, 5600, 5601, 5728, 8300]
+    rows = np.unique(np.concatenate([rows, rng.choice(int(starts[-1]), 40, replace=False)]))
+    kc, vc = oracle_caches(b)
+    ref = oracle.paged_attention(b.q, kc, vc, b.query_lens, b.seq_lens, b.block_table, rows=rows)
+    compare(got[rows], ref, what="few long requests" + (" fused" if fused else ""))
+
+
 def test_whole_units_in_the_block_plan(cuda_lib):
     """More than 32 requests take the block-wide plan kernel; 40 requests of 128
     rows at history 1024 (one kv head, one q-head pair) give 40 units of 9 tiles
