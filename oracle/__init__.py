@@ -14,6 +14,7 @@ Parity status of each function (what pins it) is listed in each module's header.
 """
 from __future__ import annotations
 
+import contextlib
 import ctypes
 import os
 import subprocess
@@ -36,23 +37,41 @@ def build(force: bool = False) -> str:
     return _LIB
 
 
+def _open(path):
+    lib = ctypes.CDLL(path)
+    P = ctypes.c_void_p
+    lib.oracle_kv_cache_write.restype = ctypes.c_long
+    lib.oracle_kv_cache_write.argtypes = [P, P, P, ctypes.c_long, ctypes.c_int, ctypes.c_int,
+                                          ctypes.c_int, ctypes.c_long, P, P]
+    lib.oracle_paged_attention.restype = ctypes.c_int
+    lib.oracle_paged_attention.argtypes = [P, P, P, P, P, P, ctypes.c_int, ctypes.c_int,
+                                           ctypes.c_long, ctypes.c_int, ctypes.c_int,
+                                           ctypes.c_int, ctypes.c_int, ctypes.c_long,
+                                           ctypes.c_double, P, ctypes.c_long, P]
+    lib.oracle_num_threads.restype = ctypes.c_int
+    return lib
+
+
 def _load():
     global _lib
     if _lib is None:
         build()
-        lib = ctypes.CDLL(_LIB)
-        P = ctypes.c_void_p
-        lib.oracle_kv_cache_write.restype = ctypes.c_long
-        lib.oracle_kv_cache_write.argtypes = [P, P, P, ctypes.c_long, ctypes.c_int, ctypes.c_int,
-                                              ctypes.c_int, ctypes.c_long, P, P]
-        lib.oracle_paged_attention.restype = ctypes.c_int
-        lib.oracle_paged_attention.argtypes = [P, P, P, P, P, P, ctypes.c_int, ctypes.c_int,
-                                               ctypes.c_long, ctypes.c_int, ctypes.c_int,
-                                               ctypes.c_int, ctypes.c_int, ctypes.c_long,
-                                               ctypes.c_double, P, ctypes.c_long, P]
-        lib.oracle_num_threads.restype = ctypes.c_int
-        _lib = lib
+        _lib = _open(_LIB)
     return _lib
+
+
+@contextlib.contextmanager
+def using_library(path):
+    """Route the oracle's C calls to another build of attention.c while the
+    block runs (the mutation test builds copies with planted slips and checks
+    that some pin catches each one)."""
+    global _lib
+    saved = _lib
+    _lib = _open(path)
+    try:
+        yield
+    finally:
+        _lib = saved
 
 
 def _ptr(a):

@@ -5,7 +5,7 @@ the oracle fails at least one of them:
   scale (1/sqrt(d))            -> hand 2x2 example
   causal offset / off-by-one   -> hand 2x2 example, chunk invariance, history case
   page gather (page vs offset) -> hand example (block_table [1, 0]), page relabelling
-  GQA head mapping             -> per-kv-head constant values
+  GQA head mapping             -> per-kv-head constant values; GQA = MHA with repeated kv heads
   softmax normalisation        -> one-hot values (probabilities sum to 1), constant V
   max subtraction / overflow   -> huge scores reduce to the argmax key's value
   KV write layout              -> hand-placed slots, sentinel bytes untouched
@@ -107,6 +107,22 @@ def test_gqa_head_mapping_by_group():
     out, _, _ = build_cache_and_run(b)
     for h in range(8):
         assert np.allclose(out[:, h, :], h // 4 + 1.0, atol=1e-13, rtol=0)
+
+
+def test_gqa_equals_mha_with_each_kv_head_repeated_for_its_group():
+    # grouped-query attention is multi-head attention whose kv head h is the
+    # grouped kv head h // g: the same rows, bit for bit, with every q head
+    # scoring its own query row (random K/V, so no head is interchangeable)
+    spec = W.BatchSpec(hist=[5, 0, 9], qlen=[7, 3, 1], num_q_heads=6, num_kv_heads=2, head_dim=8,
+                       page_size=4, seed=17)
+    b = W.make_batch(spec)
+    out_gqa, kc, vc = build_cache_and_run(b)
+    kc_mha = np.ascontiguousarray(np.repeat(kc, 3, axis=1))
+    vc_mha = np.ascontiguousarray(np.repeat(vc, 3, axis=1))
+    out_mha = oracle.paged_attention(b.q, kc_mha, vc_mha, b.query_lens, b.seq_lens, b.block_table)
+    assert np.array_equal(out_gqa, out_mha)
+    # and the heads of one group do differ (each reads its own query row)
+    assert not np.allclose(out_gqa[:, 0, :], out_gqa[:, 1, :])
 
 
 def test_one_hot_values_give_probabilities_that_sum_to_one():

@@ -28,15 +28,24 @@ def test_cycle_hand_case():
     # B has 277 left: A decodes, B finishes its prompt, C starts with the remaining 234
     assert (b3["req_ids"], b3["query_lens"], b3["seq_lens"]) == (["A", "B", "C"], [1, 277, 100], [302, 1000, 100])
     assert s.finished == 1        # B: prompt done, no decode rows asked
+    for b in (b1, b2, b3):
+        check_invariants(b, 512, 16, None)
+    # pages: A holds ceil(302 / 16) = 19, C ceil(100 / 16) = 7; B's 63 came back
+    assert len(s.free) == 256 - 19 - 7
+    # the pages of a step's first request start the free list, in order
+    assert b1["block_table"][0] == list(range(19)) and b1["slot_mapping"][:3] == [0, 1, 2]
 
 
 def test_progressive_caps_and_tile_alignment():
     s = oracle.Scheduler(4096, 128, 1000, chunk_caps=[2048, 1024, 512])
     s.add_request(0, 8000, 0)
     sizes = []
-    while s.waiting or s.running:
+    for _ in range(64):                     # 8000 tokens take 14 steps; bounded all the same
+        if not (s.waiting or s.running):
+            break
         sizes += s.step()["query_lens"]
         s.commit()
+    assert not (s.waiting or s.running)
     assert sizes[:3] == [2048, 1024, 512] and set(sizes[3:-1]) == {512} and sum(sizes) == 8000
     # tile alignment: three decode rows leave 2045 tokens, rounded down to 1920
     s = oracle.Scheduler(2048, 16, 4096, tile_align=128)
@@ -46,6 +55,10 @@ def test_progressive_caps_and_tile_alignment():
     s.step(); s.commit()          # the three 16-token prompts and 2000 of the long one (not last: 1920)
     b = s.step()
     assert b["query_lens"][:3] == [1, 1, 1] and b["query_lens"][3] == 1920
+    s.commit()
+    # its last chunk is whatever remains, 5000 - 2 x 1920 = 1160, not rounded to the tile
+    b = s.step()
+    assert b["req_ids"][3] == 9 and b["query_lens"][3] == 1160
 
 
 def check_invariants(batch, budget, P, live_pages):
