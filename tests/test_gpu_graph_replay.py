@@ -76,6 +76,8 @@ CASES = {
     "self_planned_split": dict(hist=[9000], qlen=[512]),
     # several requests and decode rows: plan kernel, split decode rows (combine kernel)
     "planned_mixed": dict(hist=[6000, 0, 9000, 5000, 300], qlen=[384, 200, 1, 1, 1]),
+    # more than 32 requests: the block-wide plan kernel
+    "block_planned": dict(hist=[0, 0, 700] + [1000] * 30, qlen=[300, 300, 200] + [1] * 30),
 }
 
 
